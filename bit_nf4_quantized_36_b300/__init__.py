@@ -1,0 +1,209 @@
+"""libqlora binding: the QLoRA NF4 frozen-base linear layer on B300.
+
+Thin marshalling over the C ABI (include/qlora.h): torch is used for device memory and the
+current CUDA stream only; every step of the layer runs in libqlora's CUDA kernels.  There is
+no CPU or PyTorch fallback -- a missing library raises.
+
+    q = nf4_quantize(W_fp32_cuda)                       # NF4 codes + double-quantized scales
+    W_hat = nf4_dequantize(q)                           # bf16 [N, K]
+    Y, U = qlora_linear_fwd(q, X, A, B, alpha)          # Y = X W^T + (alpha/r) X A^T B^T
+    dX, dA, dB = qlora_linear_bwd(q, X, A, B, alpha, dY, U)
+"""
+from __future__ import annotations
+
+import ctypes
+from dataclasses import dataclass
+
+import torch
+
+from . import _lib
+
+__all__ = ["NF4Weight", "QLoRAError", "nf4_quantize", "nf4_dequantize", "qlora_linear_fwd", "qlora_linear_bwd",
+           "nf4_storage_bytes", "quantize_workspace_bytes", "fwd_workspace_bytes", "bwd_workspace_bytes",
+           "check_device_error", "launch_count", "nf4_levels", "empty_nf4"]
+
+
+class QLoRAError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        name = _lib.QLORA_STATUS.get(status, str(status))
+        super().__init__(f"{what}: {name} ({_lib.load().qlora_status_string(status).decode()})")
+        self.status = status
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        raise QLoRAError(status, what)
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _need(t: torch.Tensor, dtype, name: str, shape=None):
+    if not isinstance(t, torch.Tensor) or t.dtype != dtype or not t.is_cuda or not t.is_contiguous():
+        raise TypeError(f"{name} must be a contiguous CUDA tensor of dtype {dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+@dataclass
+class NF4Weight:
+    """One NF4 matrix [rows, cols] with double-quantized block scales (device tensors)."""
+    rows: int
+    cols: int
+    codes: torch.Tensor         # uint8 [rows*cols/2]
+    scale_codes: torch.Tensor   # int8  [nb]
+    scale_scales: torch.Tensor  # fp32  [ng]
+    scale_offset: torch.Tensor  # fp32  [1]
+
+    def struct(self) -> _lib.NF4TensorStruct:
+        return _lib.NF4TensorStruct(self.rows, self.cols, self.codes.data_ptr(), self.scale_codes.data_ptr(),
+                                    self.scale_scales.data_ptr(), self.scale_offset.data_ptr())
+
+    @property
+    def nbytes(self) -> int:
+        return sum(t.numel() * t.element_size() for t in (self.codes, self.scale_codes, self.scale_scales,
+                                                           self.scale_offset))
+
+
+def nf4_storage_bytes(rows: int, cols: int) -> int:
+    return int(_lib.load().qlora_nf4_storage_bytes(rows, cols))
+
+
+def quantize_workspace_bytes(rows: int, cols: int) -> int:
+    return int(_lib.load().qlora_quantize_workspace_bytes(rows, cols))
+
+
+def fwd_workspace_bytes(M: int, N: int, K: int, r: int) -> int:
+    return int(_lib.load().qlora_fwd_workspace_bytes(M, N, K, r))
+
+
+def bwd_workspace_bytes(M: int, N: int, K: int, r: int) -> int:
+    return int(_lib.load().qlora_bwd_workspace_bytes(M, N, K, r))
+
+
+def launch_count() -> int:
+    return int(_lib.load().qlora_launch_count())
+
+
+def nf4_levels() -> torch.Tensor:
+    out = (ctypes.c_float * 16)()
+    _lib.load().qlora_nf4_levels(ctypes.cast(out, ctypes.c_void_p))
+    return torch.tensor(list(out), dtype=torch.float32)
+
+
+def empty_nf4(rows: int, cols: int, device="cuda") -> NF4Weight:
+    n = rows * cols
+    nb = n // 64
+    ng = (nb + 255) // 256
+    return NF4Weight(rows, cols, torch.empty(n // 2, dtype=torch.uint8, device=device),
+                     torch.empty(nb, dtype=torch.int8, device=device),
+                     torch.empty(ng, dtype=torch.float32, device=device),
+                     torch.empty(1, dtype=torch.float32, device=device))
+
+
+def _workspace(nbytes: int, ws, device):
+    if ws is not None:
+        return ws
+    return torch.empty(max(nbytes, 16), dtype=torch.uint8, device=device)
+
+
+def nf4_quantize(W: torch.Tensor, out: NF4Weight | None = None, workspace: torch.Tensor | None = None,
+                 stream=None) -> NF4Weight:
+    """NF4-quantize fp32 W [N, K] (K % 64 == 0) with double-quantized scales."""
+    _need(W, torch.float32, "W")
+    rows, cols = W.shape
+    if out is None:
+        out = empty_nf4(rows, cols, W.device)
+    L = _lib.load()
+    need = int(L.qlora_quantize_workspace_bytes(rows, cols))
+    if need == ctypes.c_size_t(-1).value:
+        raise QLoRAError(2, "nf4_quantize")
+    ws = _workspace(need, workspace, W.device)
+    st = out.struct()
+    _check(L.nf4_quantize(_ptr(W), ctypes.byref(st), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
+           "nf4_quantize")
+    return out
+
+
+def nf4_dequantize(q: NF4Weight, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """bf16 W^ [rows, cols] = bf16(NF4[c] * s'_b)."""
+    if out is None:
+        out = torch.empty((q.rows, q.cols), dtype=torch.bfloat16, device=q.codes.device)
+    _need(out, torch.bfloat16, "out", (q.rows, q.cols))
+    st = q.struct()
+    _check(_lib.load().nf4_dequantize(ctypes.byref(st), _ptr(out), _stream(stream)), "nf4_dequantize")
+    return out
+
+
+def qlora_linear_fwd(q: NF4Weight, X: torch.Tensor, A: torch.Tensor, B: torch.Tensor, alpha: float,
+                     Y: torch.Tensor | None = None, U_save: torch.Tensor | None = None, save_u: bool = True,
+                     workspace: torch.Tensor | None = None, stream=None):
+    """Y = X W^T + (alpha/r) (X A^T) B^T.  Returns (Y, U) with U = bf16((alpha/r) X A^T) or None."""
+    M = X.shape[0]
+    r = A.shape[0]
+    _need(X, torch.bfloat16, "X", (M, q.cols))
+    _need(A, torch.bfloat16, "A", (r, q.cols))
+    _need(B, torch.bfloat16, "B", (q.rows, r))
+    dev = X.device
+    if Y is None:
+        Y = torch.empty((M, q.rows), dtype=torch.bfloat16, device=dev)
+    _need(Y, torch.bfloat16, "Y", (M, q.rows))
+    if U_save is None and save_u:
+        U_save = torch.empty((M, r), dtype=torch.bfloat16, device=dev)
+    if U_save is not None:
+        _need(U_save, torch.bfloat16, "U_save", (M, r))
+    L = _lib.load()
+    need = int(L.qlora_fwd_workspace_bytes(M, q.rows, q.cols, r))
+    if need == ctypes.c_size_t(-1).value:
+        raise QLoRAError(2, "qlora_linear_fwd")
+    ws = _workspace(need, workspace, dev)
+    st = q.struct()
+    _check(L.qlora_linear_fwd(ctypes.byref(st), _ptr(X), M, _ptr(A), _ptr(B), r, float(alpha), _ptr(Y),
+                              _ptr(U_save), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
+           "qlora_linear_fwd")
+    return Y, U_save
+
+
+def qlora_linear_bwd(q: NF4Weight, X: torch.Tensor, A: torch.Tensor, B: torch.Tensor, alpha: float,
+                     dY: torch.Tensor, U_saved: torch.Tensor | None = None, dX: torch.Tensor | None = None,
+                     dA: torch.Tensor | None = None, dB: torch.Tensor | None = None,
+                     workspace: torch.Tensor | None = None, stream=None):
+    """Returns (dX bf16 [M, K], dA fp32 [r, K], dB fp32 [N, r])."""
+    M = X.shape[0]
+    r = A.shape[0]
+    N, K = q.rows, q.cols
+    _need(X, torch.bfloat16, "X", (M, K))
+    _need(A, torch.bfloat16, "A", (r, K))
+    _need(B, torch.bfloat16, "B", (N, r))
+    _need(dY, torch.bfloat16, "dY", (M, N))
+    if U_saved is not None:
+        _need(U_saved, torch.bfloat16, "U_saved", (M, r))
+    dev = X.device
+    dX = torch.empty((M, K), dtype=torch.bfloat16, device=dev) if dX is None else dX
+    dA = torch.empty((r, K), dtype=torch.float32, device=dev) if dA is None else dA
+    dB = torch.empty((N, r), dtype=torch.float32, device=dev) if dB is None else dB
+    _need(dX, torch.bfloat16, "dX", (M, K))
+    _need(dA, torch.float32, "dA", (r, K))
+    _need(dB, torch.float32, "dB", (N, r))
+    L = _lib.load()
+    need = int(L.qlora_bwd_workspace_bytes(M, N, K, r))
+    if need == ctypes.c_size_t(-1).value:
+        raise QLoRAError(2, "qlora_linear_bwd")
+    ws = _workspace(need, workspace, dev)
+    st = q.struct()
+    _check(L.qlora_linear_bwd(ctypes.byref(st), _ptr(X), M, _ptr(A), _ptr(B), r, float(alpha), _ptr(dY),
+                              _ptr(U_saved), _ptr(dX), _ptr(dA), _ptr(dB), _ptr(ws), ws.numel() * ws.element_size(),
+                              _stream(stream)),
+           "qlora_linear_bwd")
+    return dX, dA, dB
+
+
+def check_device_error(stream=None) -> None:
+    _check(_lib.load().qlora_check_device_error(_stream(stream)), "device error word")

@@ -1,0 +1,61 @@
+"""ctypes loader for libqlora.so: declares the C ABI of include/qlora.h.  No fallback: if the
+library is missing or cannot be loaded, every call raises."""
+from __future__ import annotations
+
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libqlora.so")
+
+QLORA_STATUS = {
+    0: "QLORA_OK", 1: "QLORA_ERR_INVALID_ARG", 2: "QLORA_ERR_UNSUPPORTED_SHAPE", 3: "QLORA_ERR_MISALIGNED",
+    4: "QLORA_ERR_WORKSPACE", 5: "QLORA_ERR_CUDA", 6: "QLORA_ERR_TIMEOUT",
+}
+
+# every function declared in include/qlora.h
+EXPORTS = (
+    "qlora_nf4_storage_bytes", "qlora_quantize_workspace_bytes", "qlora_fwd_workspace_bytes",
+    "qlora_bwd_workspace_bytes", "nf4_quantize", "nf4_dequantize", "qlora_linear_fwd", "qlora_linear_bwd",
+    "qlora_check_device_error", "qlora_status_string", "qlora_launch_count", "qlora_nf4_levels",
+)
+
+
+class NF4TensorStruct(ctypes.Structure):
+    _fields_ = [("rows", ctypes.c_int64), ("cols", ctypes.c_int64), ("codes", ctypes.c_void_p),
+                ("scale_codes", ctypes.c_void_p), ("scale_scales", ctypes.c_void_p),
+                ("scale_offset", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libqlora.so is not built ({LIB_PATH}); run __graft_entry__.build()")
+    L = ctypes.CDLL(LIB_PATH)
+    P, I64, I32, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t
+    ST = ctypes.POINTER(NF4TensorStruct)
+    sig = {
+        "qlora_nf4_storage_bytes": (SZ, [I64, I64]),
+        "qlora_quantize_workspace_bytes": (SZ, [I64, I64]),
+        "qlora_fwd_workspace_bytes": (SZ, [I64, I64, I64, I32]),
+        "qlora_bwd_workspace_bytes": (SZ, [I64, I64, I64, I32]),
+        "nf4_quantize": (ctypes.c_int, [P, ST, P, SZ, P]),
+        "nf4_dequantize": (ctypes.c_int, [ST, P, P]),
+        "qlora_linear_fwd": (ctypes.c_int, [ST, P, I64, P, P, I32, ctypes.c_float, P, P, P, SZ, P]),
+        "qlora_linear_bwd": (ctypes.c_int, [ST, P, I64, P, P, I32, ctypes.c_float, P, P, P, P, P, P, SZ, P]),
+        "qlora_check_device_error": (ctypes.c_int, [P]),
+        "qlora_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+        "qlora_launch_count": (ctypes.c_uint64, []),
+        "qlora_nf4_levels": (None, [P]),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(L, name)
+        f.restype = res
+        f.argtypes = args
+    _lib = L
+    return L

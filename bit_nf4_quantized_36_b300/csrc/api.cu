@@ -1,0 +1,420 @@
+// api.cu -- the C ABI of libqlora (include/qlora.h): argument checks, workspace layout,
+// TMA descriptor setup and the launch sequence of each call.  All arithmetic of the layer runs
+// in the kernels of quant.cu and gemm.cu.
+#include <atomic>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "../../include/qlora.h"
+#include "qlora_common.cuh"
+#include "qlora_kernels.cuh"
+
+namespace qlora {
+
+static std::atomic<uint64_t> g_launches{0};
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+// ---------------------------------------------------------------------------------------
+// NF4 tables: the level constants and the exact decision thresholds of the nearest-level
+// rule.  thr[k] is the smallest fp32 x in (L_k, L_k+1] with fl(L_k+1 - x) < fl(x - L_k):
+// the predicate is monotone in x (fp32 subtraction is monotone), false at L_k and true at
+// L_k+1, so a bisection over the ordered fp32 bit patterns finds it exactly.
+// ---------------------------------------------------------------------------------------
+static int64_t f32_key(float f) {
+    uint32_t u;
+    std::memcpy(&u, &f, 4);
+    return (u & 0x80000000u) ? -(int64_t)(u & 0x7FFFFFFFu) : (int64_t)u;
+}
+static float f32_from_key(int64_t k) {
+    uint32_t u = k >= 0 ? (uint32_t)k : (0x80000000u | (uint32_t)(-k));
+    float f;
+    std::memcpy(&f, &u, 4);
+    return f;
+}
+static bool closer_to_upper(volatile float lo, volatile float hi, volatile float x) {
+    volatile float du = hi - x;  // fp32, round to nearest
+    volatile float dl = x - lo;
+    return du < dl;
+}
+
+static const NF4Tables &tables() {
+    static NF4Tables t;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        for (int i = 0; i < 16; ++i) std::memcpy(&t.level[i], &kNF4Bits[i], 4);
+        for (int k = 0; k < 15; ++k) {
+            const float lo = t.level[k], hi = t.level[k + 1];
+            int64_t a = f32_key(lo), b = f32_key(hi);  // predicate false at a, true at b
+            while (b - a > 1) {
+                const int64_t m = a + (b - a) / 2;
+                if (closer_to_upper(lo, hi, f32_from_key(m))) b = m; else a = m;
+            }
+            t.thr[k] = f32_from_key(b);
+        }
+        t.thr[15] = INFINITY;
+    });
+    return t;
+}
+
+static int num_sms_current() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return 148; }
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+        cudaGetLastError();
+        return 148;
+    }
+    return n;
+}
+
+// ---------------------------------------------------------------------------------------
+// TMA descriptors
+// ---------------------------------------------------------------------------------------
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+// 2-D row-major tensor [outer, inner] of `esize`-byte elements with row stride `ld` elements.
+static bool make_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int esize, uint64_t inner,
+                     uint64_t outer, uint64_t ld, uint32_t box_inner, uint32_t box_outer, bool swz128) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {ld * (uint64_t)esize};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, dt, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    swz128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+static bool map_bf16(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, uint32_t bi, uint32_t bo) {
+    return make_map(m, base, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, inner, outer, inner, bi, bo, true);
+}
+static bool map_codes(CUtensorMap *m, const void *codes, int64_t N, int64_t K, bool dx) {
+    return make_map(m, codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)K / 2, (uint64_t)N, (uint64_t)K / 2,
+                    dx ? 64u : 32u, dx ? 64u : 128u, false);
+}
+
+// ---------------------------------------------------------------------------------------
+// Workspace layouts (one function per call, used by the size query and by the call)
+// ---------------------------------------------------------------------------------------
+static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+struct QuantWs {
+    int64_t nb, ng, p2;
+    size_t off_absmax, off_tree, total;
+};
+static QuantWs quant_ws(int64_t rows, int64_t cols) {
+    QuantWs w{};
+    w.nb = rows * cols / kBlock;
+    w.ng = (w.nb + kGroup - 1) / kGroup;
+    w.p2 = 1;
+    while (w.p2 < w.ng) w.p2 <<= 1;
+    w.off_absmax = 0;
+    w.off_tree = align256((size_t)w.nb * 4);
+    w.total = w.off_tree + align256((size_t)w.p2 * 2 * sizeof(double));
+    return w;
+}
+
+struct LayerWs {
+    int r64;
+    FusedPlan fp;
+    ProjPlan pu, pv, pda, pdb;
+    size_t off_apad, off_bpad, off_u, off_v, off_proj, off_main, total;
+};
+static LayerWs layer_ws(int64_t M, int64_t N, int64_t K, int r, bool bwd, int num_sms) {
+    LayerWs w{};
+    w.r64 = ((r + 63) / 64) * 64;
+    size_t off = 0;
+    w.off_apad = off;
+    off += align256((size_t)w.r64 * K * 2);
+    w.off_bpad = off;
+    off += align256((size_t)N * w.r64 * 2);
+    w.off_u = off;
+    off += align256((size_t)M * w.r64 * 2);
+    w.pu = plan_proj(M, K, w.r64, num_sms);
+    size_t proj = w.pu.partial_bytes;
+    if (bwd) {
+        w.off_v = off;
+        off += align256((size_t)M * w.r64 * 2);
+        w.pv = plan_proj(M, N, w.r64, num_sms);
+        w.pda = plan_proj(K, M, w.r64, num_sms);
+        w.pdb = plan_proj(N, M, w.r64, num_sms);
+        proj = std::max(std::max(proj, w.pv.partial_bytes), std::max(w.pda.partial_bytes, w.pdb.partial_bytes));
+        w.fp = plan_fused(M, K, (N + 63) / 64, w.r64, num_sms);
+    } else {
+        w.fp = plan_fused(M, N, K / 64, w.r64, num_sms);
+    }
+    w.off_proj = off;
+    off += align256(proj);
+    w.off_main = off;
+    off += align256(w.fp.partial_bytes);
+    w.total = off;
+    return w;
+}
+
+static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static qlora_status check_tensor(const qlora_nf4_tensor *t) {
+    if (!t || !t->codes || !t->scale_codes || !t->scale_scales || !t->scale_offset) return QLORA_ERR_INVALID_ARG;
+    if (t->rows < 1 || t->cols < 64 || t->cols % 64 != 0) return QLORA_ERR_UNSUPPORTED_SHAPE;
+    if (t->rows > (1LL << 31) || t->cols > (1LL << 31)) return QLORA_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned16(t->codes)) return QLORA_ERR_MISALIGNED;
+    if ((reinterpret_cast<uintptr_t>(t->scale_scales) & 3u) || (reinterpret_cast<uintptr_t>(t->scale_offset) & 3u))
+        return QLORA_ERR_MISALIGNED;
+    return QLORA_OK;
+}
+
+static qlora_status from_cuda(cudaError_t e) { return e == cudaSuccess ? QLORA_OK : QLORA_ERR_CUDA; }
+
+static qlora_status check_layer_args(const qlora_nf4_tensor *W, const uint16_t *X, int64_t M, const uint16_t *A,
+                                     const uint16_t *B, int32_t r, float alpha) {
+    qlora_status s = check_tensor(W);
+    if (s != QLORA_OK) return s;
+    if (!X || !A || !B) return QLORA_ERR_INVALID_ARG;
+    if (r < 1 || r > 256 || !std::isfinite(alpha)) return QLORA_ERR_INVALID_ARG;
+    if (M < 1 || M > (1LL << 31) - 1) return QLORA_ERR_UNSUPPORTED_SHAPE;
+    if (W->rows % 8 != 0) return QLORA_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned16(X) || !aligned16(A) || !aligned16(B)) return QLORA_ERR_MISALIGNED;
+    return QLORA_OK;
+}
+
+}  // namespace qlora
+
+using namespace qlora;
+
+extern "C" {
+
+const char *qlora_status_string(qlora_status s) {
+    switch (s) {
+        case QLORA_OK: return "ok";
+        case QLORA_ERR_INVALID_ARG: return "invalid argument";
+        case QLORA_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+        case QLORA_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+        case QLORA_ERR_WORKSPACE: return "workspace missing or too small";
+        case QLORA_ERR_CUDA: return "CUDA error";
+        case QLORA_ERR_TIMEOUT: return "device-side wait timed out";
+    }
+    return "unknown status";
+}
+
+uint64_t qlora_launch_count(void) { return g_launches.load(); }
+
+void qlora_nf4_levels(float out[16]) {
+    if (!out) return;
+    for (int i = 0; i < 16; ++i) out[i] = tables().level[i];
+}
+
+size_t qlora_nf4_storage_bytes(int64_t rows, int64_t cols) {
+    if (rows < 1 || cols < 64 || cols % 64 != 0) return 0;
+    const int64_t n = rows * cols, nb = n / 64, ng = (nb + 255) / 256;
+    return (size_t)(n / 2 + nb + 4 * ng + 4);
+}
+
+size_t qlora_quantize_workspace_bytes(int64_t rows, int64_t cols) {
+    if (rows < 1 || cols < 64 || cols % 64 != 0) return (size_t)-1;
+    return quant_ws(rows, cols).total;
+}
+
+size_t qlora_fwd_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t r) {
+    if (M < 1 || N < 1 || N % 8 != 0 || K < 64 || K % 64 != 0 || r < 1 || r > 256) return (size_t)-1;
+    return layer_ws(M, N, K, r, false, num_sms_current()).total;
+}
+
+size_t qlora_bwd_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t r) {
+    if (M < 1 || N < 1 || N % 8 != 0 || K < 64 || K % 64 != 0 || r < 1 || r > 256) return (size_t)-1;
+    return layer_ws(M, N, K, r, true, num_sms_current()).total;
+}
+
+qlora_status nf4_quantize(const float *W, const qlora_nf4_tensor *out, void *ws, size_t ws_bytes, void *stream) {
+    if (!W) return QLORA_ERR_INVALID_ARG;
+    qlora_status s = check_tensor(out);
+    if (s != QLORA_OK) return s;
+    if (!aligned16(W)) return QLORA_ERR_MISALIGNED;
+    const QuantWs w = quant_ws(out->rows, out->cols);
+    if (!ws || ws_bytes < w.total || !aligned16(ws)) return QLORA_ERR_WORKSPACE;
+    uint8_t *base = static_cast<uint8_t *>(ws);
+    return from_cuda(launch_quantize(W, out->rows * out->cols, out->codes, out->scale_codes, out->scale_scales,
+                                     out->scale_offset, reinterpret_cast<float *>(base + w.off_absmax),
+                                     reinterpret_cast<double *>(base + w.off_tree), w.p2, tables(), num_sms_current(),
+                                     static_cast<cudaStream_t>(stream)));
+}
+
+qlora_status nf4_dequantize(const qlora_nf4_tensor *q, uint16_t *W_out, void *stream) {
+    qlora_status s = check_tensor(q);
+    if (s != QLORA_OK) return s;
+    if (!W_out) return QLORA_ERR_INVALID_ARG;
+    if (!aligned16(W_out)) return QLORA_ERR_MISALIGNED;
+    return from_cuda(launch_dequantize(q->codes, q->scale_codes, q->scale_scales, q->scale_offset, q->rows * q->cols,
+                                       W_out, tables(), num_sms_current(), static_cast<cudaStream_t>(stream)));
+}
+
+qlora_status qlora_linear_fwd(const qlora_nf4_tensor *W, const uint16_t *X, int64_t M, const uint16_t *A,
+                              const uint16_t *B, int32_t r, float alpha, uint16_t *Y, uint16_t *U_save, void *ws,
+                              size_t ws_bytes, void *stream) {
+    qlora_status s = check_layer_args(W, X, M, A, B, r, alpha);
+    if (s != QLORA_OK) return s;
+    if (!Y) return QLORA_ERR_INVALID_ARG;
+    if (!aligned16(Y) || (U_save && !aligned16(U_save))) return QLORA_ERR_MISALIGNED;
+    const int64_t N = W->rows, K = W->cols;
+    const int sms = num_sms_current();
+    const LayerWs w = layer_ws(M, N, K, r, false, sms);
+    if (!ws || ws_bytes < w.total || !aligned16(ws)) return QLORA_ERR_WORKSPACE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t *base = static_cast<uint8_t *>(ws);
+    uint16_t *Apad = reinterpret_cast<uint16_t *>(base + w.off_apad);
+    uint16_t *Bpad = reinterpret_cast<uint16_t *>(base + w.off_bpad);
+    uint16_t *U = reinterpret_cast<uint16_t *>(base + w.off_u);
+    float *proj = reinterpret_cast<float *>(base + w.off_proj);
+    float *mainp = reinterpret_cast<float *>(base + w.off_main);
+    const float scale = alpha / (float)r;
+
+    CUtensorMap mX_k, mA_k, mCodes, mX_act, mU_act;
+    if (!map_bf16(&mX_k, X, K, M, 64, 128) || !map_bf16(&mA_k, Apad, K, w.r64, 64, w.r64) ||
+        !map_codes(&mCodes, W->codes, N, K, false) || !map_bf16(&mX_act, X, K, M, 64, w.fp.BN) ||
+        !map_bf16(&mU_act, U, w.r64, M, 64, w.fp.BN))
+        return QLORA_ERR_CUDA;
+
+    cudaError_t e;
+    if ((e = launch_pad_2d(A, r, K, Apad, w.r64, K, sms, st)) != cudaSuccess) return from_cuda(e);
+    if ((e = launch_pad_2d(B, N, r, Bpad, N, w.r64, sms, st)) != cudaSuccess) return from_cuda(e);
+    // U = bf16(s * X A^T)
+    if ((e = launch_proj(false, false, mX_k, mA_k, M, K, w.r64, w.pu, proj, st)) != cudaSuccess) return from_cuda(e);
+    if ((e = launch_proj_finalize(0, proj, w.pu.splits, M, w.r64, r, scale, U, U_save, nullptr, sms, st)) != cudaSuccess)
+        return from_cuda(e);
+    // Y = X W^T + U Bp^T
+    FusedArgs fa{};
+    fa.scale_codes = W->scale_codes;
+    fa.scale_scales = W->scale_scales;
+    fa.scale_offset = W->scale_offset;
+    fa.N = N;
+    fa.K = K;
+    fa.KB = (int32_t)(K / 64);
+    fa.M = (int32_t)M;
+    fa.lora_rows = Bpad;
+    fa.r64 = w.r64;
+    fa.BN = w.fp.BN;
+    fa.w_tiles = w.fp.w_tiles;
+    fa.m_tiles = w.fp.m_tiles;
+    fa.splits = w.fp.splits;
+    fa.kt_main = w.fp.kt_main;
+    fa.kt_lora = w.fp.kt_lora;
+    fa.out = Y;
+    fa.partial = mainp;
+    fa.wdim = N;
+    fa.tab = tables();
+    if ((e = launch_fused(false, mCodes, mX_act, mU_act, fa, w.fp, st)) != cudaSuccess) return from_cuda(e);
+    if (w.fp.splits > 1 && (e = launch_splitk_reduce(mainp, w.fp.splits, M, N, Y, sms, st)) != cudaSuccess)
+        return from_cuda(e);
+    return QLORA_OK;
+}
+
+qlora_status qlora_linear_bwd(const qlora_nf4_tensor *W, const uint16_t *X, int64_t M, const uint16_t *A,
+                              const uint16_t *B, int32_t r, float alpha, const uint16_t *dY, const uint16_t *U_saved,
+                              uint16_t *dX, float *dA, float *dB, void *ws, size_t ws_bytes, void *stream) {
+    qlora_status s = check_layer_args(W, X, M, A, B, r, alpha);
+    if (s != QLORA_OK) return s;
+    if (!dY || !dX || !dA || !dB) return QLORA_ERR_INVALID_ARG;
+    if (!aligned16(dY) || !aligned16(dX) || !aligned16(dA) || !aligned16(dB) || (U_saved && !aligned16(U_saved)))
+        return QLORA_ERR_MISALIGNED;
+    const int64_t N = W->rows, K = W->cols;
+    const int sms = num_sms_current();
+    const LayerWs w = layer_ws(M, N, K, r, true, sms);
+    if (!ws || ws_bytes < w.total || !aligned16(ws)) return QLORA_ERR_WORKSPACE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t *base = static_cast<uint8_t *>(ws);
+    uint16_t *Apad = reinterpret_cast<uint16_t *>(base + w.off_apad);
+    uint16_t *Bpad = reinterpret_cast<uint16_t *>(base + w.off_bpad);
+    uint16_t *U = reinterpret_cast<uint16_t *>(base + w.off_u);
+    uint16_t *V = reinterpret_cast<uint16_t *>(base + w.off_v);
+    float *proj = reinterpret_cast<float *>(base + w.off_proj);
+    float *mainp = reinterpret_cast<float *>(base + w.off_main);
+    const float scale = alpha / (float)r;
+
+    CUtensorMap mX_k, mA_k, mG_k, mBpad_mn, mX_mn, mV_mn, mG_mn, mU_mn, mCodes, mG_act, mV_act;
+    if (!map_bf16(&mX_k, X, K, M, 64, 128) || !map_bf16(&mA_k, Apad, K, w.r64, 64, w.r64) ||
+        !map_bf16(&mG_k, dY, N, M, 64, 128) || !map_bf16(&mBpad_mn, Bpad, w.r64, N, 64, 64) ||
+        !map_bf16(&mX_mn, X, K, M, 64, 64) || !map_bf16(&mV_mn, V, w.r64, M, 64, 64) ||
+        !map_bf16(&mG_mn, dY, N, M, 64, 64) || !map_bf16(&mU_mn, U, w.r64, M, 64, 64) ||
+        !map_codes(&mCodes, W->codes, N, K, true) || !map_bf16(&mG_act, dY, N, M, 64, w.fp.BN) ||
+        !map_bf16(&mV_act, V, w.r64, M, 64, w.fp.BN))
+        return QLORA_ERR_CUDA;
+
+    cudaError_t e;
+    if ((e = launch_pad_2d(A, r, K, Apad, w.r64, K, sms, st)) != cudaSuccess) return from_cuda(e);
+    if ((e = launch_pad_2d(B, N, r, Bpad, N, w.r64, sms, st)) != cudaSuccess) return from_cuda(e);
+    // U: the forward's saved copy, or recomputed
+    if (U_saved) {
+        if ((e = launch_pad_2d(U_saved, M, r, U, M, w.r64, sms, st)) != cudaSuccess) return from_cuda(e);
+    } else {
+        if ((e = launch_proj(false, false, mX_k, mA_k, M, K, w.r64, w.pu, proj, st)) != cudaSuccess) return from_cuda(e);
+        if ((e = launch_proj_finalize(0, proj, w.pu.splits, M, w.r64, r, scale, U, nullptr, nullptr, sms, st)) !=
+            cudaSuccess)
+            return from_cuda(e);
+    }
+    // V = bf16(s * G B)
+    if ((e = launch_proj(false, true, mG_k, mBpad_mn, M, N, w.r64, w.pv, proj, st)) != cudaSuccess) return from_cuda(e);
+    if ((e = launch_proj_finalize(0, proj, w.pv.splits, M, w.r64, r, scale, V, nullptr, nullptr, sms, st)) !=
+        cudaSuccess)
+        return from_cuda(e);
+    // dX = G W^ + V Ap
+    FusedArgs fa{};
+    fa.scale_codes = W->scale_codes;
+    fa.scale_scales = W->scale_scales;
+    fa.scale_offset = W->scale_offset;
+    fa.N = N;
+    fa.K = K;
+    fa.KB = (int32_t)(K / 64);
+    fa.M = (int32_t)M;
+    fa.lora_rows = Apad;
+    fa.r64 = w.r64;
+    fa.BN = w.fp.BN;
+    fa.w_tiles = w.fp.w_tiles;
+    fa.m_tiles = w.fp.m_tiles;
+    fa.splits = w.fp.splits;
+    fa.kt_main = w.fp.kt_main;
+    fa.kt_lora = w.fp.kt_lora;
+    fa.out = dX;
+    fa.partial = mainp;
+    fa.wdim = K;
+    fa.tab = tables();
+    if ((e = launch_fused(true, mCodes, mG_act, mV_act, fa, w.fp, st)) != cudaSuccess) return from_cuda(e);
+    if (w.fp.splits > 1 && (e = launch_splitk_reduce(mainp, w.fp.splits, M, K, dX, sms, st)) != cudaSuccess)
+        return from_cuda(e);
+    // dA = V^T X  -> D[k, j] = sum_m X[m, k] V[m, j]
+    if ((e = launch_proj(true, true, mX_mn, mV_mn, K, M, w.r64, w.pda, proj, st)) != cudaSuccess) return from_cuda(e);
+    if ((e = launch_proj_finalize(1, proj, w.pda.splits, K, w.r64, r, 1.0f, nullptr, nullptr, dA, sms, st)) !=
+        cudaSuccess)
+        return from_cuda(e);
+    // dB = G^T U  -> D[n, j] = sum_m G[m, n] U[m, j]
+    if ((e = launch_proj(true, true, mG_mn, mU_mn, N, M, w.r64, w.pdb, proj, st)) != cudaSuccess) return from_cuda(e);
+    if ((e = launch_proj_finalize(2, proj, w.pdb.splits, N, w.r64, r, 1.0f, nullptr, nullptr, dB, sms, st)) !=
+        cudaSuccess)
+        return from_cuda(e);
+    return QLORA_OK;
+}
+
+qlora_status qlora_check_device_error(void *stream) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return QLORA_ERR_CUDA;
+    uint32_t word = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&word, g_error_word, sizeof(word)) != cudaSuccess) return QLORA_ERR_CUDA;
+    if (word && cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero)) != cudaSuccess) return QLORA_ERR_CUDA;
+    return (word & kErrTimeout) ? QLORA_ERR_TIMEOUT : QLORA_OK;
+}
+
+}  // extern "C"

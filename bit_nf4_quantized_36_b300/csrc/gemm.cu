@@ -1,0 +1,672 @@
+// gemm.cu -- tensor-core kernels of the QLoRA linear layer (sm_103a, tcgen05 + TMEM + TMA).
+//
+// 1. nf4_lora_gemm_kernel<dx>: the fused NF4-dequant GEMM.  The weight side is the MMA's
+//    128-row A operand ("swap-AB": weights are the M side, tokens the N side), so that each
+//    expanded weight is reused by up to 256 tokens.  TMA stages the packed nibbles and the
+//    activation tile; eight decode warps expand nibbles to bf16 through a per-block 16-entry
+//    register table (byte-permute lookups) straight into the 128-byte-swizzled smem layout the
+//    MMA reads; one thread issues tcgen05.mma into a double-buffered TMEM accumulator; four
+//    epilogue warps drain TMEM while the next tile is computed.  The rank-r LoRA term is
+//    appended as extra K-steps (weights side: zero-padded B or A rows; token side: U or V).
+//      forward : A = W^ tile (K-major: rows = out features, 64 k per row)
+//      backward: A = W^^T tile (MN-major: each 128-byte row holds 64 consecutive k of one
+//                weight row n, the contraction index), so the same decode routine serves both.
+//    Source: "QLoRA -- La base en 4 bits, LoRA encima" (paperclase, lesson 8), "Parte 4 - LoRA
+//    encima": h = W^ x + (alpha/r) B A x and dL/dx = (W^ + (alpha/r) B A)^T dL/dh, with W^
+//    rebuilt on every pass ("QLoRA" glossary, ultralytics: dequantized to bfloat16 right before
+//    the matmul, in the forward and in backprop).
+// 2. lora_proj_kernel<p_mn, q_mn>: skinny products with N = r64 <= 256 (U = X A^T, V = G B,
+//    dA = V^T X, dB = G^T U), split over the contraction with fp32 partials and a fixed-order
+//    finalize (deterministic).
+#include <algorithm>
+
+#include "qlora_common.cuh"
+#include "qlora_kernels.cuh"
+
+namespace qlora {
+
+static constexpr int kStages = 4;
+static constexpr uint32_t kATileBytes = 128u * 128u;  // 128 rows x 64 bf16
+static constexpr uint32_t kCodesTileBytes = 4096u;    // 128 rows x 32 B or 64 rows x 64 B
+static constexpr int kFusedThreads = 448;              // 14 warps
+static constexpr int kDecodeWarp0 = 6;                 // warps 6..13 decode
+static constexpr int kEpiWarp0 = 2;                    // warps 2..5 epilogue
+static constexpr uint32_t kTmemCols = 512;             // two accumulators of up to 256 columns
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t bf16x2(float lo, float hi) {
+    __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&p);
+}
+
+// The 16 dequantized values of one block, v[c] = bf16_rne(fl32(NF4[c] * s)), split into byte
+// tables: lo[i] holds the low bytes of v[4i..4i+3], hi[i] the high bytes.
+__device__ __forceinline__ void build_table(float s, const NF4Tables &tab, uint32_t (&lo)[4], uint32_t (&hi)[4]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t p01 = bf16x2(__fmul_rn(tab.level[4 * i], s), __fmul_rn(tab.level[4 * i + 1], s));
+        const uint32_t p23 = bf16x2(__fmul_rn(tab.level[4 * i + 2], s), __fmul_rn(tab.level[4 * i + 3], s));
+        lo[i] = prmt(p01, p23, 0x6420u);
+        hi[i] = prmt(p01, p23, 0x7531u);
+    }
+}
+
+// Look up 4 codes held in the low 16 bits of q, in nibble order (c1, c0, c3, c2) (the packing
+// puts element 2j in the high nibble of byte j), and return the bf16 pairs (e0 | e1 << 16) and
+// (e2 | e3 << 16).  The low 3 bits of each code select within 8-entry halves; bit 3 picks
+// the half.
+__device__ __forceinline__ void lookup4(uint32_t q, const uint32_t (&lo)[4], const uint32_t (&hi)[4], uint32_t &o0,
+                                        uint32_t &o1) {
+    const uint32_t sel = q & 0x7777u;
+    const uint32_t sel2 = ((q >> 1) & 0x4444u) | 0x3210u;
+    const uint32_t l4 = prmt(prmt(lo[0], lo[1], sel), prmt(lo[2], lo[3], sel), sel2);
+    const uint32_t h4 = prmt(prmt(hi[0], hi[1], sel), prmt(hi[2], hi[3], sel), sel2);
+    o0 = prmt(l4, h4, 0x4051u);
+    o1 = prmt(l4, h4, 0x6273u);
+}
+
+// 8 codes (one 32-bit word, elements 0..7) -> 4 words of bf16 pairs.
+__device__ __forceinline__ uint4 decode8(uint32_t x, const uint32_t (&lo)[4], const uint32_t (&hi)[4]) {
+    uint4 o;
+    lookup4(x, lo, hi, o.x, o.y);
+    lookup4(x >> 16, lo, hi, o.z, o.w);
+    return o;
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ float dq_block_scale(const FusedArgs &p, int64_t b, float mu) {
+    const float c2 = __ldg(p.scale_scales + (b >> 8));
+    return __fmaf_rn((float)__ldg(p.scale_codes + b), __fdiv_rn(c2, 127.0f), mu);
+}
+
+// Warp-uniform bounded wait: lane 0 polls, the result is broadcast, and __syncwarp orders the
+// other lanes' later accesses after lane 0's acquire.
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile uint32_t *abort) {
+    uint32_t ok = 0;
+    if ((threadIdx.x & 31u) == 0) ok = mbar_wait(bar, parity, abort) ? 1u : 0u;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    __syncwarp();
+    return ok != 0;
+}
+
+struct UnitInfo {
+    int w_tile, m_tile, split, kt0, kt1, nk;
+};
+
+__device__ __forceinline__ UnitInfo unit_info(const FusedArgs &p, int u) {
+    UnitInfo ui;
+    ui.split = u % p.splits;
+    const int t = u / p.splits;
+    ui.w_tile = t % p.w_tiles;
+    ui.m_tile = t / p.w_tiles;
+    ui.kt0 = (int)((int64_t)ui.split * p.kt_main / p.splits);
+    ui.kt1 = (int)((int64_t)(ui.split + 1) * p.kt_main / p.splits);
+    ui.nk = (ui.kt1 - ui.kt0) + (ui.split == p.splits - 1 ? p.kt_lora : 0);
+    return ui;
+}
+
+template <bool kDX>
+__global__ void __launch_bounds__(kFusedThreads, 1)
+    nf4_lora_gemm_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant__ CUtensorMap map_act,
+                         const __grid_constant__ CUtensorMap map_lora, const FusedArgs p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+    const uint32_t b_bytes = (uint32_t)p.BN * 128u;
+    uint8_t *sA = smem;
+    uint8_t *sB = sA + kStages * kATileBytes;
+    uint8_t *sC = sB + kStages * b_bytes;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sC + kStages * kCodesTileBytes);
+    uint64_t *full_c = bars;                 // codes landed (or LoRA k-step announced)
+    uint64_t *full_b = bars + kStages;       // activation tile landed
+    uint64_t *full_a = bars + 2 * kStages;   // decoded weight tile written
+    uint64_t *empty = bars + 3 * kStages;    // MMAs reading the stage finished
+    uint64_t *acc_full = bars + 4 * kStages; // [2]
+    uint64_t *acc_empty = acc_full + 2;      // [2]
+    uint64_t *drain = acc_empty + 2;         // [1]
+    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(drain + 1);
+    volatile uint32_t *s_abort = s_tmem + 1;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full_c[s], 1);
+            mbar_init(&full_b[s], 1);
+            mbar_init(&full_a[s], 8);
+            mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&acc_full[a], 1);
+            mbar_init(&acc_empty[a], 4);
+        }
+        mbar_init(drain, 1);
+        *s_abort = 0u;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(s_tmem, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *s_tmem;
+
+    const int total_units = p.w_tiles * p.m_tiles * p.splits;
+
+    if (warp == 0) {
+        // ------------------------------ TMA producer ------------------------------------
+        if (lane == 0) {
+            tma_prefetch_desc(&map_codes);
+            tma_prefetch_desc(&map_act);
+            tma_prefetch_desc(&map_lora);
+            int s = 0;
+            uint32_t ph = 0;
+            uint32_t issued_parity[kStages];
+            bool issued[kStages];
+            for (int i = 0; i < kStages; ++i) issued[i] = false, issued_parity[i] = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
+                const UnitInfo ui = unit_info(p, u);
+                for (int j = 0; j < ui.nk; ++j) {
+                    if (!mbar_wait(&empty[s], ph ^ 1u, s_abort)) { ok = false; break; }
+                    const bool lora = (ui.kt0 + j) >= ui.kt1;
+                    if (!lora) {
+                        const int kt = ui.kt0 + j;
+                        mbar_arrive_expect_tx(&full_c[s], kCodesTileBytes);
+                        if (kDX)
+                            tma_load_2d(sC + s * kCodesTileBytes, &map_codes, &full_c[s], ui.w_tile * 64, kt * 64);
+                        else
+                            tma_load_2d(sC + s * kCodesTileBytes, &map_codes, &full_c[s], kt * 32, ui.w_tile * 128);
+                        mbar_arrive_expect_tx(&full_b[s], b_bytes);
+                        tma_load_2d(sB + s * b_bytes, &map_act, &full_b[s], kt * 64, ui.m_tile * p.BN);
+                    } else {
+                        const int lt = j - (ui.kt1 - ui.kt0);
+                        mbar_arrive(&full_c[s]);
+                        mbar_arrive_expect_tx(&full_b[s], b_bytes);
+                        tma_load_2d(sB + s * b_bytes, &map_lora, &full_b[s], lt * 64, ui.m_tile * p.BN);
+                    }
+                    issued[s] = true;
+                    issued_parity[s] = ph;
+                    if (++s == kStages) { s = 0; ph ^= 1u; }
+                }
+            }
+            if (!ok) {
+                // let copies already in flight land before the CTA can exit
+                for (int i = 0; i < kStages; ++i) {
+                    if (!issued[i]) continue;
+                    const uint64_t t0 = globaltimer_ns();
+                    while (!mbar_try_wait(&full_b[i], issued_parity[i]) && globaltimer_ns() - t0 < 10000000ull) {}
+                    while (!mbar_try_wait(&full_c[i], issued_parity[i]) && globaltimer_ns() - t0 < 20000000ull) {}
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------ MMA issuer ---------------------------------------
+        if (lane == 0) {
+            const uint32_t idesc = make_idesc_bf16((uint32_t)p.BN, kDX, false);
+            const uint32_t a_base = smem_u32(sA), b_base = smem_u32(sB);
+            int s = 0;
+            uint32_t ph = 0;
+            int lt = 0;
+            bool ok = true;
+            bool any = false;
+            for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x, ++lt) {
+                const UnitInfo ui = unit_info(p, u);
+                const int a = lt & 1;
+                if (!mbar_wait(&acc_empty[a], ((lt >> 1) & 1) ^ 1u, s_abort)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)a * 256u;
+                for (int j = 0; j < ui.nk; ++j) {
+                    if (!mbar_wait(&full_a[s], ph, s_abort) || !mbar_wait(&full_b[s], ph, s_abort)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_addr = a_base + (uint32_t)s * kATileBytes;
+                    const uint32_t b_addr = b_base + (uint32_t)s * b_bytes;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t adesc = kDX ? make_sw128_desc(a_addr + kk * 2048u, 8192u, 1024u)
+                                                   : make_sw128_desc(a_addr + kk * 32u, 16u, 1024u);
+                        const uint64_t bdesc = make_sw128_desc(b_addr + kk * 32u, 16u, 1024u);
+                        umma_bf16(d_tmem, adesc, bdesc, idesc, (j > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    any = true;
+                    umma_commit(&empty[s]);
+                    if (++s == kStages) { s = 0; ph ^= 1u; }
+                }
+                if (!ok) break;
+                umma_commit(&acc_full[a]);
+            }
+            if (!ok && any) {
+                umma_commit(drain);
+                const uint64_t t0 = globaltimer_ns();
+                while (!mbar_try_wait(drain, 0) && globaltimer_ns() - t0 < 20000000ull) {}
+            }
+        }
+        __syncwarp();
+    } else if (warp < kDecodeWarp0) {
+        // ------------------------------ epilogue -----------------------------------------
+        const int quarter = warp & 3;  // TMEM lanes this warp may access
+        int lt = 0;
+        for (int u = blockIdx.x; u < total_units; u += gridDim.x, ++lt) {
+            const UnitInfo ui = unit_info(p, u);
+            const int a = lt & 1;
+            if (!warp_wait(&acc_full[a], (lt >> 1) & 1, s_abort)) break;
+            tc_fence_after();
+            const int64_t f = (int64_t)ui.w_tile * 128 + quarter * 32 + lane;
+            const int m0 = ui.m_tile * p.BN;
+            const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)a * 256u;
+            for (int c = 0; c < p.BN / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(taddr + (uint32_t)c * 32u, r);
+                tmem_ld_wait();
+                if (f < p.wdim) {
+                    if (p.splits == 1) {
+#pragma unroll
+                        for (int jj = 0; jj < 32; ++jj) {
+                            const int m = m0 + c * 32 + jj;
+                            if (m < p.M) {
+                                __nv_bfloat16 h = __float2bfloat16_rn(__uint_as_float(r[jj]));
+                                p.out[(int64_t)m * p.wdim + f] = *reinterpret_cast<uint16_t *>(&h);
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int jj = 0; jj < 32; ++jj) {
+                            const int m = m0 + c * 32 + jj;
+                            if (m < p.M) p.partial[((int64_t)ui.split * p.M + m) * p.wdim + f] = __uint_as_float(r[jj]);
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[a]);
+        }
+    } else {
+        // ------------------------------ decode warps -------------------------------------
+        const int t = threadIdx.x - kDecodeWarp0 * 32;  // 0..255
+        const float mu = __ldg(p.scale_offset);
+        const uint32_t a_base = smem_u32(sA);
+        int s = 0;
+        uint32_t ph = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
+            const UnitInfo ui = unit_info(p, u);
+            for (int j = 0; j < ui.nk; ++j) {
+                const bool lora = (ui.kt0 + j) >= ui.kt1;
+                const int kt = lora ? j - (ui.kt1 - ui.kt0) : ui.kt0 + j;
+                // this thread's 32 weights: a 128-byte smem row, chunks half*4 .. half*4+3
+                int64_t wrow;       // weight row n (main) or LoRA row
+                int64_t blk = -1;   // NF4 block index, -1 if out of range
+                uint32_t row_addr;  // smem byte address of the 128-byte row
+                uint32_t code_off;  // byte offset of the 16 code bytes in the codes tile
+                const uint16_t *lsrc = nullptr;
+                const int half = t & 1;
+                if (!kDX) {
+                    const int row = t >> 1;
+                    wrow = (int64_t)ui.w_tile * 128 + row;
+                    row_addr = a_base + (uint32_t)s * kATileBytes + (uint32_t)row * 128u;
+                    code_off = (uint32_t)row * 32u + (uint32_t)half * 16u;
+                    if (wrow < p.N) {
+                        if (!lora) blk = wrow * p.KB + kt;
+                        else lsrc = p.lora_rows + wrow * p.r64 + kt * 64 + half * 32;
+                    }
+                } else {
+                    const int nl = t >> 2, kbl = (t >> 1) & 1;
+                    const int kblock = ui.w_tile * 2 + kbl;  // 64-column block along K
+                    row_addr = a_base + (uint32_t)s * kATileBytes + (uint32_t)kbl * 8192u + (uint32_t)nl * 128u;
+                    code_off = (uint32_t)nl * 64u + (uint32_t)kbl * 32u + (uint32_t)half * 16u;
+                    if (!lora) {
+                        wrow = (int64_t)kt * 64 + nl;
+                        if (wrow < p.N && kblock < p.KB) blk = wrow * p.KB + kblock;
+                    } else {
+                        wrow = (int64_t)kt * 64 + nl;  // LoRA row j < r64
+                        if (kblock < p.KB) lsrc = p.lora_rows + wrow * p.K + (int64_t)kblock * 64 + half * 32;
+                    }
+                }
+                float sc = 0.0f;
+                if (blk >= 0) sc = dq_block_scale(p, blk, mu);  // issued before the waits
+                uint4 lv[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
+                               make_uint4(0, 0, 0, 0)};
+                if (lsrc) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) lv[i] = __ldg(reinterpret_cast<const uint4 *>(lsrc) + i);
+                }
+                if (!warp_wait(&empty[s], ph ^ 1u, s_abort)) { ok = false; break; }
+                if (!warp_wait(&full_c[s], ph, s_abort)) { ok = false; break; }
+                uint4 outv[4];
+                if (!lora) {
+                    if (blk >= 0) {
+                        const uint4 cw = *reinterpret_cast<const uint4 *>(sC + s * kCodesTileBytes + code_off);
+                        uint32_t lo[4], hi[4];
+                        build_table(sc, p.tab, lo, hi);
+                        outv[0] = decode8(cw.x, lo, hi);
+                        outv[1] = decode8(cw.y, lo, hi);
+                        outv[2] = decode8(cw.z, lo, hi);
+                        outv[3] = decode8(cw.w, lo, hi);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) outv[i] = make_uint4(0, 0, 0, 0);
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) outv[i] = lv[i];
+                }
+                // 128-byte swizzle: 16-byte chunk c of row r lives at chunk c ^ (r & 7); rows are
+                // 128-byte aligned inside 1024-byte-aligned tiles, so (row_addr >> 7) & 7 == r & 7.
+                const uint32_t r7 = (row_addr >> 7) & 7u;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint32_t chunk = (uint32_t)(half * 4 + i);
+                    st_shared_v4(row_addr + ((chunk ^ r7) << 4), outv[i]);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&full_a[s]);
+                if (++s == kStages) { s = 0; ph ^= 1u; }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------------------------------
+// Skinny LoRA products.
+// ---------------------------------------------------------------------------------------
+template <bool kPMN, bool kQMN>
+__global__ void __launch_bounds__(128, 1)
+    lora_proj_kernel(const __grid_constant__ CUtensorMap map_p, const __grid_constant__ CUtensorMap map_q, int Mp,
+                     int r64, int tiles, int splits, int ktiles, float *__restrict__ partial) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+    const uint32_t q_bytes = (uint32_t)r64 * 128u;
+    uint8_t *sP = smem;
+    uint8_t *sQ = sP + kStages * kATileBytes;
+    uint64_t *full = reinterpret_cast<uint64_t *>(sQ + kStages * q_bytes);
+    uint64_t *empty = full + kStages;
+    uint64_t *done = empty + kStages;
+    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(done + 1);
+    volatile uint32_t *s_abort = s_tmem + 1;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tile = blockIdx.x % tiles, split = blockIdx.x / tiles;
+    const int kt0 = (int)((int64_t)split * ktiles / splits), kt1 = (int)((int64_t)(split + 1) * ktiles / splits);
+    const uint32_t ncols = r64 <= 64 ? 64u : (r64 <= 128 ? 128u : 256u);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(done, 1);
+        *s_abort = 0u;
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(s_tmem, ncols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *s_tmem;
+
+    if (warp == 0 && lane == 0) {
+        int s = 0;
+        uint32_t ph = 0;
+        for (int kt = kt0; kt < kt1; ++kt) {
+            if (!mbar_wait(&empty[s], ph ^ 1u, s_abort)) break;
+            mbar_arrive_expect_tx(&full[s], kATileBytes + q_bytes);
+            uint8_t *dp = sP + s * kATileBytes;
+            uint8_t *dq = sQ + s * q_bytes;
+            if (kPMN) {
+                tma_load_2d(dp, &map_p, &full[s], tile * 128, kt * 64);
+                tma_load_2d(dp + 8192, &map_p, &full[s], tile * 128 + 64, kt * 64);
+            } else {
+                tma_load_2d(dp, &map_p, &full[s], kt * 64, tile * 128);
+            }
+            if (kQMN) {
+                for (int jb = 0; jb < r64 / 64; ++jb) tma_load_2d(dq + jb * 8192, &map_q, &full[s], jb * 64, kt * 64);
+            } else {
+                tma_load_2d(dq, &map_q, &full[s], kt * 64, 0);
+            }
+            if (++s == kStages) { s = 0; ph ^= 1u; }
+        }
+    } else if (warp == 1 && lane == 0) {
+        const uint32_t idesc = make_idesc_bf16((uint32_t)r64, kPMN, kQMN);
+        const uint32_t p_base = smem_u32(sP), q_base = smem_u32(sQ);
+        int s = 0;
+        uint32_t ph = 0;
+        bool ok = true;
+        for (int kt = kt0; kt < kt1; ++kt) {
+            if (!mbar_wait(&full[s], ph, s_abort)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t pa = p_base + (uint32_t)s * kATileBytes, qa = q_base + (uint32_t)s * q_bytes;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t adesc = kPMN ? make_sw128_desc(pa + kk * 2048u, 8192u, 1024u)
+                                            : make_sw128_desc(pa + kk * 32u, 16u, 1024u);
+                const uint64_t bdesc = kQMN ? make_sw128_desc(qa + kk * 2048u, 8192u, 1024u)
+                                            : make_sw128_desc(qa + kk * 32u, 16u, 1024u);
+                umma_bf16(tmem_base, adesc, bdesc, idesc, (kt > kt0 || kk > 0) ? 1u : 0u);
+            }
+            umma_commit(&empty[s]);
+            if (++s == kStages) { s = 0; ph ^= 1u; }
+        }
+        (void)ok;
+        umma_commit(done);  // also drains on the error path
+    }
+    __syncwarp();
+    // epilogue: all four warps (warp w reads TMEM lanes 32w..32w+31)
+    if (warp_wait(done, 0, s_abort)) {
+        tc_fence_after();
+        const int64_t i = (int64_t)tile * 128 + warp * 32 + lane;
+        const uint32_t taddr = tmem_base + ((uint32_t)(warp * 32) << 16);
+        for (int c = 0; c < r64 / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(taddr + (uint32_t)c * 32u, r);
+            tmem_ld_wait();
+            if (i < Mp) {
+                float4 *dst = reinterpret_cast<float4 *>(partial + ((int64_t)split * Mp + i) * r64 + c * 32);
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    dst[q] = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                                         __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, ncols);
+    }
+}
+
+// ---------------------------------------------------------------------------------------
+// Small elementwise kernels
+// ---------------------------------------------------------------------------------------
+__global__ void splitk_reduce_kernel(const float *__restrict__ partial, int splits, int64_t total,
+                                     uint16_t *__restrict__ out) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        float acc = partial[i];
+        for (int s = 1; s < splits; ++s) acc = __fadd_rn(acc, partial[(int64_t)s * total + i]);
+        __nv_bfloat16 h = __float2bfloat16_rn(acc);
+        out[i] = *reinterpret_cast<uint16_t *>(&h);
+    }
+}
+
+__global__ void proj_finalize_kernel(int mode, const float *__restrict__ partial, int splits, int64_t Mp, int r64,
+                                     int r, float scale, uint16_t *__restrict__ out_pad, uint16_t *__restrict__ out_r,
+                                     float *__restrict__ out_f) {
+    const int64_t total = Mp * r64;
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total; e += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t i = e / r64;
+        const int j = (int)(e % r64);
+        float acc = partial[e];
+        for (int s = 1; s < splits; ++s) acc = __fadd_rn(acc, partial[(int64_t)s * total + e]);
+        if (mode == 0) {
+            __nv_bfloat16 h = __float2bfloat16_rn(__fmul_rn(acc, scale));
+            const uint16_t hb = *reinterpret_cast<uint16_t *>(&h);
+            out_pad[e] = hb;
+            if (out_r && j < r) out_r[i * r + j] = hb;
+        } else if (mode == 1) {
+            if (j < r) out_f[(int64_t)j * Mp + i] = acc;
+        } else {
+            if (j < r) out_f[i * r + j] = acc;
+        }
+    }
+}
+
+__global__ void pad_2d_kernel(const uint16_t *__restrict__ src, int64_t rows_src, int64_t cols_src,
+                              uint16_t *__restrict__ dst, int64_t rows_dst, int64_t cols_dst) {
+    const int64_t total = rows_dst * cols_dst;
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total; e += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t i = e / cols_dst, j = e % cols_dst;
+        dst[e] = (i < rows_src && j < cols_src) ? src[i * cols_src + j] : (uint16_t)0;
+    }
+}
+
+// ---------------------------------------------------------------------------------------
+// Plans and launchers
+// ---------------------------------------------------------------------------------------
+// The fused kernel allocates all 512 TMEM columns, so it must be alone on its SM: asking for
+// more than half of the SM's shared memory guarantees one resident CTA.
+static size_t fused_smem_bytes(int BN) {
+    const size_t need = 1024 + (size_t)kStages * (kATileBytes + (size_t)BN * 128 + kCodesTileBytes) + 256;
+    return std::max<size_t>(need, 120 * 1024);
+}
+static size_t proj_smem_bytes(int r64) { return 1024 + (size_t)kStages * (kATileBytes + (size_t)r64 * 128) + 128; }
+
+FusedPlan plan_fused(int64_t M, int64_t wdim, int64_t kt_main, int r64, int num_sms) {
+    FusedPlan pl{};
+    int64_t bn = M >= 256 ? 256 : ((M + 31) / 32) * 32;
+    if (bn < 32) bn = 32;
+    pl.BN = (int)bn;
+    pl.m_tiles = (int)((M + bn - 1) / bn);
+    pl.w_tiles = (int)((wdim + 127) / 128);
+    pl.kt_main = (int)kt_main;
+    pl.kt_lora = r64 / 64;
+    pl.splits = 1;
+    const int64_t units = (int64_t)pl.w_tiles * pl.m_tiles;
+    if (pl.m_tiles == 1 && units < 2LL * num_sms) {
+        // small token count: split the contraction so that the units fill whole waves
+        int best = 1;
+        double best_eff = 0.0;
+        for (int s = 1; s <= 16 && s <= kt_main / 4; ++s) {
+            const int64_t us = units * s;
+            const double eff = (double)us / (double)(((us + num_sms - 1) / num_sms) * num_sms);
+            if (eff > best_eff + 1e-9) { best_eff = eff; best = s; }
+            if (eff >= 0.9) break;
+        }
+        pl.splits = best;
+    }
+    const int64_t total = units * pl.splits;
+    pl.grid = (int)std::min<int64_t>(total, num_sms);
+    pl.partial_bytes = pl.splits > 1 ? (size_t)pl.splits * (size_t)M * (size_t)wdim * 4 : 0;
+    return pl;
+}
+
+ProjPlan plan_proj(int64_t Mp, int64_t Kc, int r64, int num_sms) {
+    ProjPlan pl{};
+    pl.tiles = (int)((Mp + 127) / 128);
+    pl.ktiles = (int)((Kc + 63) / 64);
+    const int per_sm = r64 <= 64 ? 2 : 1;
+    int64_t s = ((int64_t)per_sm * num_sms + pl.tiles - 1) / pl.tiles;
+    s = std::max<int64_t>(1, std::min<int64_t>(s, std::min<int64_t>(pl.ktiles, 32)));
+    pl.splits = (int)s;
+    pl.partial_bytes = (size_t)pl.splits * (size_t)Mp * (size_t)r64 * 4;
+    return pl;
+}
+
+cudaError_t launch_fused(bool dx, const CUtensorMap &map_codes, const CUtensorMap &map_act, const CUtensorMap &map_lora,
+                         const FusedArgs &args, const FusedPlan &plan, cudaStream_t st) {
+    const size_t smem = fused_smem_bytes(plan.BN);
+    cudaError_t e;
+    if (dx) {
+        e = cudaFuncSetAttribute(nf4_lora_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        nf4_lora_gemm_kernel<true><<<plan.grid, kFusedThreads, smem, st>>>(map_codes, map_act, map_lora, args);
+    } else {
+        e = cudaFuncSetAttribute(nf4_lora_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        nf4_lora_gemm_kernel<false><<<plan.grid, kFusedThreads, smem, st>>>(map_codes, map_act, map_lora, args);
+    }
+    count_launch();
+    return cudaGetLastError();
+}
+
+static int ew_grid(int64_t n, int num_sms) {
+    int64_t g = (n + 255) / 256;
+    return (int)std::max<int64_t>(1, std::min<int64_t>(g, (int64_t)num_sms * 8));
+}
+
+cudaError_t launch_splitk_reduce(const float *partial, int splits, int64_t rows, int64_t cols, uint16_t *out,
+                                 int num_sms, cudaStream_t st) {
+    const int64_t total = rows * cols;
+    splitk_reduce_kernel<<<ew_grid(total, num_sms), 256, 0, st>>>(partial, splits, total, out);
+    count_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t launch_proj(bool p_mn, bool q_mn, const CUtensorMap &map_p, const CUtensorMap &map_q, int64_t Mp,
+                        int64_t Kc, int r64, const ProjPlan &plan, float *partial, cudaStream_t st) {
+    (void)Kc;
+    const size_t smem = proj_smem_bytes(r64);
+    const int grid = plan.tiles * plan.splits;
+#define QLORA_PROJ_CASE(PM, QM)                                                                                     \
+    if (p_mn == PM && q_mn == QM) {                                                                                 \
+        cudaError_t e =                                                                                             \
+            cudaFuncSetAttribute(lora_proj_kernel<PM, QM>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
+        if (e != cudaSuccess) return e;                                                                             \
+        lora_proj_kernel<PM, QM><<<grid, 128, smem, st>>>(map_p, map_q, (int)Mp, r64, plan.tiles, plan.splits,      \
+                                                          plan.ktiles, partial);                                    \
+    }
+    QLORA_PROJ_CASE(false, false)
+    QLORA_PROJ_CASE(false, true)
+    QLORA_PROJ_CASE(true, false)
+    QLORA_PROJ_CASE(true, true)
+#undef QLORA_PROJ_CASE
+    count_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t launch_proj_finalize(int mode, const float *partial, int splits, int64_t Mp, int r64, int r, float scale,
+                                 uint16_t *out_pad, uint16_t *out_r, float *out_f, int num_sms, cudaStream_t st) {
+    proj_finalize_kernel<<<ew_grid(Mp * r64, num_sms), 256, 0, st>>>(mode, partial, splits, Mp, r64, r, scale, out_pad,
+                                                                     out_r, out_f);
+    count_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pad_2d(const uint16_t *src, int64_t rows_src, int64_t cols_src, uint16_t *dst, int64_t rows_dst,
+                          int64_t cols_dst, int num_sms, cudaStream_t st) {
+    pad_2d_kernel<<<ew_grid(rows_dst * cols_dst, num_sms), 256, 0, st>>>(src, rows_src, cols_src, dst, rows_dst,
+                                                                         cols_dst);
+    count_launch();
+    return cudaGetLastError();
+}
+
+}  // namespace qlora

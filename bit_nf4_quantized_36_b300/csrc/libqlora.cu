@@ -1,0 +1,5 @@
+// libqlora.cu -- single translation unit of the library (the device error word and the
+// kernels that set it must live in one device module without relocatable device code).
+#include "quant.cu"
+#include "gemm.cu"
+#include "api.cu"

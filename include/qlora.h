@@ -1,0 +1,142 @@
+/*
+ * qlora.h -- C ABI of libqlora: the QLoRA frozen-base linear layer on NVIDIA B300 (sm_103a).
+ *
+ * The layer keeps a frozen weight matrix W [N_out, K_in] in 4-bit NormalFloat (NF4) with
+ * double-quantized block scales, and trains a rank-r adapter (A [r, K], B [N, r]) on top:
+ *
+ *     Y = X W^T + (alpha / r) (X A^T) B^T,        W^ = dequant_bf16(W_nf4)
+ *
+ * Sources (page title and section):
+ *   - "QLoRA -- La base en 4 bits, LoRA encima" (paperclase.com, LoRA course, lesson 8):
+ *     "Parte 1" absmax per block; "Parte 2 - NormalFloat" quantile levels with an exact zero,
+ *     W^ = NF4[c] * absmax; "Parte 3 - Cuanta memoria" 4 + 8/64 + 32/(64*256) bits per weight;
+ *     "Parte 4 - LoRA encima" the Lineal4bit layer, h = W^ x + (alpha/r) B A x and
+ *     dL/dx = (W^ + (alpha/r) B A)^T dL/dh, no gradient for W^.
+ *   - "QLoRA" glossary (ultralytics.com), "Como funciona a QLoRA": NF4 levels as built in
+ *     bitsandbytes, one absmax per 64 weights, scales double-quantized to 8 bits in blocks
+ *     of 256, dequantized to bfloat16 right before the matmul, only the LoRA matrices updated.
+ *
+ * Conventions for every call:
+ *   - All tensor pointers are DEVICE pointers, owned by the caller, row-major, 16-byte
+ *     aligned.  bf16 tensors are passed as uint16_t bit patterns.  The library never
+ *     allocates device memory; scratch space is the caller's workspace (size queries below).
+ *   - Calls are asynchronous and ordered on `stream` (a cudaStream_t, NULL = legacy default
+ *     stream).  The returned status covers argument checks and launch errors only.
+ *     Device-side faults of the pipelined kernels (a bounded wait that ran out) are latched
+ *     in a device word and reported by qlora_check_device_error().
+ *   - Calls keep no state between them and may be issued from several host threads.
+ *   - Shape rules: cols (K) % 64 == 0 so that no 64-weight block straddles two rows;
+ *     rows (N) >= 1; tokens M >= 1; 1 <= r <= 256; alpha finite.
+ */
+#ifndef QLORA_H
+#define QLORA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    QLORA_OK = 0,
+    QLORA_ERR_INVALID_ARG = 1,      /* NULL pointer, non-finite alpha, r out of range ...      */
+    QLORA_ERR_UNSUPPORTED_SHAPE = 2,/* cols % 64 != 0, empty matrix, too large ...            */
+    QLORA_ERR_MISALIGNED = 3,       /* a pointer is not 16-byte aligned                        */
+    QLORA_ERR_WORKSPACE = 4,        /* workspace NULL or smaller than the size query returns  */
+    QLORA_ERR_CUDA = 5,             /* a CUDA runtime/driver call or a kernel launch failed    */
+    QLORA_ERR_TIMEOUT = 6           /* a device-side bounded wait ran out (from the check call)*/
+} qlora_status;
+
+/* One NF4 matrix with double-quantized scales.
+ * Let n = rows*cols, nb = n/64 blocks (block b = flat elements [64b, 64b+64) of row-major W),
+ * ng = ceil(nb/256) groups (group g = blocks [256g, 256g+256)).
+ *   codes[n/2]        : byte j = (c[2j] << 4) | c[2j+1]; c = index into the NF4 table
+ *   scale_codes[nb]   : int8 code q_b of the block scale, in [-127, 127]
+ *   scale_scales[ng]  : fp32 c2_g, the largest |s_b - mu| in the group
+ *   scale_offset[1]   : fp32 mu, the mean of all block scales of the matrix
+ * The block scale is rebuilt as s'_b = fmaf(q_b, c2_g / 127, mu) and a weight as
+ * bf16_rne(NF4[c] * s'_b).  All four arrays are device memory owned by the caller. */
+typedef struct {
+    int64_t rows;          /* N_out */
+    int64_t cols;          /* K_in, a multiple of 64 */
+    uint8_t *codes;
+    int8_t *scale_codes;
+    float *scale_scales;
+    float *scale_offset;
+} qlora_nf4_tensor;
+
+/* Bytes of the four arrays of one quantized matrix: n/2 + nb + 4*ng + 4.
+ * ("Parte 3 - Cuanta memoria", "Bits por parametro": 4 + 8/64 + 32/(64*256) bits per weight.)
+ * Returns 0 if the shape is unsupported. */
+size_t qlora_nf4_storage_bytes(int64_t rows, int64_t cols);
+
+/* Workspace sizes (bytes, device memory) of the calls below; 0 means "no workspace needed"
+ * for quantize only.  A call given less returns QLORA_ERR_WORKSPACE.  Returns (size_t)-1 if
+ * the shape is unsupported. */
+size_t qlora_quantize_workspace_bytes(int64_t rows, int64_t cols);
+size_t qlora_fwd_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t r);
+size_t qlora_bwd_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t r);
+
+/* NF4-quantize an fp32 matrix W [rows, cols] into `out` (its four arrays must be allocated
+ * with the sizes above; out->rows/cols give the shape).
+ * Definition ("Una capa QLoRA, a mano" and the glossary's NF4 snippet): per 64-block,
+ * s_b = max |w|; each weight gets c = argmin_k |fl32(w / s_b) - NF4[k]| (fp32 division and
+ * distances, ties to the lower k; an all-zero block gets the zero level); then the scales are
+ * double-quantized ("Parte 3": 8 bits per scale, one 32-bit constant per 256 blocks):
+ *   mu   = fl32(T / nb), T = pairwise fp64 tree (zero-padded to a power of two) over the
+ *          group sums S_g, each S_g the fp64 sum of its scales in index order
+ *   c2_g = max over the group of |fl32(s_b - mu)|
+ *   q_b  = rint(fl32(fl32(fl32(s_b - mu) / c2_g) * 127)), or 0 when c2_g == 0.
+ * Deterministic and bit-exact.  W must be finite.
+ * ws: qlora_quantize_workspace_bytes(rows, cols) bytes of device memory (block scales and
+ * group sums). */
+qlora_status nf4_quantize(const float *W, const qlora_nf4_tensor *out, void *ws, size_t ws_bytes,
+                          void *stream);
+
+/* Dequantize to bf16: W_out[rows, cols] = bf16_rne(NF4[c] * s'_b) ("Cuantiles": w^ = NF4[c] *
+ * absmax; glossary: dequantized to bfloat16 before the matmul).  No workspace. */
+qlora_status nf4_dequantize(const qlora_nf4_tensor *q, uint16_t *W_out, void *stream);
+
+/* Forward of the layer ("Parte 4 - LoRA encima", h = W^ x + (alpha/r) B A x):
+ *   Y [M, N] (bf16) = X W^T + U B^T,   U = bf16((alpha/r) X A^T)  [M, r]
+ * X [M, K] bf16, A [r, K] bf16, B [N, r] bf16; fp32 accumulation; W^ is dequantized inside the
+ * GEMM main loop and never written to memory.
+ * U_save (nullable) receives U [M, r] (bf16, already multiplied by alpha/r) for the backward. */
+qlora_status qlora_linear_fwd(const qlora_nf4_tensor *W, const uint16_t *X, int64_t M,
+                              const uint16_t *A, const uint16_t *B, int32_t r, float alpha,
+                              uint16_t *Y, uint16_t *U_save, void *ws, size_t ws_bytes, void *stream);
+
+/* Backward of the layer ("El gradiente atraviesa la base de 4 bits": dL/dx = (W^ + (alpha/r)
+ * B A)^T dL/dh; dL/dW^ is not computed; glossary: only the two LoRA matrices are updated):
+ *   V  = bf16((alpha/r) dY B)                [M, r]
+ *   dX = dY W^ + V A                          [M, K] bf16
+ *   dA = V^T X                                [r, K] fp32   (= (alpha/r) (dY B)^T X)
+ *   dB = dY^T U                               [N, r] fp32   (= (alpha/r) dY^T X A^T)
+ * U_saved (nullable): the U_save of the forward; when NULL, U is recomputed from X and A.
+ * dX, dA, dB are overwritten (not accumulated). */
+qlora_status qlora_linear_bwd(const qlora_nf4_tensor *W, const uint16_t *X, int64_t M,
+                              const uint16_t *A, const uint16_t *B, int32_t r, float alpha,
+                              const uint16_t *dY, const uint16_t *U_saved, uint16_t *dX, float *dA,
+                              float *dB, void *ws, size_t ws_bytes, void *stream);
+
+/* Synchronizes `stream`, then reads and clears the library's device error word on the current
+ * device.  QLORA_OK, QLORA_ERR_TIMEOUT (a pipelined kernel gave up a bounded wait and exited
+ * early; its outputs are undefined) or QLORA_ERR_CUDA. */
+qlora_status qlora_check_device_error(void *stream);
+
+/* Short English description of a status code (static string). */
+const char *qlora_status_string(qlora_status s);
+
+/* Number of kernels this library has launched in this process (all devices).  Used by
+ * benchmarks to count launches inside a timed region. */
+uint64_t qlora_launch_count(void);
+
+/* The 16 NF4 levels used by the library's kernels (fp32, ascending), for inspection. */
+void qlora_nf4_levels(float out[16]);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QLORA_H */

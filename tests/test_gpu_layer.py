@@ -1,0 +1,156 @@
+"""GPU parity of qlora_linear_fwd / qlora_linear_bwd (through the C ABI) with the fp64 CPU oracle.
+
+The oracle multiplies the bit-exact dequantized bf16 weights in fp64; the GPU accumulates in
+fp32 and rounds the LoRA intermediates U, V and the outputs Y, dX to bf16.  Acceptance: relative
+Frobenius error <= 5e-3 and max-abs error <= 2e-2 * max|ref| on every compared output."""
+import numpy as np
+import pytest
+import torch
+
+import bit_nf4_quantized_36_b300 as q
+from bit_nf4_quantized_36_b300 import synth
+from gpu_util import assert_close, dev_bf16, host_bits, host_f64, nf4_to_host
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from bit_nf4_quantized_36_b300 import build
+    build.build()
+    yield
+    q.check_device_error()
+
+
+def run_layer(inp, fwd_only=False, use_saved_u=True):
+    W = torch.from_numpy(inp.W).cuda()
+    X, A, B = dev_bf16(inp.X), dev_bf16(inp.A), dev_bf16(inp.B)
+    qw = q.nf4_quantize(W)
+    Y, U = q.qlora_linear_fwd(qw, X, A, B, inp.alpha)
+    out = dict(qw=qw, Y=Y, U=U)
+    if not fwd_only:
+        G = dev_bf16(inp.G)
+        dX, dA, dB = q.qlora_linear_bwd(qw, X, A, B, inp.alpha, G, U if use_saved_u else None)
+        out.update(dX=dX, dA=dA, dB=dB)
+    torch.cuda.synchronize()
+    q.check_device_error()
+    return out
+
+
+def oracle_what(orc, inp, qw):
+    ref = orc.nf4_quantize(inp.W)
+    got = nf4_to_host(qw)
+    np.testing.assert_array_equal(got["packed"], ref["packed"])
+    N, K = inp.W.shape
+    return orc.nf4_dequantize(ref["packed"], ref["qcode"], ref["c2"], ref["mu"], N, K)
+
+
+def check_full(orc, inp, out, rows=None, jsel=None):
+    What = oracle_what(orc, inp, out["qw"])
+    M = inp.X.shape[0]
+    sel = np.arange(M) if rows is None else np.asarray(rows)
+    Yr, Ur = orc.layer_fwd_rows(What, inp.X, inp.A, inp.B, inp.alpha, sel)
+    s = inp.alpha / inp.r
+    assert_close("Y", host_f64(out["Y"])[sel], Yr)
+    assert_close("U", host_f64(out["U"])[sel], s * Ur)
+    if "dX" in out:
+        dXr = orc.layer_dx_rows(What, inp.A, inp.B, inp.G, inp.alpha, sel)
+        assert_close("dX", host_f64(out["dX"])[sel], dXr)
+        if jsel is None:
+            dAr, dBr = orc.layer_adapter_grads(inp.X, inp.A, inp.B, inp.G, inp.alpha)
+            assert_close("dA", out["dA"].cpu().numpy(), dAr)
+            assert_close("dB", out["dB"].cpu().numpy(), dBr)
+        else:
+            js = np.asarray(jsel)
+            dAr, dBt = orc.layer_adapter_grads_cols(inp.X, inp.A, inp.B, inp.G, inp.alpha, js)
+            assert_close("dA[j]", out["dA"].cpu().numpy()[js], dAr)
+            assert_close("dB[:, j]", out["dB"].cpu().numpy()[:, js].T, dBt)
+
+
+def test_tiny_workload(orc):
+    inp = synth.tiny_inputs()
+    check_full(orc, inp, run_layer(inp))
+
+
+@pytest.mark.parametrize("M,N,K,r", [
+    (1, 8, 64, 1),         # smallest everything
+    (17, 136, 192, 5),     # ragged tokens, N not a multiple of 128, odd rank
+    (130, 264, 320, 24),   # two token tiles with a ragged tail, K % 128 != 0
+    (300, 128, 128, 72),   # r64 = 128 (two LoRA k-steps)
+    (40, 256, 512, 256),   # maximum rank
+    (257, 520, 640, 16),   # token tile 256 + 1, weight tiles 4 + ragged
+])
+def test_shapes(orc, M, N, K, r):
+    inp = synth.layer_inputs(100 + r, M, N, K, r, 2.0 * r, b_std=0.3)
+    check_full(orc, inp, run_layer(inp))
+
+
+def test_saved_u_equals_recomputed_u():
+    inp = synth.layer_inputs(201, 96, 256, 384, 16, 32.0)
+    a = run_layer(inp, use_saved_u=True)
+    b = run_layer(inp, use_saved_u=False)
+    for k in ("dX", "dA", "dB"):
+        assert torch.equal(a[k], b[k]), k
+
+
+def test_deterministic():
+    inp = synth.layer_inputs(202, 200, 512, 512, 16, 32.0)
+    a = run_layer(inp)
+    b = run_layer(inp)
+    for k in ("Y", "U", "dX", "dA", "dB"):
+        assert torch.equal(a[k], b[k]), k
+
+
+def test_adapter_b_zero(orc):
+    # LoRA init of the lesson (B = 0): Y is the base product, dA is exactly zero
+    inp = synth.layer_inputs(203, 64, 256, 512, 8, 16.0)
+    inp.B[:] = 0
+    out = run_layer(inp)
+    assert torch.count_nonzero(out["dA"]).item() == 0
+    check_full(orc, inp, out)
+
+
+def test_all_zero_weight(orc):
+    # W^ = 0: Y is the adapter term alone; the adapter has O(|Y|) weight here
+    inp = synth.layer_inputs(204, 48, 128, 256, 8, 16.0, b_std=1.0)
+    inp.W[:] = 0
+    out = run_layer(inp)
+    assert np.all(out["qw"].codes.cpu().numpy() == 0x77)
+    check_full(orc, inp, out)
+
+
+def test_adapter_term_dominant(orc):
+    # B ~ N(0, 1): the LoRA term is of the order of |Y|, not hidden by the tolerance
+    inp = synth.layer_inputs(205, 128, 256, 512, 16, 32.0, b_std=1.0)
+    check_full(orc, inp, run_layer(inp))
+
+
+def test_llama8b_attn(orc):
+    c = synth.LLAMA8B_ATTN
+    inp = synth.layer_inputs(c["id"], c["M"], c["N"], c["K"], c["r"], c["alpha"])
+    out = run_layer(inp)
+    rows = np.random.default_rng(0).choice(c["M"], 64, replace=False)
+    check_full(orc, inp, out, rows=np.sort(rows))
+
+
+@pytest.mark.parametrize("mat", [0, 2])
+def test_llama8b_mlp(orc, mat):
+    c = synth.LLAMA8B_MLP
+    name, N, K = c["mats"][mat]
+    inp = synth.layer_inputs(c["id"], c["M"], N, K, c["r"], c["alpha"], outliers="uniform", sub=mat)
+    out = run_layer(inp)
+    rows = np.sort(np.random.default_rng(1).choice(c["M"], 32, replace=False))
+    check_full(orc, inp, out, rows=rows, jsel=[0, 37, 63])
+
+
+@pytest.mark.parametrize("M", [1, 8, 32])
+@pytest.mark.parametrize("mat", [0, 1])
+def test_llama70b_decode(orc, M, mat):
+    c = synth.LLAMA70B_DECODE
+    name, N, K = c["mats"][mat]
+    inp = synth.layer_inputs(c["id"], M, N, K, c["r"], c["alpha"], w_std=c["w_std"], sub=mat, with_grad=False)
+    out = run_layer(inp, fwd_only=True)
+    rows = np.arange(M) if M <= 8 else np.array([0, 5, 17, 31])
+    check_full(orc, inp, out, rows=rows)

@@ -390,3 +390,12 @@ def test_layer_special_cases(orc):
     Wz = np.zeros_like(What)
     Y2, U2 = orc.layer_fwd_rows(Wz, X, A, B, alpha)
     np.testing.assert_allclose(Y2, alpha / A.shape[0] * U2 @ f(B).T, rtol=1e-12)
+
+
+def test_sampled_adapter_grads_match_full(orc):
+    What, X, A, B, G = _small_layer(24, M=7, N=9, K=64, r=4)
+    dA, dB = orc.layer_adapter_grads(X, A, B, G, 3.0)
+    js = np.array([3, 0], dtype=np.int64)
+    dAs, dBt = orc.layer_adapter_grads_cols(X, A, B, G, 3.0, js)
+    np.testing.assert_allclose(dAs, dA[js], rtol=1e-13)
+    np.testing.assert_allclose(dBt, dB[:, js].T, rtol=1e-13)
