@@ -71,6 +71,7 @@ def _declare(L):
     L.orc_layer_fwd_rows.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _I64, _D, _P, _I64, _P, _P]
     L.orc_layer_dx_rows.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _I64, _D, _P, _I64, _P]
     L.orc_layer_adapter_grads.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _I64, _D, _P, _P]
+    L.orc_layer_adapter_grads_cols.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _I64, _D, _P, _I64, _P, _P]
     L.orc_nf4_storage_bytes.argtypes = [_I64, _I64]
     L.orc_nf4_storage_bytes.restype = _I64
 
@@ -243,6 +244,20 @@ def layer_adapter_grads(X, A, B, G, alpha: float):
     dB = np.zeros((N, r), dtype=np.float64)
     lib().orc_layer_adapter_grads(_ptr(X), _ptr(A), _ptr(B), _ptr(G), M, N, K, r, float(alpha), _ptr(dA), _ptr(dB))
     return dA, dB
+
+
+def layer_adapter_grads_cols(X, A, B, G, alpha: float, jsel):
+    """fp64 dA[jsel, :] ([nj, K]) and dB[:, jsel]^T ([nj, N]) over all tokens."""
+    X, A, B, G = (_c(t, np.uint16) for t in (X, A, B, G))
+    M, K = X.shape
+    N = G.shape[1]
+    r = A.shape[0]
+    js = _c(jsel, np.int64)
+    dA = np.zeros((js.size, K), dtype=np.float64)
+    dBt = np.zeros((js.size, N), dtype=np.float64)
+    lib().orc_layer_adapter_grads_cols(_ptr(X), _ptr(A), _ptr(B), _ptr(G), M, N, K, r, float(alpha), _ptr(js), js.size,
+                                       _ptr(dA), _ptr(dBt))
+    return dA, dBt
 
 
 def nf4_storage_bytes(rows: int, cols: int) -> int:

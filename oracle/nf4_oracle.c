@@ -456,3 +456,38 @@ int64_t orc_nf4_storage_bytes(int64_t rows, int64_t cols)
     int64_t n = rows * cols, nb = n / 64, ng = (nb + 255) / 256;
     return n / 2 + nb + 4 * ng + 4;
 }
+
+/* Sampled adapter gradients for large shapes (same formulas as orc_layer_adapter_grads,
+ * restricted to some rank indices j):
+ *   dA[j, :] = s * sum_m V[m, j] X[m, :],  V[:, j] = G B[:, j]      (out [nj, K])
+ *   dB[:, j] = s * sum_m G[m, :] U[m, j],  U[:, j] = X A[j, :]^T    (out [nj, N], i.e. transposed) */
+void orc_layer_adapter_grads_cols(const uint16_t *X, const uint16_t *A, const uint16_t *B, const uint16_t *G,
+                                  int64_t M, int64_t N, int64_t K, int64_t r, double alpha,
+                                  const int64_t *jsel, int64_t nj, double *dA_rows, double *dB_cols)
+{
+    double s = alpha / (double)r;
+    double *u = (double *)malloc(sizeof(double) * (size_t)M);
+    double *v = (double *)malloc(sizeof(double) * (size_t)M);
+    for (int64_t jj = 0; jj < nj; ++jj) {
+        int64_t j = jsel[jj];
+        for (int64_t m = 0; m < M; ++m) {
+            double au = 0.0, av = 0.0;
+            for (int64_t k = 0; k < K; ++k) au += orc_bf16_to_double(X[m * K + k]) * orc_bf16_to_double(A[j * K + k]);
+            for (int64_t n = 0; n < N; ++n) av += orc_bf16_to_double(G[m * N + n]) * orc_bf16_to_double(B[n * r + j]);
+            u[m] = au;
+            v[m] = av;
+        }
+        for (int64_t k = 0; k < K; ++k) {
+            double acc = 0.0;
+            for (int64_t m = 0; m < M; ++m) acc += v[m] * orc_bf16_to_double(X[m * K + k]);
+            dA_rows[jj * K + k] = s * acc;
+        }
+        for (int64_t n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (int64_t m = 0; m < M; ++m) acc += orc_bf16_to_double(G[m * N + n]) * u[m];
+            dB_cols[jj * N + n] = s * acc;
+        }
+    }
+    free(u);
+    free(v);
+}
