@@ -1,0 +1,482 @@
+#!/usr/bin/env python
+"""Benchmark of the QLoRA NF4 frozen-base linear layer on B300.
+
+One step = one pass of the whole hot path over one synthetic batch of the Llama-3-8B-shaped
+attention projection (W 4096x4096 fp32 ~ N(0, 0.02), X/dY 4096x4096 bf16 ~ N(0, 1), r = 16,
+alpha = 32): nf4_quantize -> nf4_dequantize -> qlora_linear_fwd -> qlora_linear_bwd.
+value = (4 M N K + 6 M r (N + K)) / step time, in TFLOP/s (fwd+bwd model FLOPs; the
+quantize/dequantize inside the step add time, not FLOPs).
+
+--impl reference times the CPU oracle (the plain C restatement of the method) on a bounded
+sample of the same workload, scaled to a whole step.
+
+Prints one JSON line (rank 0).  Under torchrun (WORLD_SIZE > 1) every rank runs its own batch
+(weak scaling) and the adapter gradients dA, dB are summed over ranks with one all-reduce per
+step, the data-parallel exchange of the layer.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "QLoRA NF4 linear fwd+bwd TFLOP/s (Llama-8B shapes); NF4 dequant GB/s"
+WORKLOAD = "llama3-8b-attn-proj: W 4096x4096 NF4 (blk64, double-quant blk256), M=4096 tokens, r=16, alpha=32"
+L2_FLUSH_BYTES = 512 << 20
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return dict(hbm_gbs=p["hbm_gbs"], bf16_tflops=p["bf16_tflops"],
+                    bf16_tflops_sustained=p.get("bf16_tflops_sustained"), source="measured")
+    except Exception:
+        return dict(hbm_gbs=6400.0, bf16_tflops=1800.0, bf16_tflops_sustained=1400.0, source="fallback")
+
+
+def new_events(n):
+    """n timing events whose CUDA handles exist (torch creates them on first record)."""
+    import torch
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    for e in ev:
+        e.record()
+    torch.cuda.synchronize()
+    assert all(e.cuda_event for e in ev)
+    return ev
+
+
+def layer_flops(M, N, K, r):
+    return 4.0 * M * N * K + 6.0 * M * r * (N + K)
+
+
+# ---------------------------------------------------------------------------------------
+# Clock sampling during the timed region (NVML, the library behind nvidia-smi)
+# ---------------------------------------------------------------------------------------
+REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
+           0x10: "sync_boost", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+           0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting"}
+
+
+class _NVML:
+    """Minimal ctypes binding of NVML (the library nvidia-smi reads clocks from)."""
+    CLOCK_SM = 1
+
+    def __init__(self):
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+
+    def handle(self, torch_dev):
+        import torch
+        h = ctypes.c_void_p()
+        props = torch.cuda.get_device_properties(torch_dev)
+        uuid = str(getattr(props, "uuid", "") or "")
+        if uuid:
+            u = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+            if self.lib.nvmlDeviceGetHandleByUUID(u.encode(), ctypes.byref(h)) == 0:
+                return h
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        idx = torch_dev.index or 0
+        if vis and all(v.strip().isdigit() for v in vis.split(",")):
+            idx = int(vis.split(",")[idx])
+        if self.lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(idx), ctypes.byref(h)) != 0:
+            raise RuntimeError("no NVML handle")
+        return h
+
+    def clock(self, h, max_clock=False):
+        v = ctypes.c_uint()
+        f = self.lib.nvmlDeviceGetMaxClockInfo if max_clock else self.lib.nvmlDeviceGetClockInfo
+        return v.value if f(h, ctypes.c_int(self.CLOCK_SM), ctypes.byref(v)) == 0 else None
+
+    def reasons(self, h):
+        v = ctypes.c_ulonglong()
+        f = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        return v.value if f(h, ctypes.byref(v)) == 0 else 0
+
+
+class ClockSampler:
+    def __init__(self, torch_dev):
+        self.samples = []
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._h = None
+        try:
+            self.nv = _NVML()
+            self._h = self.nv.handle(torch_dev)
+            self.max_mhz = self.nv.clock(self._h, max_clock=True)
+        except Exception as e:  # no NVML: report it instead of inventing clocks
+            self.error = repr(e)
+            self._h = None
+
+    def _run(self):
+        while not self._stop.is_set():
+            c = self.nv.clock(self._h)
+            if c is not None:
+                self.samples.append((c, self.nv.reasons(self._h)))
+            time.sleep(0.002)
+
+    def __enter__(self):
+        if self._h is not None:
+            self._t = threading.Thread(target=self._run, daemon=True)
+            self._t.start()
+        return self
+
+    def __exit__(self, *a):
+        if self._h is not None:
+            self._stop.set()
+            self._t.join()
+
+    def summary(self):
+        if self._h is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "error": getattr(self, "error", "no NVML")}
+        mhz = [s[0] for s in self.samples]
+        mask = 0
+        for _, r in self.samples:
+            mask |= r
+        reasons = [name for bit, name in REASONS.items() if mask & bit and name != "gpu_idle"]
+        return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": self.max_mhz, "reasons": reasons,
+                "samples": len(mhz), "source": "NVML (nvidia-smi's library), 2 ms polling during the timed steps"}
+
+
+# ---------------------------------------------------------------------------------------
+# CPU oracle sample (the reference arm and the cpu_baseline key)
+# ---------------------------------------------------------------------------------------
+def oracle_step_sample(inp, What_ref, rows_q: int, tokens: int):
+    """Time the oracle on a bounded sample and scale it to one whole step.
+    quantize + dequantize of `rows_q` weight rows (scaled by N / rows_q), and the layer forward
+    and backward on `tokens` tokens (Y rows, dX rows, dA and dB over those tokens; scaled by
+    M / tokens).  Returns (seconds per whole step, description)."""
+    import oracle
+    M, N, K = inp.shape
+    t0 = time.perf_counter()
+    qz = oracle.nf4_quantize(inp.W[:rows_q])
+    oracle.nf4_dequantize(qz["packed"], qz["qcode"], qz["c2"], qz["mu"], rows_q, K)
+    t_q = time.perf_counter() - t0
+    sel = np.arange(tokens, dtype=np.int64)
+    t0 = time.perf_counter()
+    oracle.layer_fwd_rows(What_ref, inp.X, inp.A, inp.B, inp.alpha, sel)
+    oracle.layer_dx_rows(What_ref, inp.A, inp.B, inp.G, inp.alpha, sel)
+    oracle.layer_adapter_grads(inp.X[:tokens], inp.A, inp.B, inp.G[:tokens], inp.alpha)
+    t_l = time.perf_counter() - t0
+    step_s = t_q * (N / rows_q) + t_l * (M / tokens)
+    desc = (f"oracle (plain C, 1 thread): quantize+dequantize of {rows_q} of {N} weight rows scaled x{N / rows_q:g}, "
+            f"layer fwd+bwd on {tokens} of {M} tokens scaled x{M / tokens:g}")
+    return step_s, desc, t_q + t_l
+
+
+def make_inputs():
+    from bit_nf4_quantized_36_b300 import synth
+    c = synth.LLAMA8B_ATTN
+    return synth.layer_inputs(c["id"], c["M"], c["N"], c["K"], c["r"], c["alpha"]), c
+
+
+def run_reference(args):
+    """The reference arm: the CPU oracle, as it stands, on this host's cores."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import oracle
+    inp, c = make_inputs()
+    M, N, K, r = c["M"], c["N"], c["K"], c["r"]
+    ref = oracle.nf4_quantize(inp.W)
+    What_ref = oracle.nf4_dequantize(ref["packed"], ref["qcode"], ref["c2"], ref["mu"], N, K)
+    # size the per-step sample so that warm-up + timed steps take about two minutes
+    t1 = oracle_step_sample(inp, What_ref, 64, 1)[2]
+    tokens = int(max(1, min(16, 120.0 / (args.steps + args.warmup) / max(t1, 1e-3))))
+    rows_q = 64 * tokens
+    for _ in range(args.warmup):
+        oracle_step_sample(inp, What_ref, rows_q, tokens)
+    steps = []
+    desc = ""
+    for _ in range(args.steps):
+        s, desc, _ = oracle_step_sample(inp, What_ref, rows_q, tokens)
+        steps.append(s)
+    step_s = statistics.mean(steps)
+    value = layer_flops(M, N, K, r) / step_s / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K, "r": r, "alpha": c["alpha"]},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": 1, "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------------------
+# Our arm
+# ---------------------------------------------------------------------------------------
+def traffic_from_profile(gemm_src_sha):
+    """DRAM bytes per fused-kernel launch from the committed ncu summary, if that summary was
+    taken on the current kernel source; otherwise None."""
+    path = os.path.join(ROOT, "profiles", "fused_gemm_llama8b_attn.md")
+    try:
+        kv = {}
+        for line in open(path):
+            if ":" in line and line.strip().startswith("- "):
+                k, v = line.strip()[2:].split(":", 1)
+                kv[k.strip()] = v.strip().strip("`")
+        if kv.get("kernel_source_sha256") != gemm_src_sha:
+            return None
+        return float(kv["dram_bytes_per_launch_avg"])
+    except Exception:
+        return None
+
+
+def run_ours(args):
+    import torch
+
+    import bit_nf4_quantized_36_b300 as q
+    from bit_nf4_quantized_36_b300 import _lib, synth
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    L = _lib.load()
+    peaks = load_peaks()
+
+    c = synth.LLAMA8B_ATTN
+    M, N, K, r, alpha = c["M"], c["N"], c["K"], c["r"], c["alpha"]
+    inp = synth.layer_inputs(c["id"], M, N, K, r, alpha, sub=rank)  # each rank its own batch
+    to_bf = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+    W_h = torch.from_numpy(inp.W).pin_memory()
+    X_h, A_h, B_h, G_h = (to_bf(t).pin_memory() for t in (inp.X, inp.A, inp.B, inp.G))
+    W, X, A, B, G = (t.to(dev) for t in (W_h, X_h, A_h, B_h, G_h))
+
+    qw = q.empty_nf4(N, K, dev)
+    What = torch.empty((N, K), dtype=torch.bfloat16, device=dev)
+    Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    U = torch.empty((M, r), dtype=torch.bfloat16, device=dev)
+    dX = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+    dA = torch.empty((r, K), dtype=torch.float32, device=dev)
+    dB = torch.empty((N, r), dtype=torch.float32, device=dev)
+    ws_q = torch.empty(q.quantize_workspace_bytes(N, K), dtype=torch.uint8, device=dev)
+    ws_f = torch.empty(q.fwd_workspace_bytes(M, N, K, r), dtype=torch.uint8, device=dev)
+    ws_b = torch.empty(q.bwd_workspace_bytes(M, N, K, r), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def step():
+        q.nf4_quantize(W, out=qw, workspace=ws_q)
+        q.nf4_dequantize(qw, out=What)
+        q.qlora_linear_fwd(qw, X, A, B, alpha, Y=Y, U_save=U, workspace=ws_f)
+        q.qlora_linear_bwd(qw, X, A, B, alpha, G, U, dX=dX, dA=dA, dB=dB, workspace=ws_b)
+        if dist is not None:
+            dist.all_reduce(dA)
+            dist.all_reduce(dB)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    q.check_device_error()
+
+    # ---- timed region: K steps, L2 flushed between steps (outside the step events) ------
+    Ksteps = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(Ksteps)]
+    kev = new_events(4 * Ksteps)  # 2 fused launches per step
+    kev_arr = (ctypes.c_void_p * len(kev))(*[e.cuda_event for e in kev])
+    sampler = ClockSampler(dev)
+    barrier()
+    n0 = q.launch_count()
+    if L.qlora_set_kernel_timer(ctypes.cast(kev_arr, ctypes.c_void_p), 2 * Ksteps) != 0:
+        raise RuntimeError("qlora_set_kernel_timer rejected the events")
+    with sampler:
+        for i in range(Ksteps):
+            flush.zero_()
+            ev[i][0].record()
+            step()
+            ev[i][1].record()
+        barrier()
+    launches = q.launch_count() - n0
+    nk = L.qlora_kernel_timer_count()
+    L.qlora_set_kernel_timer(None, 0)
+    q.check_device_error()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    ms_per_step = sum(step_ms) / Ksteps
+    kt = [kev[2 * i].elapsed_time(kev[2 * i + 1]) for i in range(nk)]
+    t_fwd = statistics.mean(kt[0::2]) if nk >= 2 else float("nan")
+    t_dx = statistics.mean(kt[1::2]) if nk >= 2 else float("nan")
+    if dist is not None:
+        t = torch.tensor([ms_per_step, t_fwd, t_dx], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_per_step, t_fwd, t_dx = t.tolist()
+
+    flops = layer_flops(M, N, K, r)
+    value = world * flops / (ms_per_step * 1e-3) / 1e12
+    fl_fwd = 2.0 * M * N * K + 2.0 * M * N * r
+    fl_dx = 2.0 * M * N * K + 2.0 * M * K * r
+    achieved = (fl_fwd + fl_dx) / ((t_fwd + t_dx) * 1e-3) / 1e12
+    gemm_src = os.path.join(ROOT, "bit_nf4_quantized_36_b300", "csrc", "gemm.cu")
+    src_sha = hashlib.sha256(open(gemm_src, "rb").read()).hexdigest()
+    roofline = {"kernel": "nf4_lora_gemm_kernel (fused NF4-dequant tcgen05 GEMM; forward and dX launches)",
+                "bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops"], "traffic": traffic_from_profile(src_sha),
+                "peak_source": f"{peaks['source']} bf16 dense (burst: the kernel runs ~0.1 ms at a time)",
+                "launch_ms": {"forward": t_fwd, "dx": t_dx},
+                "algorithmic_flops_per_launch": {"forward": fl_fwd, "dx": fl_dx}}
+    clocks = sampler.summary()
+
+    # ---- end to end through the C ABI with host buffers ------------------------------------
+    e2e_steps = min(Ksteps, 20)
+    outs_h = [torch.empty_like(t, device="cpu").pin_memory() for t in (What, Y, dX, dA, dB)]
+    h2d = sum(t.numel() * t.element_size() for t in (W_h, X_h, A_h, B_h, G_h))
+    d2h = sum(t.numel() * t.element_size() for t in outs_h)
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(e2e_steps)]
+    barrier()
+    for i in range(e2e_steps):
+        e2e_ev[i][0].record()
+        for d, h in ((W, W_h), (X, X_h), (A, A_h), (B, B_h), (G, G_h)):
+            d.copy_(h, non_blocking=True)
+        step()
+        for h, d in zip(outs_h, (What, Y, dX, dA, dB)):
+            h.copy_(d, non_blocking=True)
+        e2e_ev[i][1].record()
+    barrier()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev) / e2e_steps
+    if dist is not None:
+        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = t.item()
+    e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+
+    extras = {}
+    if rank == 0 and not args.no_extras:
+        try:
+            extras = hbm_extras(q, _lib, L, dev, peaks, flush)
+        except Exception as e:  # the headline line must still print
+            extras = {"error": repr(e)}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        ref = oracle.nf4_quantize(inp.W)
+        What_ref = oracle.nf4_dequantize(ref["packed"], ref["qcode"], ref["c2"], ref["mu"], N, K)
+        step_s, desc, spent = oracle_step_sample(inp, What_ref, 1024, 128)
+        cpu = {"value": flops / step_s / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+               "sample": desc + f" ({spent:.1f} s of CPU work)", "ms_per_step": step_s * 1e3}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": Ksteps,
+                "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": {"workload": WORKLOAD, "M_per_gpu": M, "N": N, "K": K, "r": r, "alpha": alpha,
+                           "step": "nf4_quantize + nf4_dequantize + qlora_linear_fwd + qlora_linear_bwd",
+                           "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write, outside the step events)",
+                           "parallelism": f"dp{world}"},
+                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+                "gpu_launches_per_step": launches / Ksteps, "clocks": clocks,
+                "step_ms_min_max": [min(step_ms), max(step_ms)], "hbm_kernels": extras}
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def hbm_extras(q, _lib, L, dev, peaks, flush):
+    """Secondary numbers for the HBM-bound kernels on a Llama-70B MLP matrix (28672 x 8192):
+    nf4_dequantize and nf4_quantize GB/s, and the small-M forward (decode) GB/s."""
+    import torch
+    from bit_nf4_quantized_36_b300 import synth
+    rows, cols = 28672, 8192
+    n = rows * cols
+    storage = q.nf4_storage_bytes(rows, cols)
+    W = synth.sweep_weight_gpu(0, 4, rows, cols)
+    qw = q.nf4_quantize(W)
+    What = q.nf4_dequantize(qw)
+    ws = torch.empty(q.quantize_workspace_bytes(rows, cols), dtype=torch.uint8, device=dev)
+    torch.cuda.synchronize()
+
+    def timed(fn, reps=10):
+        ts = []
+        for _ in range(reps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        return statistics.median(ts)
+
+    out = {}
+    t = timed(lambda: q.nf4_dequantize(qw, out=What))
+    byt = storage + 2 * n
+    out["dequantize"] = {"matrix": f"{rows}x{cols}", "ms": t, "GB/s": byt / t / 1e6,
+                         "frac_hbm": byt / t / 1e6 / peaks["hbm_gbs"], "algorithmic_bytes": byt}
+    t = timed(lambda: q.nf4_quantize(W, out=qw, workspace=ws))
+    byt = 4 * n + storage
+    out["quantize"] = {"matrix": f"{rows}x{cols}", "ms": t, "GB/s": byt / t / 1e6,
+                       "frac_hbm": byt / t / 1e6 / peaks["hbm_gbs"], "algorithmic_bytes": byt}
+    del W, What
+    # decode-like forward: M tokens through the up projection (N = 28672, K = 8192), r = 16
+    r = 16
+    A = (torch.randn((r, cols), device=dev) / cols ** 0.5).to(torch.bfloat16)
+    B = (torch.randn((rows, r), device=dev) * 0.01).to(torch.bfloat16)
+    dec = {}
+    for M in (1, 8, 32):
+        X = torch.randn((M, cols), device=dev).to(torch.bfloat16)
+        Y = torch.empty((M, rows), dtype=torch.bfloat16, device=dev)
+        U = torch.empty((M, r), dtype=torch.bfloat16, device=dev)
+        wsf = torch.empty(q.fwd_workspace_bytes(M, rows, cols, r), dtype=torch.uint8, device=dev)
+        t = timed(lambda: q.qlora_linear_fwd(qw, X, A, B, 32.0, Y=Y, U_save=U, workspace=wsf))
+        kev = new_events(20)
+        arr = (ctypes.c_void_p * 20)(*[e.cuda_event for e in kev])
+        if L.qlora_set_kernel_timer(ctypes.cast(arr, ctypes.c_void_p), 10) != 0:
+            raise RuntimeError("qlora_set_kernel_timer rejected the events")
+        for _ in range(10):
+            flush.zero_()
+            q.qlora_linear_fwd(qw, X, A, B, 32.0, Y=Y, U_save=U, workspace=wsf)
+        torch.cuda.synchronize()
+        L.qlora_set_kernel_timer(None, 0)
+        tk = statistics.median(kev[2 * i].elapsed_time(kev[2 * i + 1]) for i in range(10))
+        byt = storage + 2 * r * (rows + cols) + 2 * M * (rows + cols)
+        dec[f"M={M}"] = {"call_ms": t, "fused_kernel_ms": tk, "GB/s_kernel": byt / tk / 1e6,
+                         "frac_hbm_kernel": byt / tk / 1e6 / peaks["hbm_gbs"], "GB/s_call": byt / t / 1e6}
+    out["decode_forward_28672x8192_r16"] = dec
+    out["hbm_peak_GB/s"] = f"{peaks['hbm_gbs']} ({peaks['source']})"
+    return out
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

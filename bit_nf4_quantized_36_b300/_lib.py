@@ -18,6 +18,7 @@ EXPORTS = (
     "qlora_nf4_storage_bytes", "qlora_quantize_workspace_bytes", "qlora_fwd_workspace_bytes",
     "qlora_bwd_workspace_bytes", "nf4_quantize", "nf4_dequantize", "qlora_linear_fwd", "qlora_linear_bwd",
     "qlora_check_device_error", "qlora_status_string", "qlora_launch_count", "qlora_nf4_levels",
+    "qlora_set_kernel_timer", "qlora_kernel_timer_count",
 )
 
 
@@ -52,6 +53,8 @@ def load():
         "qlora_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "qlora_launch_count": (ctypes.c_uint64, []),
         "qlora_nf4_levels": (None, [P]),
+        "qlora_set_kernel_timer": (ctypes.c_int, [P, I32]),
+        "qlora_kernel_timer_count": (I32, []),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)

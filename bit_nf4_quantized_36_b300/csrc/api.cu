@@ -1,6 +1,7 @@
 // api.cu -- the C ABI of libqlora (include/qlora.h): argument checks, workspace layout,
 // TMA descriptor setup and the launch sequence of each call.  All arithmetic of the layer runs
 // in the kernels of quant.cu and gemm.cu.
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstring>
@@ -16,6 +17,29 @@ namespace qlora {
 
 static std::atomic<uint64_t> g_launches{0};
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+// optional event pairs around the fused kernel (benchmark instrumentation)
+static void **g_timer_events = nullptr;
+static int32_t g_timer_cap = 0;
+static std::atomic<int32_t> g_timer_n{0};
+
+static cudaError_t timed_fused(bool dx, const CUtensorMap &mc, const CUtensorMap &ms, const CUtensorMap &ma,
+                               const CUtensorMap &ml, const FusedArgs &fa, const FusedPlan &fp, cudaStream_t st) {
+    void **ev = g_timer_events;
+    int32_t i = -1;
+    if (ev) {
+        i = g_timer_n.fetch_add(1);
+        if (i >= g_timer_cap) i = -1;
+    }
+    // a failed record (e.g. a NULL handle) must not be reported as the kernel's launch error
+    if (i >= 0 && cudaEventRecord(static_cast<cudaEvent_t>(ev[2 * i]), st) != cudaSuccess) {
+        cudaGetLastError();
+        i = -1;
+    }
+    cudaError_t e = launch_fused(dx, mc, ms, ma, ml, fa, fp, st);
+    if (i >= 0 && cudaEventRecord(static_cast<cudaEvent_t>(ev[2 * i + 1]), st) != cudaSuccess) cudaGetLastError();
+    return e;
+}
 
 // ---------------------------------------------------------------------------------------
 // NF4 tables: the level constants and the exact decision thresholds of the nearest-level
@@ -109,6 +133,11 @@ static bool map_codes(CUtensorMap *m, const void *codes, int64_t N, int64_t K, b
     return make_map(m, codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)K / 2, (uint64_t)N, (uint64_t)K / 2,
                     dx ? 64u : 32u, dx ? 64u : 128u, false);
 }
+// rebuilt block scales, transposed [KB][N] fp32
+static bool map_scales(CUtensorMap *m, const float *sT, int64_t N, int64_t KB, bool dx) {
+    return make_map(m, sT, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, (uint64_t)N, (uint64_t)KB, (uint64_t)N, dx ? 64u : 128u,
+                    dx ? 2u : 1u, false);
+}
 
 // ---------------------------------------------------------------------------------------
 // Workspace layouts (one function per call, used by the size query and by the call)
@@ -132,34 +161,41 @@ static QuantWs quant_ws(int64_t rows, int64_t cols) {
 }
 
 struct LayerWs {
-    int r64;
+    int r8, r64;
     FusedPlan fp;
     ProjPlan pu, pv, pda, pdb;
-    size_t off_apad, off_bpad, off_u, off_v, off_proj, off_main, total;
+    int ncounters;
+    size_t off_scales, off_counters, off_u, off_v, off_bpad, off_proj, off_main, total;
 };
 static LayerWs layer_ws(int64_t M, int64_t N, int64_t K, int r, bool bwd, int num_sms) {
     LayerWs w{};
+    w.r8 = ((r + 7) / 8) * 8;
     w.r64 = ((r + 63) / 64) * 64;
-    size_t off = 0;
-    w.off_apad = off;
-    off += align256((size_t)w.r64 * K * 2);
-    w.off_bpad = off;
-    off += align256((size_t)N * w.r64 * 2);
-    w.off_u = off;
-    off += align256((size_t)M * w.r64 * 2);
+    const int64_t KB = K / 64;
     w.pu = plan_proj(M, K, w.r64, num_sms);
     size_t proj = w.pu.partial_bytes;
+    w.ncounters = w.pu.tiles;
     if (bwd) {
-        w.off_v = off;
-        off += align256((size_t)M * w.r64 * 2);
         w.pv = plan_proj(M, N, w.r64, num_sms);
         w.pda = plan_proj(K, M, w.r64, num_sms);
         w.pdb = plan_proj(N, M, w.r64, num_sms);
         proj = std::max(std::max(proj, w.pv.partial_bytes), std::max(w.pda.partial_bytes, w.pdb.partial_bytes));
+        w.ncounters += w.pv.tiles + w.pda.tiles + w.pdb.tiles;
         w.fp = plan_fused(M, K, (N + 63) / 64, w.r64, num_sms);
     } else {
         w.fp = plan_fused(M, N, K / 64, w.r64, num_sms);
     }
+    size_t off = 0;
+    w.off_scales = off;
+    off += align256((size_t)KB * N * 4);
+    w.off_counters = off;
+    off += align256((size_t)w.ncounters * 4);
+    w.off_u = off;
+    off += align256((size_t)M * w.r8 * 2);
+    w.off_v = off;
+    if (bwd) off += align256((size_t)M * w.r8 * 2);
+    w.off_bpad = off;
+    if (bwd && r % 8 != 0) off += align256((size_t)N * w.r8 * 2);
     w.off_proj = off;
     off += align256(proj);
     w.off_main = off;
@@ -264,6 +300,45 @@ qlora_status nf4_dequantize(const qlora_nf4_tensor *q, uint16_t *W_out, void *st
                                        W_out, tables(), num_sms_current(), static_cast<cudaStream_t>(stream)));
 }
 
+static ProjArgs proj_args(const ProjPlan &pl, int64_t Mp, const LayerWs &w, int r, int mode, float scale,
+                          float *partial, uint32_t *counters) {
+    ProjArgs a{};
+    a.Mp = (int)Mp;
+    a.r64 = w.r64;
+    a.r = r;
+    a.tiles = pl.tiles;
+    a.splits = pl.splits;
+    a.ktiles = pl.ktiles;
+    a.mode = mode;
+    a.scale = scale;
+    a.partial = partial;
+    a.counters = counters;
+    return a;
+}
+
+static FusedArgs fused_args(const qlora_nf4_tensor *W, int64_t M, const LayerWs &w, int r, const uint16_t *lora_src,
+                            int64_t lora_ld, uint16_t *out, float *partial, int64_t wdim) {
+    FusedArgs fa{};
+    fa.N = W->rows;
+    fa.K = W->cols;
+    fa.KB = (int32_t)(W->cols / 64);
+    fa.M = (int32_t)M;
+    fa.lora_src = lora_src;
+    fa.lora_ld = lora_ld;
+    fa.r = r;
+    fa.BN = w.fp.BN;
+    fa.w_tiles = w.fp.w_tiles;
+    fa.m_tiles = w.fp.m_tiles;
+    fa.splits = w.fp.splits;
+    fa.kt_main = w.fp.kt_main;
+    fa.kt_lora = w.fp.kt_lora;
+    fa.out = out;
+    fa.partial = partial;
+    fa.wdim = wdim;
+    fa.tab = tables();
+    return fa;
+}
+
 qlora_status qlora_linear_fwd(const qlora_nf4_tensor *W, const uint16_t *X, int64_t M, const uint16_t *A,
                               const uint16_t *B, int32_t r, float alpha, uint16_t *Y, uint16_t *U_save, void *ws,
                               size_t ws_bytes, void *stream) {
@@ -271,54 +346,38 @@ qlora_status qlora_linear_fwd(const qlora_nf4_tensor *W, const uint16_t *X, int6
     if (s != QLORA_OK) return s;
     if (!Y) return QLORA_ERR_INVALID_ARG;
     if (!aligned16(Y) || (U_save && !aligned16(U_save))) return QLORA_ERR_MISALIGNED;
-    const int64_t N = W->rows, K = W->cols;
+    const int64_t N = W->rows, K = W->cols, KB = K / 64;
     const int sms = num_sms_current();
     const LayerWs w = layer_ws(M, N, K, r, false, sms);
     if (!ws || ws_bytes < w.total || !aligned16(ws)) return QLORA_ERR_WORKSPACE;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     uint8_t *base = static_cast<uint8_t *>(ws);
-    uint16_t *Apad = reinterpret_cast<uint16_t *>(base + w.off_apad);
-    uint16_t *Bpad = reinterpret_cast<uint16_t *>(base + w.off_bpad);
+    float *scalesT = reinterpret_cast<float *>(base + w.off_scales);
+    uint32_t *counters = reinterpret_cast<uint32_t *>(base + w.off_counters);
     uint16_t *U = reinterpret_cast<uint16_t *>(base + w.off_u);
     float *proj = reinterpret_cast<float *>(base + w.off_proj);
     float *mainp = reinterpret_cast<float *>(base + w.off_main);
     const float scale = alpha / (float)r;
 
-    CUtensorMap mX_k, mA_k, mCodes, mX_act, mU_act;
-    if (!map_bf16(&mX_k, X, K, M, 64, 128) || !map_bf16(&mA_k, Apad, K, w.r64, 64, w.r64) ||
-        !map_codes(&mCodes, W->codes, N, K, false) || !map_bf16(&mX_act, X, K, M, 64, w.fp.BN) ||
-        !map_bf16(&mU_act, U, w.r64, M, 64, w.fp.BN))
+    CUtensorMap mX_k, mA_k, mCodes, mScales, mX_act, mU_act;
+    if (!map_bf16(&mX_k, X, K, M, 64, 128) || !map_bf16(&mA_k, A, K, r, 64, w.r64) ||
+        !map_codes(&mCodes, W->codes, N, K, false) || !map_scales(&mScales, scalesT, N, KB, false) ||
+        !map_bf16(&mX_act, X, K, M, 64, w.fp.BN) || !map_bf16(&mU_act, U, w.r8, M, 64, w.fp.BN))
         return QLORA_ERR_CUDA;
 
     cudaError_t e;
-    if ((e = launch_pad_2d(A, r, K, Apad, w.r64, K, sms, st)) != cudaSuccess) return from_cuda(e);
-    if ((e = launch_pad_2d(B, N, r, Bpad, N, w.r64, sms, st)) != cudaSuccess) return from_cuda(e);
-    // U = bf16(s * X A^T)
-    if ((e = launch_proj(false, false, mX_k, mA_k, M, K, w.r64, w.pu, proj, st)) != cudaSuccess) return from_cuda(e);
-    if ((e = launch_proj_finalize(0, proj, w.pu.splits, M, w.r64, r, scale, U, U_save, nullptr, sms, st)) != cudaSuccess)
+    if ((e = launch_dq_scales_t(W->scale_codes, W->scale_scales, W->scale_offset, N, (int)KB, scalesT, counters,
+                                w.ncounters, st)) != cudaSuccess)
         return from_cuda(e);
-    // Y = X W^T + U Bp^T
-    FusedArgs fa{};
-    fa.scale_codes = W->scale_codes;
-    fa.scale_scales = W->scale_scales;
-    fa.scale_offset = W->scale_offset;
-    fa.N = N;
-    fa.K = K;
-    fa.KB = (int32_t)(K / 64);
-    fa.M = (int32_t)M;
-    fa.lora_rows = Bpad;
-    fa.r64 = w.r64;
-    fa.BN = w.fp.BN;
-    fa.w_tiles = w.fp.w_tiles;
-    fa.m_tiles = w.fp.m_tiles;
-    fa.splits = w.fp.splits;
-    fa.kt_main = w.fp.kt_main;
-    fa.kt_lora = w.fp.kt_lora;
-    fa.out = Y;
-    fa.partial = mainp;
-    fa.wdim = N;
-    fa.tab = tables();
-    if ((e = launch_fused(false, mCodes, mX_act, mU_act, fa, w.fp, st)) != cudaSuccess) return from_cuda(e);
+    // U = bf16(s * X A^T)  [M, r8] (+ U_save [M, r])
+    ProjArgs pu = proj_args(w.pu, M, w, r, 0, scale, proj, counters);
+    pu.out_h = U;
+    pu.ld_h = w.r8;
+    pu.out_h2 = U_save;
+    if ((e = launch_proj(false, false, mX_k, mA_k, pu, st)) != cudaSuccess) return from_cuda(e);
+    // Y = X W^T + U B^T
+    const FusedArgs fa = fused_args(W, M, w, r, B, r, Y, mainp, N);
+    if ((e = timed_fused(false, mCodes, mScales, mX_act, mU_act, fa, w.fp, st)) != cudaSuccess) return from_cuda(e);
     if (w.fp.splits > 1 && (e = launch_splitk_reduce(mainp, w.fp.splits, M, N, Y, sms, st)) != cudaSuccess)
         return from_cuda(e);
     return QLORA_OK;
@@ -332,82 +391,85 @@ qlora_status qlora_linear_bwd(const qlora_nf4_tensor *W, const uint16_t *X, int6
     if (!dY || !dX || !dA || !dB) return QLORA_ERR_INVALID_ARG;
     if (!aligned16(dY) || !aligned16(dX) || !aligned16(dA) || !aligned16(dB) || (U_saved && !aligned16(U_saved)))
         return QLORA_ERR_MISALIGNED;
-    const int64_t N = W->rows, K = W->cols;
+    const int64_t N = W->rows, K = W->cols, KB = K / 64;
     const int sms = num_sms_current();
     const LayerWs w = layer_ws(M, N, K, r, true, sms);
     if (!ws || ws_bytes < w.total || !aligned16(ws)) return QLORA_ERR_WORKSPACE;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     uint8_t *base = static_cast<uint8_t *>(ws);
-    uint16_t *Apad = reinterpret_cast<uint16_t *>(base + w.off_apad);
-    uint16_t *Bpad = reinterpret_cast<uint16_t *>(base + w.off_bpad);
+    float *scalesT = reinterpret_cast<float *>(base + w.off_scales);
+    uint32_t *counters = reinterpret_cast<uint32_t *>(base + w.off_counters);
     uint16_t *U = reinterpret_cast<uint16_t *>(base + w.off_u);
     uint16_t *V = reinterpret_cast<uint16_t *>(base + w.off_v);
+    uint16_t *Bpad = reinterpret_cast<uint16_t *>(base + w.off_bpad);
     float *proj = reinterpret_cast<float *>(base + w.off_proj);
     float *mainp = reinterpret_cast<float *>(base + w.off_main);
     const float scale = alpha / (float)r;
+    const bool r_vec = (r % 8) == 0;
+    // U as a TMA-readable [M, ru] tensor: the caller's copy when its rows are 16-byte multiples
+    const uint16_t *Uq = (U_saved && r_vec) ? U_saved : U;
+    const int64_t ru = (U_saved && r_vec) ? r : w.r8;
+    const uint16_t *Bq = r_vec ? B : Bpad;
+    const int64_t rb = r_vec ? r : w.r8;
 
-    CUtensorMap mX_k, mA_k, mG_k, mBpad_mn, mX_mn, mV_mn, mG_mn, mU_mn, mCodes, mG_act, mV_act;
-    if (!map_bf16(&mX_k, X, K, M, 64, 128) || !map_bf16(&mA_k, Apad, K, w.r64, 64, w.r64) ||
-        !map_bf16(&mG_k, dY, N, M, 64, 128) || !map_bf16(&mBpad_mn, Bpad, w.r64, N, 64, 64) ||
-        !map_bf16(&mX_mn, X, K, M, 64, 64) || !map_bf16(&mV_mn, V, w.r64, M, 64, 64) ||
-        !map_bf16(&mG_mn, dY, N, M, 64, 64) || !map_bf16(&mU_mn, U, w.r64, M, 64, 64) ||
-        !map_codes(&mCodes, W->codes, N, K, true) || !map_bf16(&mG_act, dY, N, M, 64, w.fp.BN) ||
-        !map_bf16(&mV_act, V, w.r64, M, 64, w.fp.BN))
+    CUtensorMap mX_k, mA_k, mG_k, mB_mn, mX_mn, mV_mn, mG_mn, mU_mn, mCodes, mScales, mG_act, mV_act;
+    if (!map_bf16(&mX_k, X, K, M, 64, 128) || !map_bf16(&mA_k, A, K, r, 64, w.r64) ||
+        !map_bf16(&mG_k, dY, N, M, 64, 128) || !map_bf16(&mB_mn, Bq, rb, N, 64, 64) ||
+        !map_bf16(&mX_mn, X, K, M, 64, 64) || !map_bf16(&mV_mn, V, w.r8, M, 64, 64) ||
+        !map_bf16(&mG_mn, dY, N, M, 64, 64) || !map_bf16(&mU_mn, Uq, ru, M, 64, 64) ||
+        !map_codes(&mCodes, W->codes, N, K, true) || !map_scales(&mScales, scalesT, N, KB, true) ||
+        !map_bf16(&mG_act, dY, N, M, 64, w.fp.BN) || !map_bf16(&mV_act, V, w.r8, M, 64, w.fp.BN))
         return QLORA_ERR_CUDA;
 
+    uint32_t *cnt_u = counters, *cnt_v = cnt_u + w.pu.tiles, *cnt_da = cnt_v + w.pv.tiles;
+    uint32_t *cnt_db = cnt_da + w.pda.tiles;
     cudaError_t e;
-    if ((e = launch_pad_2d(A, r, K, Apad, w.r64, K, sms, st)) != cudaSuccess) return from_cuda(e);
-    if ((e = launch_pad_2d(B, N, r, Bpad, N, w.r64, sms, st)) != cudaSuccess) return from_cuda(e);
+    if ((e = launch_dq_scales_t(W->scale_codes, W->scale_scales, W->scale_offset, N, (int)KB, scalesT, counters,
+                                w.ncounters, st)) != cudaSuccess)
+        return from_cuda(e);
+    if (!r_vec && (e = launch_pad_2d(B, N, r, Bpad, N, w.r8, sms, st)) != cudaSuccess) return from_cuda(e);
     // U: the forward's saved copy, or recomputed
     if (U_saved) {
-        if ((e = launch_pad_2d(U_saved, M, r, U, M, w.r64, sms, st)) != cudaSuccess) return from_cuda(e);
+        if (!r_vec && (e = launch_pad_2d(U_saved, M, r, U, M, w.r8, sms, st)) != cudaSuccess) return from_cuda(e);
     } else {
-        if ((e = launch_proj(false, false, mX_k, mA_k, M, K, w.r64, w.pu, proj, st)) != cudaSuccess) return from_cuda(e);
-        if ((e = launch_proj_finalize(0, proj, w.pu.splits, M, w.r64, r, scale, U, nullptr, nullptr, sms, st)) !=
-            cudaSuccess)
-            return from_cuda(e);
+        ProjArgs pu = proj_args(w.pu, M, w, r, 0, scale, proj, cnt_u);
+        pu.out_h = U;
+        pu.ld_h = w.r8;
+        if ((e = launch_proj(false, false, mX_k, mA_k, pu, st)) != cudaSuccess) return from_cuda(e);
     }
-    // V = bf16(s * G B)
-    if ((e = launch_proj(false, true, mG_k, mBpad_mn, M, N, w.r64, w.pv, proj, st)) != cudaSuccess) return from_cuda(e);
-    if ((e = launch_proj_finalize(0, proj, w.pv.splits, M, w.r64, r, scale, V, nullptr, nullptr, sms, st)) !=
-        cudaSuccess)
-        return from_cuda(e);
-    // dX = G W^ + V Ap
-    FusedArgs fa{};
-    fa.scale_codes = W->scale_codes;
-    fa.scale_scales = W->scale_scales;
-    fa.scale_offset = W->scale_offset;
-    fa.N = N;
-    fa.K = K;
-    fa.KB = (int32_t)(K / 64);
-    fa.M = (int32_t)M;
-    fa.lora_rows = Apad;
-    fa.r64 = w.r64;
-    fa.BN = w.fp.BN;
-    fa.w_tiles = w.fp.w_tiles;
-    fa.m_tiles = w.fp.m_tiles;
-    fa.splits = w.fp.splits;
-    fa.kt_main = w.fp.kt_main;
-    fa.kt_lora = w.fp.kt_lora;
-    fa.out = dX;
-    fa.partial = mainp;
-    fa.wdim = K;
-    fa.tab = tables();
-    if ((e = launch_fused(true, mCodes, mG_act, mV_act, fa, w.fp, st)) != cudaSuccess) return from_cuda(e);
+    // V = bf16(s * G B)  [M, r8]
+    ProjArgs pv = proj_args(w.pv, M, w, r, 0, scale, proj, cnt_v);
+    pv.out_h = V;
+    pv.ld_h = w.r8;
+    if ((e = launch_proj(false, true, mG_k, mB_mn, pv, st)) != cudaSuccess) return from_cuda(e);
+    // dX = G W^ + V A
+    const FusedArgs fa = fused_args(W, M, w, r, A, K, dX, mainp, K);
+    if ((e = timed_fused(true, mCodes, mScales, mG_act, mV_act, fa, w.fp, st)) != cudaSuccess) return from_cuda(e);
     if (w.fp.splits > 1 && (e = launch_splitk_reduce(mainp, w.fp.splits, M, K, dX, sms, st)) != cudaSuccess)
         return from_cuda(e);
-    // dA = V^T X  -> D[k, j] = sum_m X[m, k] V[m, j]
-    if ((e = launch_proj(true, true, mX_mn, mV_mn, K, M, w.r64, w.pda, proj, st)) != cudaSuccess) return from_cuda(e);
-    if ((e = launch_proj_finalize(1, proj, w.pda.splits, K, w.r64, r, 1.0f, nullptr, nullptr, dA, sms, st)) !=
-        cudaSuccess)
-        return from_cuda(e);
-    // dB = G^T U  -> D[n, j] = sum_m G[m, n] U[m, j]
-    if ((e = launch_proj(true, true, mG_mn, mU_mn, N, M, w.r64, w.pdb, proj, st)) != cudaSuccess) return from_cuda(e);
-    if ((e = launch_proj_finalize(2, proj, w.pdb.splits, N, w.r64, r, 1.0f, nullptr, nullptr, dB, sms, st)) !=
-        cudaSuccess)
-        return from_cuda(e);
+    // dA = V^T X  (D[k, j] = sum_m X[m, k] V[m, j], stored transposed)
+    ProjArgs pa = proj_args(w.pda, K, w, r, 1, 1.0f, proj, cnt_da);
+    pa.out_f = dA;
+    if ((e = launch_proj(true, true, mX_mn, mV_mn, pa, st)) != cudaSuccess) return from_cuda(e);
+    // dB = G^T U  (D[n, j] = sum_m G[m, n] U[m, j])
+    ProjArgs pb = proj_args(w.pdb, N, w, r, 2, 1.0f, proj, cnt_db);
+    pb.out_f = dB;
+    if ((e = launch_proj(true, true, mG_mn, mU_mn, pb, st)) != cudaSuccess) return from_cuda(e);
     return QLORA_OK;
 }
+
+qlora_status qlora_set_kernel_timer(void **events, int32_t capacity) {
+    if (capacity < 0) return QLORA_ERR_INVALID_ARG;
+    for (int32_t i = 0; events && i < 2 * capacity; ++i)
+        if (!events[i]) return QLORA_ERR_INVALID_ARG;
+    g_timer_events = nullptr;
+    g_timer_cap = events ? capacity : 0;
+    g_timer_n.store(0);
+    g_timer_events = events;
+    return QLORA_OK;
+}
+
+int32_t qlora_kernel_timer_count(void) { return std::min(g_timer_n.load(), g_timer_cap); }
 
 qlora_status qlora_check_device_error(void *stream) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return QLORA_ERR_CUDA;

@@ -28,6 +28,8 @@ namespace qlora {
 static constexpr int kStages = 4;
 static constexpr uint32_t kATileBytes = 128u * 128u;  // 128 rows x 64 bf16
 static constexpr uint32_t kCodesTileBytes = 4096u;    // 128 rows x 32 B or 64 rows x 64 B
+static constexpr uint32_t kScaleTileBytes = 512u;     // 128 (or 2 x 64) fp32 block scales
+static constexpr uint32_t kCStageBytes = kCodesTileBytes + kScaleTileBytes;
 static constexpr int kFusedThreads = 448;              // 14 warps
 static constexpr int kDecodeWarp0 = 6;                 // warps 6..13 decode
 static constexpr int kEpiWarp0 = 2;                    // warps 2..5 epilogue
@@ -83,9 +85,23 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
                  : "memory");
 }
 
-__device__ __forceinline__ float dq_block_scale(const FusedArgs &p, int64_t b, float mu) {
-    const float c2 = __ldg(p.scale_scales + (b >> 8));
-    return __fmaf_rn((float)__ldg(p.scale_codes + b), __fdiv_rn(c2, 127.0f), mu);
+// 32 consecutive bf16 of one row starting at column j0, zero beyond column `jmax` (exclusive).
+__device__ __forceinline__ void load_row32(const uint16_t *row, int64_t j0, int64_t jmax, bool vec_ok, uint4 (&v)[4]) {
+    if (vec_ok && j0 + 32 <= jmax) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = __ldg(reinterpret_cast<const uint4 *>(row + j0) + i);
+        return;
+    }
+    uint32_t w[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+        const int64_t j = j0 + 2 * e;
+        const uint32_t lo = (j < jmax) ? (uint32_t)__ldg(row + j) : 0u;
+        const uint32_t hi = (j + 1 < jmax) ? (uint32_t)__ldg(row + j + 1) : 0u;
+        w[e] = lo | (hi << 16);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
 }
 
 // Warp-uniform bounded wait: lane 0 polls, the result is broadcast, and __syncwarp orders the
@@ -116,8 +132,9 @@ __device__ __forceinline__ UnitInfo unit_info(const FusedArgs &p, int u) {
 
 template <bool kDX>
 __global__ void __launch_bounds__(kFusedThreads, 1)
-    nf4_lora_gemm_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant__ CUtensorMap map_act,
-                         const __grid_constant__ CUtensorMap map_lora, const FusedArgs p) {
+    nf4_lora_gemm_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant__ CUtensorMap map_scales,
+                         const __grid_constant__ CUtensorMap map_act, const __grid_constant__ CUtensorMap map_lora,
+                         const FusedArgs p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -125,8 +142,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     uint8_t *sA = smem;
     uint8_t *sB = sA + kStages * kATileBytes;
     uint8_t *sC = sB + kStages * b_bytes;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sC + kStages * kCodesTileBytes);
-    uint64_t *full_c = bars;                 // codes landed (or LoRA k-step announced)
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sC + kStages * kCStageBytes);
+    uint64_t *full_c = bars;                 // codes + scales landed (or LoRA k-step announced)
     uint64_t *full_b = bars + kStages;       // activation tile landed
     uint64_t *full_a = bars + 2 * kStages;   // decoded weight tile written
     uint64_t *empty = bars + 3 * kStages;    // MMAs reading the stage finished
@@ -143,7 +160,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full_c[s], 1);
             mbar_init(&full_b[s], 1);
-            mbar_init(&full_a[s], 8);
+            mbar_init(&full_a[s], 4);  // the four warps of the stage's decode group
             mbar_init(&empty[s], 1);
         }
         for (int a = 0; a < 2; ++a) {
@@ -169,6 +186,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         // ------------------------------ TMA producer ------------------------------------
         if (lane == 0) {
             tma_prefetch_desc(&map_codes);
+            tma_prefetch_desc(&map_scales);
             tma_prefetch_desc(&map_act);
             tma_prefetch_desc(&map_lora);
             int s = 0;
@@ -184,11 +202,15 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
                     const bool lora = (ui.kt0 + j) >= ui.kt1;
                     if (!lora) {
                         const int kt = ui.kt0 + j;
-                        mbar_arrive_expect_tx(&full_c[s], kCodesTileBytes);
-                        if (kDX)
-                            tma_load_2d(sC + s * kCodesTileBytes, &map_codes, &full_c[s], ui.w_tile * 64, kt * 64);
-                        else
-                            tma_load_2d(sC + s * kCodesTileBytes, &map_codes, &full_c[s], kt * 32, ui.w_tile * 128);
+                        uint8_t *dc = sC + s * kCStageBytes;
+                        mbar_arrive_expect_tx(&full_c[s], kCStageBytes);
+                        if (kDX) {
+                            tma_load_2d(dc, &map_codes, &full_c[s], ui.w_tile * 64, kt * 64);
+                            tma_load_2d(dc + kCodesTileBytes, &map_scales, &full_c[s], kt * 64, ui.w_tile * 2);
+                        } else {
+                            tma_load_2d(dc, &map_codes, &full_c[s], kt * 32, ui.w_tile * 128);
+                            tma_load_2d(dc + kCodesTileBytes, &map_scales, &full_c[s], ui.w_tile * 128, kt);
+                        }
                         mbar_arrive_expect_tx(&full_b[s], b_bytes);
                         tma_load_2d(sB + s * b_bytes, &map_act, &full_b[s], kt * 64, ui.m_tile * p.BN);
                     } else {
@@ -299,85 +321,88 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         }
     } else {
         // ------------------------------ decode warps -------------------------------------
-        const int t = threadIdx.x - kDecodeWarp0 * 32;  // 0..255
-        const float mu = __ldg(p.scale_offset);
+        // Two groups of four warps take alternate pipeline stages (stage s always goes to
+        // group s % 2, kStages being even).  Each thread expands one 128-byte smem row: the 64
+        // weights of one NF4 block, so the block's 16-entry table is built once per 64 weights.
+        const int t = (threadIdx.x - kDecodeWarp0 * 32) & 127;  // row slot 0..127
+        const int group = (threadIdx.x - kDecodeWarp0 * 32) >> 7;
         const uint32_t a_base = smem_u32(sA);
+        const bool lora_vec = (p.lora_ld % 8) == 0;
+        // per-thread geometry of the 128-row A tile
+        uint32_t row_off, code_off, scale_off;
+        int nl = 0, kbl = 0;
+        if (!kDX) {
+            row_off = (uint32_t)t * 128u;
+            code_off = (uint32_t)t * 32u;
+            scale_off = kCodesTileBytes + (uint32_t)t * 4u;
+        } else {
+            nl = t >> 1;
+            kbl = t & 1;
+            row_off = (uint32_t)kbl * 8192u + (uint32_t)nl * 128u;
+            code_off = (uint32_t)nl * 64u + (uint32_t)kbl * 32u;
+            scale_off = kCodesTileBytes + (uint32_t)(kbl * 64 + nl) * 4u;
+        }
+        const uint32_t r7 = (row_off >> 7) & 7u;  // swizzle phase of this row (tiles are 1024-aligned)
         int s = 0;
         uint32_t ph = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
             const UnitInfo ui = unit_info(p, u);
+            const int64_t n_fwd = (int64_t)ui.w_tile * 128 + t;  // forward: weight row of this thread
+            const int kblock = ui.w_tile * 2 + kbl;              // backward: 64-column block along K
             for (int j = 0; j < ui.nk; ++j) {
-                const bool lora = (ui.kt0 + j) >= ui.kt1;
-                const int kt = lora ? j - (ui.kt1 - ui.kt0) : ui.kt0 + j;
-                // this thread's 32 weights: a 128-byte smem row, chunks half*4 .. half*4+3
-                int64_t wrow;       // weight row n (main) or LoRA row
-                int64_t blk = -1;   // NF4 block index, -1 if out of range
-                uint32_t row_addr;  // smem byte address of the 128-byte row
-                uint32_t code_off;  // byte offset of the 16 code bytes in the codes tile
-                const uint16_t *lsrc = nullptr;
-                const int half = t & 1;
-                if (!kDX) {
-                    const int row = t >> 1;
-                    wrow = (int64_t)ui.w_tile * 128 + row;
-                    row_addr = a_base + (uint32_t)s * kATileBytes + (uint32_t)row * 128u;
-                    code_off = (uint32_t)row * 32u + (uint32_t)half * 16u;
-                    if (wrow < p.N) {
-                        if (!lora) blk = wrow * p.KB + kt;
-                        else lsrc = p.lora_rows + wrow * p.r64 + kt * 64 + half * 32;
-                    }
-                } else {
-                    const int nl = t >> 2, kbl = (t >> 1) & 1;
-                    const int kblock = ui.w_tile * 2 + kbl;  // 64-column block along K
-                    row_addr = a_base + (uint32_t)s * kATileBytes + (uint32_t)kbl * 8192u + (uint32_t)nl * 128u;
-                    code_off = (uint32_t)nl * 64u + (uint32_t)kbl * 32u + (uint32_t)half * 16u;
-                    if (!lora) {
-                        wrow = (int64_t)kt * 64 + nl;
-                        if (wrow < p.N && kblock < p.KB) blk = wrow * p.KB + kblock;
+                const int my_stage = (s & 1) == group;
+                if (my_stage) {
+                    const bool lora = (ui.kt0 + j) >= ui.kt1;
+                    const int kt = lora ? j - (ui.kt1 - ui.kt0) : ui.kt0 + j;
+                    bool valid;
+                    uint4 lv[8];
+                    if (!kDX) {
+                        valid = n_fwd < p.N;
+                        if (lora && valid) {
+                            const uint16_t *row = p.lora_src + n_fwd * p.lora_ld;
+                            load_row32(row, (int64_t)kt * 64, p.r, lora_vec, *reinterpret_cast<uint4(*)[4]>(&lv[0]));
+                            load_row32(row, (int64_t)kt * 64 + 32, p.r, lora_vec, *reinterpret_cast<uint4(*)[4]>(&lv[4]));
+                        }
                     } else {
-                        wrow = (int64_t)kt * 64 + nl;  // LoRA row j < r64
-                        if (kblock < p.KB) lsrc = p.lora_rows + wrow * p.K + (int64_t)kblock * 64 + half * 32;
-                    }
-                }
-                float sc = 0.0f;
-                if (blk >= 0) sc = dq_block_scale(p, blk, mu);  // issued before the waits
-                uint4 lv[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
-                               make_uint4(0, 0, 0, 0)};
-                if (lsrc) {
+                        const int64_t n = (int64_t)kt * 64 + nl;  // contraction row (weight or LoRA row)
+                        valid = kblock < p.KB && n < (lora ? (int64_t)p.r : p.N);
+                        if (lora && valid) {
+                            const uint4 *src = reinterpret_cast<const uint4 *>(p.lora_src + n * p.lora_ld + (int64_t)kblock * 64);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) lv[i] = __ldg(reinterpret_cast<const uint4 *>(lsrc) + i);
-                }
-                if (!warp_wait(&empty[s], ph ^ 1u, s_abort)) { ok = false; break; }
-                if (!warp_wait(&full_c[s], ph, s_abort)) { ok = false; break; }
-                uint4 outv[4];
-                if (!lora) {
-                    if (blk >= 0) {
-                        const uint4 cw = *reinterpret_cast<const uint4 *>(sC + s * kCodesTileBytes + code_off);
+                            for (int i = 0; i < 8; ++i) lv[i] = __ldg(src + i);
+                        }
+                    }
+                    if (!warp_wait(&empty[s], ph ^ 1u, s_abort)) { ok = false; break; }
+                    if (!warp_wait(&full_c[s], ph, s_abort)) { ok = false; break; }
+                    const uint32_t row_addr = a_base + (uint32_t)s * kATileBytes + row_off;
+                    if (!valid) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) st_shared_v4(row_addr + (((uint32_t)i ^ r7) << 4), make_uint4(0, 0, 0, 0));
+                    } else if (!lora) {
+                        const uint8_t *cst = sC + s * kCStageBytes;
+                        const uint4 c0 = *reinterpret_cast<const uint4 *>(cst + code_off);
+                        const uint4 c1 = *reinterpret_cast<const uint4 *>(cst + code_off + 16);
+                        const float sc = *reinterpret_cast<const float *>(cst + scale_off);
                         uint32_t lo[4], hi[4];
                         build_table(sc, p.tab, lo, hi);
-                        outv[0] = decode8(cw.x, lo, hi);
-                        outv[1] = decode8(cw.y, lo, hi);
-                        outv[2] = decode8(cw.z, lo, hi);
-                        outv[3] = decode8(cw.w, lo, hi);
+                        // 128-byte swizzle: chunk c of row r lives at chunk c ^ (r & 7)
+                        st_shared_v4(row_addr + ((0u ^ r7) << 4), decode8(c0.x, lo, hi));
+                        st_shared_v4(row_addr + ((1u ^ r7) << 4), decode8(c0.y, lo, hi));
+                        st_shared_v4(row_addr + ((2u ^ r7) << 4), decode8(c0.z, lo, hi));
+                        st_shared_v4(row_addr + ((3u ^ r7) << 4), decode8(c0.w, lo, hi));
+                        st_shared_v4(row_addr + ((4u ^ r7) << 4), decode8(c1.x, lo, hi));
+                        st_shared_v4(row_addr + ((5u ^ r7) << 4), decode8(c1.y, lo, hi));
+                        st_shared_v4(row_addr + ((6u ^ r7) << 4), decode8(c1.z, lo, hi));
+                        st_shared_v4(row_addr + ((7u ^ r7) << 4), decode8(c1.w, lo, hi));
                     } else {
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) outv[i] = make_uint4(0, 0, 0, 0);
+                        for (int i = 0; i < 8; ++i) st_shared_v4(row_addr + (((uint32_t)i ^ r7) << 4), lv[i]);
                     }
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) outv[i] = lv[i];
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&full_a[s]);
                 }
-                // 128-byte swizzle: 16-byte chunk c of row r lives at chunk c ^ (r & 7); rows are
-                // 128-byte aligned inside 1024-byte-aligned tiles, so (row_addr >> 7) & 7 == r & 7.
-                const uint32_t r7 = (row_addr >> 7) & 7u;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const uint32_t chunk = (uint32_t)(half * 4 + i);
-                    st_shared_v4(row_addr + ((chunk ^ r7) << 4), outv[i]);
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&full_a[s]);
                 if (++s == kStages) { s = 0; ph ^= 1u; }
             }
         }
@@ -392,15 +417,34 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
 }
 
 // ---------------------------------------------------------------------------------------
-// Skinny LoRA products.
+// Skinny LoRA products D[i, j] = sum_c P[i, c] Q[j, c] (N = r64 <= 256), split over the
+// contraction.  Each split writes its fp32 partial tile; the last CTA of a tile to finish
+// (a per-tile arrival counter) adds the partials in split order -- deterministic whatever
+// the finishing order -- and applies the finalize of the product.
 // ---------------------------------------------------------------------------------------
+__device__ __forceinline__ void proj_store(const ProjArgs &a, int64_t i, int j, float v) {
+    if (a.mode == 0) {
+        if (j < a.ld_h) {
+            __nv_bfloat16 h = __float2bfloat16_rn(__fmul_rn(v, a.scale));
+            const uint16_t hb = *reinterpret_cast<uint16_t *>(&h);
+            a.out_h[i * a.ld_h + j] = hb;
+            if (a.out_h2 && j < a.r) a.out_h2[i * a.r + j] = hb;
+        }
+    } else if (a.mode == 1) {
+        if (j < a.r) a.out_f[(int64_t)j * a.Mp + i] = v;
+    } else {
+        if (j < a.r) a.out_f[i * a.r + j] = v;
+    }
+}
+
 template <bool kPMN, bool kQMN>
 __global__ void __launch_bounds__(128, 1)
-    lora_proj_kernel(const __grid_constant__ CUtensorMap map_p, const __grid_constant__ CUtensorMap map_q, int Mp,
-                     int r64, int tiles, int splits, int ktiles, float *__restrict__ partial) {
+    lora_proj_kernel(const __grid_constant__ CUtensorMap map_p, const __grid_constant__ CUtensorMap map_q,
+                     const ProjArgs a) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+    const int r64 = a.r64;
     const uint32_t q_bytes = (uint32_t)r64 * 128u;
     uint8_t *sP = smem;
     uint8_t *sQ = sP + kStages * kATileBytes;
@@ -409,10 +453,12 @@ __global__ void __launch_bounds__(128, 1)
     uint64_t *done = empty + kStages;
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(done + 1);
     volatile uint32_t *s_abort = s_tmem + 1;
+    volatile uint32_t *s_last = s_tmem + 2;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int tile = blockIdx.x % tiles, split = blockIdx.x / tiles;
-    const int kt0 = (int)((int64_t)split * ktiles / splits), kt1 = (int)((int64_t)(split + 1) * ktiles / splits);
+    const int tile = blockIdx.x % a.tiles, split = blockIdx.x / a.tiles;
+    const int kt0 = (int)((int64_t)split * a.ktiles / a.splits);
+    const int kt1 = (int)((int64_t)(split + 1) * a.ktiles / a.splits);
     const uint32_t ncols = r64 <= 64 ? 64u : (r64 <= 128 ? 128u : 256u);
 
     if (threadIdx.x == 0) {
@@ -422,6 +468,7 @@ __global__ void __launch_bounds__(128, 1)
         }
         mbar_init(done, 1);
         *s_abort = 0u;
+        *s_last = 0u;
         fence_mbar_init();
     }
     if (warp == 0) {
@@ -459,9 +506,8 @@ __global__ void __launch_bounds__(128, 1)
         const uint32_t p_base = smem_u32(sP), q_base = smem_u32(sQ);
         int s = 0;
         uint32_t ph = 0;
-        bool ok = true;
         for (int kt = kt0; kt < kt1; ++kt) {
-            if (!mbar_wait(&full[s], ph, s_abort)) { ok = false; break; }
+            if (!mbar_wait(&full[s], ph, s_abort)) break;
             tc_fence_after();
             const uint32_t pa = p_base + (uint32_t)s * kATileBytes, qa = q_base + (uint32_t)s * q_bytes;
 #pragma unroll
@@ -475,34 +521,103 @@ __global__ void __launch_bounds__(128, 1)
             umma_commit(&empty[s]);
             if (++s == kStages) { s = 0; ph ^= 1u; }
         }
-        (void)ok;
-        umma_commit(done);  // also drains on the error path
+        umma_commit(done);  // also drains the MMAs on the error path
     }
     __syncwarp();
     // epilogue: all four warps (warp w reads TMEM lanes 32w..32w+31)
-    if (warp_wait(done, 0, s_abort)) {
+    const int64_t i = (int64_t)tile * 128 + warp * 32 + lane;
+    const bool ok = warp_wait(done, 0, s_abort);
+    if (ok) {
         tc_fence_after();
-        const int64_t i = (int64_t)tile * 128 + warp * 32 + lane;
         const uint32_t taddr = tmem_base + ((uint32_t)(warp * 32) << 16);
         for (int c = 0; c < r64 / 32; ++c) {
             uint32_t r[32];
             tmem_ld_32x32b_x32(taddr + (uint32_t)c * 32u, r);
             tmem_ld_wait();
-            if (i < Mp) {
-                float4 *dst = reinterpret_cast<float4 *>(partial + ((int64_t)split * Mp + i) * r64 + c * 32);
+            if (i < a.Mp) {
+                if (a.splits == 1) {
 #pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    dst[q] = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
-                                         __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+                    for (int q = 0; q < 32; ++q) proj_store(a, i, c * 32 + q, __uint_as_float(r[q]));
+                } else {
+                    float4 *dst = reinterpret_cast<float4 *>(a.partial + ((int64_t)split * a.Mp + i) * r64 + c * 32);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        dst[q] = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                                             __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+                }
             }
         }
     }
     tc_fence_before();
+    if (a.splits > 1) {
+        __threadfence();
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            const uint32_t prev = atomicAdd(a.counters + tile, 1u);
+            *s_last = (prev == (uint32_t)(a.splits - 1)) ? 1u : 0u;
+        }
+        __syncthreads();
+        if (*s_last) {
+            __threadfence();
+            if (i < a.Mp) {
+                for (int j4 = 0; j4 < r64; j4 += 4) {
+                    float4 acc = __ldcg(reinterpret_cast<const float4 *>(a.partial + i * r64 + j4));
+                    for (int sp = 1; sp < a.splits; ++sp) {
+                        const float4 v =
+                            __ldcg(reinterpret_cast<const float4 *>(a.partial + ((int64_t)sp * a.Mp + i) * r64 + j4));
+                        acc.x = __fadd_rn(acc.x, v.x);
+                        acc.y = __fadd_rn(acc.y, v.y);
+                        acc.z = __fadd_rn(acc.z, v.z);
+                        acc.w = __fadd_rn(acc.w, v.w);
+                    }
+                    proj_store(a, i, j4, acc.x);
+                    proj_store(a, i, j4 + 1, acc.y);
+                    proj_store(a, i, j4 + 2, acc.z);
+                    proj_store(a, i, j4 + 3, acc.w);
+                }
+            }
+            if (threadIdx.x == 0) a.counters[tile] = 0u;  // ready for the next call
+        }
+    }
     __syncthreads();
     if (warp == 0) {
         tc_fence_after();
         tmem_dealloc(tmem_base, ncols);
     }
+}
+
+// ---------------------------------------------------------------------------------------
+// Rebuilt block scales for the fused kernel: out[kb, n] = fmaf(q_b, fl32(c2_g / 127), mu) for
+// block b = n * KB + kb (transposed, so that a weight tile's scales are one contiguous TMA
+// box).  Block (0, 0) also zeroes the split-reduction counters of the call.
+// ---------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) dq_scales_t_kernel(const int8_t *__restrict__ q, const float *__restrict__ c2,
+                                                          const float *__restrict__ mu_p, int64_t N, int KB,
+                                                          float *__restrict__ out, uint32_t *__restrict__ zero,
+                                                          int nzero) {
+    __shared__ float tile[32][33];
+    const float mu = *mu_p;
+    const int64_t n0 = (int64_t)blockIdx.x * 32;
+    const int kb0 = blockIdx.y * 32;
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    for (int i = ty; i < 32; i += 8) {
+        const int64_t n = n0 + i;
+        const int kb = kb0 + tx;
+        float v = 0.0f;
+        if (n < N && kb < KB) {
+            const int64_t b = n * KB + kb;
+            v = __fmaf_rn((float)q[b], __fdiv_rn(c2[b >> 8], 127.0f), mu);
+        }
+        tile[i][tx] = v;
+    }
+    __syncthreads();
+    for (int i = ty; i < 32; i += 8) {
+        const int kb = kb0 + i;
+        const int64_t n = n0 + tx;
+        if (n < N && kb < KB) out[(int64_t)kb * N + n] = tile[tx][i];
+    }
+    if (blockIdx.x == 0 && blockIdx.y == 0)
+        for (int k = threadIdx.x; k < nzero; k += blockDim.x) zero[k] = 0u;
 }
 
 // ---------------------------------------------------------------------------------------
@@ -515,28 +630,6 @@ __global__ void splitk_reduce_kernel(const float *__restrict__ partial, int spli
         for (int s = 1; s < splits; ++s) acc = __fadd_rn(acc, partial[(int64_t)s * total + i]);
         __nv_bfloat16 h = __float2bfloat16_rn(acc);
         out[i] = *reinterpret_cast<uint16_t *>(&h);
-    }
-}
-
-__global__ void proj_finalize_kernel(int mode, const float *__restrict__ partial, int splits, int64_t Mp, int r64,
-                                     int r, float scale, uint16_t *__restrict__ out_pad, uint16_t *__restrict__ out_r,
-                                     float *__restrict__ out_f) {
-    const int64_t total = Mp * r64;
-    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total; e += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t i = e / r64;
-        const int j = (int)(e % r64);
-        float acc = partial[e];
-        for (int s = 1; s < splits; ++s) acc = __fadd_rn(acc, partial[(int64_t)s * total + e]);
-        if (mode == 0) {
-            __nv_bfloat16 h = __float2bfloat16_rn(__fmul_rn(acc, scale));
-            const uint16_t hb = *reinterpret_cast<uint16_t *>(&h);
-            out_pad[e] = hb;
-            if (out_r && j < r) out_r[i * r + j] = hb;
-        } else if (mode == 1) {
-            if (j < r) out_f[(int64_t)j * Mp + i] = acc;
-        } else {
-            if (j < r) out_f[i * r + j] = acc;
-        }
     }
 }
 
@@ -555,7 +648,7 @@ __global__ void pad_2d_kernel(const uint16_t *__restrict__ src, int64_t rows_src
 // The fused kernel allocates all 512 TMEM columns, so it must be alone on its SM: asking for
 // more than half of the SM's shared memory guarantees one resident CTA.
 static size_t fused_smem_bytes(int BN) {
-    const size_t need = 1024 + (size_t)kStages * (kATileBytes + (size_t)BN * 128 + kCodesTileBytes) + 256;
+    const size_t need = 1024 + (size_t)kStages * (kATileBytes + (size_t)BN * 128 + kCStageBytes) + 256;
     return std::max<size_t>(need, 120 * 1024);
 }
 static size_t proj_smem_bytes(int r64) { return 1024 + (size_t)kStages * (kATileBytes + (size_t)r64 * 128) + 128; }
@@ -594,25 +687,29 @@ ProjPlan plan_proj(int64_t Mp, int64_t Kc, int r64, int num_sms) {
     pl.tiles = (int)((Mp + 127) / 128);
     pl.ktiles = (int)((Kc + 63) / 64);
     const int per_sm = r64 <= 64 ? 2 : 1;
-    int64_t s = ((int64_t)per_sm * num_sms + pl.tiles - 1) / pl.tiles;
+    // as many splits as fit in one wave of resident CTAs
+    int64_t s = std::max<int64_t>(1, ((int64_t)per_sm * num_sms) / pl.tiles);
     s = std::max<int64_t>(1, std::min<int64_t>(s, std::min<int64_t>(pl.ktiles, 32)));
     pl.splits = (int)s;
-    pl.partial_bytes = (size_t)pl.splits * (size_t)Mp * (size_t)r64 * 4;
+    pl.partial_bytes = pl.splits > 1 ? (size_t)pl.splits * (size_t)Mp * (size_t)r64 * 4 : 0;
     return pl;
 }
 
-cudaError_t launch_fused(bool dx, const CUtensorMap &map_codes, const CUtensorMap &map_act, const CUtensorMap &map_lora,
-                         const FusedArgs &args, const FusedPlan &plan, cudaStream_t st) {
+cudaError_t launch_fused(bool dx, const CUtensorMap &map_codes, const CUtensorMap &map_scales,
+                         const CUtensorMap &map_act, const CUtensorMap &map_lora, const FusedArgs &args,
+                         const FusedPlan &plan, cudaStream_t st) {
     const size_t smem = fused_smem_bytes(plan.BN);
     cudaError_t e;
     if (dx) {
         e = cudaFuncSetAttribute(nf4_lora_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        nf4_lora_gemm_kernel<true><<<plan.grid, kFusedThreads, smem, st>>>(map_codes, map_act, map_lora, args);
+        nf4_lora_gemm_kernel<true>
+            <<<plan.grid, kFusedThreads, smem, st>>>(map_codes, map_scales, map_act, map_lora, args);
     } else {
         e = cudaFuncSetAttribute(nf4_lora_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        nf4_lora_gemm_kernel<false><<<plan.grid, kFusedThreads, smem, st>>>(map_codes, map_act, map_lora, args);
+        nf4_lora_gemm_kernel<false>
+            <<<plan.grid, kFusedThreads, smem, st>>>(map_codes, map_scales, map_act, map_lora, args);
     }
     count_launch();
     return cudaGetLastError();
@@ -631,18 +728,16 @@ cudaError_t launch_splitk_reduce(const float *partial, int splits, int64_t rows,
     return cudaGetLastError();
 }
 
-cudaError_t launch_proj(bool p_mn, bool q_mn, const CUtensorMap &map_p, const CUtensorMap &map_q, int64_t Mp,
-                        int64_t Kc, int r64, const ProjPlan &plan, float *partial, cudaStream_t st) {
-    (void)Kc;
-    const size_t smem = proj_smem_bytes(r64);
-    const int grid = plan.tiles * plan.splits;
+cudaError_t launch_proj(bool p_mn, bool q_mn, const CUtensorMap &map_p, const CUtensorMap &map_q, const ProjArgs &args,
+                        cudaStream_t st) {
+    const size_t smem = proj_smem_bytes(args.r64);
+    const int grid = args.tiles * args.splits;
 #define QLORA_PROJ_CASE(PM, QM)                                                                                     \
     if (p_mn == PM && q_mn == QM) {                                                                                 \
         cudaError_t e =                                                                                             \
             cudaFuncSetAttribute(lora_proj_kernel<PM, QM>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
         if (e != cudaSuccess) return e;                                                                             \
-        lora_proj_kernel<PM, QM><<<grid, 128, smem, st>>>(map_p, map_q, (int)Mp, r64, plan.tiles, plan.splits,      \
-                                                          plan.ktiles, partial);                                    \
+        lora_proj_kernel<PM, QM><<<grid, 128, smem, st>>>(map_p, map_q, args);                                       \
     }
     QLORA_PROJ_CASE(false, false)
     QLORA_PROJ_CASE(false, true)
@@ -653,10 +748,10 @@ cudaError_t launch_proj(bool p_mn, bool q_mn, const CUtensorMap &map_p, const CU
     return cudaGetLastError();
 }
 
-cudaError_t launch_proj_finalize(int mode, const float *partial, int splits, int64_t Mp, int r64, int r, float scale,
-                                 uint16_t *out_pad, uint16_t *out_r, float *out_f, int num_sms, cudaStream_t st) {
-    proj_finalize_kernel<<<ew_grid(Mp * r64, num_sms), 256, 0, st>>>(mode, partial, splits, Mp, r64, r, scale, out_pad,
-                                                                     out_r, out_f);
+cudaError_t launch_dq_scales_t(const int8_t *q, const float *c2, const float *mu, int64_t N, int KB, float *out,
+                               uint32_t *zero, int nzero, cudaStream_t st) {
+    dim3 grid((unsigned)((N + 31) / 32), (unsigned)((KB + 31) / 32));
+    dq_scales_t_kernel<<<grid, 256, 0, st>>>(q, c2, mu, N, KB, out, zero, nzero);
     count_launch();
     return cudaGetLastError();
 }

@@ -63,35 +63,37 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
                  : "memory");
 }
+// try_wait with a suspend-time hint: a waiting thread sleeps in hardware until the phase
+// completes (or the hint elapses) instead of spinning and taking issue slots from the warps
+// that do the work.
+static constexpr uint32_t kSuspendHintNs = 200000;
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}\n"
         : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendHintNs)
         : "memory");
     return ok != 0;
 }
 
-// Wait for the phase with the given parity to complete, for at most `timeout_ns`.  Every wait
-// in the pipelined kernels goes through here: on a timeout (or when another thread of the
-// CTA already gave up, flagged in *abort) it latches the device error word and returns false,
-// so that the kernel unwinds instead of hanging.
+// Wait for the phase with the given parity to complete, for at most kWaitTimeoutNs.  Every wait
+// in the pipelined kernels goes through here: on a timeout (or when another thread of the CTA
+// already gave up, flagged in *abort) it latches the device error word and returns false, so
+// that the kernel unwinds instead of hanging.
 static constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // 2 s; a stage normally takes us
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile uint32_t *abort) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
-    for (uint32_t i = 1;; ++i) {
+    while (true) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 31u) == 0) {
-            if (*abort) return false;
-            if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
-                *abort = 1u;
-                atomicOr(&g_error_word, kErrTimeout);
-                return false;
-            }
+        if (*abort) return false;
+        if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+            *abort = 1u;
+            atomicOr(&g_error_word, kErrTimeout);
+            return false;
         }
     }
 }

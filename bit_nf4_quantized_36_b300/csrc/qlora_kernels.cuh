@@ -21,22 +21,20 @@ cudaError_t launch_dequantize(const uint8_t *codes, const int8_t *qcode, const f
 
 // ---- fused NF4-dequant GEMM with the LoRA term as extra K-steps (gemm.cu) ---------------
 // Computes, per output row m (token) and feature f:
-//   forward  (dx = false): Y[m, f]  = sum_k X[m, k] W^[f, k] + sum_j U[m, j] Bp[f, j]
-//   backward (dx = true) : dX[m, f] = sum_n G[m, n] W^[n, f] + sum_j V[m, j] Ap[j, f]
-// with W^ dequantized from the NF4 tensor inside the main loop.
+//   forward  (dx = false): Y[m, f]  = sum_k X[m, k] W^[f, k] + sum_j U[m, j] B[f, j]
+//   backward (dx = true) : dX[m, f] = sum_n G[m, n] W^[n, f] + sum_j V[m, j] A[j, f]
+// with W^ dequantized from the NF4 codes and the rebuilt block scales inside the main loop.
 struct FusedArgs {
-    const int8_t *scale_codes;
-    const float *scale_scales;
-    const float *scale_offset;
     int64_t N, K;          // weight matrix rows, cols
     int32_t KB;            // K / 64
     int32_t M;             // tokens
-    const uint16_t *lora_rows;  // forward: Bp [N, r64]; backward: Ap [r64, K] (zero padded)
-    int32_t r64;           // padded rank, multiple of 64
+    const uint16_t *lora_src;  // forward: B [N, r]; backward: A [r, K]
+    int64_t lora_ld;       // row stride of lora_src in elements (r or K)
+    int32_t r;             // LoRA rank
     int32_t BN;            // token tile = MMA N (multiple of 32, <= 256)
     int32_t w_tiles, m_tiles, splits;
     int32_t kt_main;       // k-tiles of 64 over the main contraction (K or ceil(N / 64))
-    int32_t kt_lora;       // r64 / 64
+    int32_t kt_lora;       // ceil(r / 64)
     uint16_t *out;         // [M, wdim] bf16 (splits == 1)
     float *partial;        // [splits, M, wdim] fp32 (splits > 1)
     int64_t wdim;          // output features: N (forward) or K (backward)
@@ -49,34 +47,47 @@ struct FusedPlan {
 };
 FusedPlan plan_fused(int64_t M, int64_t wdim, int64_t kt_main, int r64, int num_sms);
 
-// map_codes: codes as a 2-D byte tensor {K/2, N}; box {32, 128} (forward) or {64, 64} (backward)
-// map_act:   X [M, K] (forward) or G [M, N] (backward), bf16, box {64, BN}, 128-byte swizzle
-// map_lora:  U [M, r64] (forward) or V [M, r64] (backward), box {64, BN}, 128-byte swizzle
-cudaError_t launch_fused(bool dx, const CUtensorMap &map_codes, const CUtensorMap &map_act,
-                         const CUtensorMap &map_lora, const FusedArgs &args, const FusedPlan &plan, cudaStream_t st);
+// map_codes : codes as a 2-D byte tensor {K/2, N}; box {32, 128} (forward) or {64, 64} (backward)
+// map_scales: rebuilt block scales, fp32 {N, KB} (transposed, [KB][N]); box {128, 1} or {64, 2}
+// map_act   : X [M, K] (forward) or G [M, N] (backward), bf16, box {64, BN}, 128-byte swizzle
+// map_lora  : U or V [M, ld] bf16, box {64, BN}, 128-byte swizzle (columns >= r read as 0)
+cudaError_t launch_fused(bool dx, const CUtensorMap &map_codes, const CUtensorMap &map_scales,
+                         const CUtensorMap &map_act, const CUtensorMap &map_lora, const FusedArgs &args,
+                         const FusedPlan &plan, cudaStream_t st);
 cudaError_t launch_splitk_reduce(const float *partial, int splits, int64_t rows, int64_t cols, uint16_t *out,
                                  int num_sms, cudaStream_t st);
+// out[kb, n] = fmaf(q[n*KB + kb], fl32(c2 / 127), mu); also zeroes zero[0..nzero)
+cudaError_t launch_dq_scales_t(const int8_t *q, const float *c2, const float *mu, int64_t N, int KB, float *out,
+                               uint32_t *zero, int nzero, cudaStream_t st);
 
 // ---- skinny LoRA products D[i, j] = sum_c P[i, c] Q[j, c], j < r64 (gemm.cu) -------------
 // P: K-major ([Mp, Kc] row-major, map dims {Kc, Mp}, box {64, 128}) or
 //    MN-major ([Kc, Mp] row-major, map dims {Mp, Kc}, box {64, 64}).
-// Q: K-major ([r64, Kc], map dims {Kc, r64}, box {64, r64}) or
-//    MN-major ([Kc, r64], map dims {r64, Kc}, box {64, 64}).
-// Writes fp32 partial sums [splits, Mp, r64].
+// Q: K-major ([r, Kc], map dims {Kc, r}, box {64, r64}) or
+//    MN-major ([Kc, r], map dims {r, Kc}, box {64, 64}); rows/columns >= r read as zero.
+// Split over the contraction; the last CTA of each 128-row tile sums the fp32 partials in
+// split order and stores:
+//   mode 0: out_h[i, j] = bf16(scale * D) for j < ld_h; out_h2[i, j] (nullable) for j < r
+//   mode 1: out_f[j, i] = D for j < r  (transposed fp32)
+//   mode 2: out_f[i, j] = D for j < r  (fp32)
+struct ProjArgs {
+    int Mp, r64, r, tiles, splits, ktiles;
+    int mode;
+    float scale;
+    float *partial;        // [splits, Mp, r64] when splits > 1
+    uint32_t *counters;    // [tiles], zero before the launch (left zero after it)
+    uint16_t *out_h;
+    int ld_h;
+    uint16_t *out_h2;
+    float *out_f;
+};
 struct ProjPlan {
     int tiles, splits, ktiles;
     size_t partial_bytes;
 };
 ProjPlan plan_proj(int64_t Mp, int64_t Kc, int r64, int num_sms);
-cudaError_t launch_proj(bool p_mn, bool q_mn, const CUtensorMap &map_p, const CUtensorMap &map_q, int64_t Mp,
-                        int64_t Kc, int r64, const ProjPlan &plan, float *partial, cudaStream_t st);
-
-// Finalize of the skinny products (sum of the splits in index order, then):
-//   mode 0: out_pad[i, j] = bf16(scale * sum) for j < r64; out_r[i, j] (nullable) for j < r
-//   mode 1: out_f[j, i] = sum for j < r  (transposed fp32, dA)
-//   mode 2: out_f[i, j] = sum for j < r  (fp32, dB)
-cudaError_t launch_proj_finalize(int mode, const float *partial, int splits, int64_t Mp, int r64, int r, float scale,
-                                 uint16_t *out_pad, uint16_t *out_r, float *out_f, int num_sms, cudaStream_t st);
+cudaError_t launch_proj(bool p_mn, bool q_mn, const CUtensorMap &map_p, const CUtensorMap &map_q, const ProjArgs &args,
+                        cudaStream_t st);
 
 // dst[rows_dst, cols_dst] = src[rows_src, cols_src] where both indices are in range, else 0
 cudaError_t launch_pad_2d(const uint16_t *src, int64_t rows_src, int64_t cols_src, uint16_t *dst, int64_t rows_dst,

@@ -56,7 +56,7 @@ __global__ void __launch_bounds__(256) nf4_quantize_blocks_kernel(const float4 *
 }
 
 // K2a: S_g = fp64 sum of the group's scales in index order; slots ng..p2-1 get +0.0.
-__global__ void __launch_bounds__(256) dq_group_sums_kernel(const float *__restrict__ absmax, int64_t nb, int64_t ng,
+__global__ void __launch_bounds__(32) dq_group_sums_kernel(const float *__restrict__ absmax, int64_t nb, int64_t ng,
                                                             int64_t p2, double *__restrict__ tree) {
     for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < p2; g += (int64_t)gridDim.x * blockDim.x) {
         double acc = 0.0;
@@ -166,7 +166,8 @@ cudaError_t launch_quantize(const float *W, int64_t n, uint8_t *codes, int8_t *q
     nf4_quantize_blocks_kernel<<<grid_for(nb, 16, num_sms, 8), 256, 0, st>>>(
         reinterpret_cast<const float4 *>(W), nb, reinterpret_cast<uint16_t *>(codes), ws_absmax, tab);
     count_launch();
-    dq_group_sums_kernel<<<grid_for(p2, 256, num_sms, 4), 256, 0, st>>>(ws_absmax, nb, ng, p2, ws_tree);
+    // one thread per group (a sequential fp64 chain); small CTAs spread the chains over many SMs
+    dq_group_sums_kernel<<<grid_for(p2, 32, num_sms, 64), 32, 0, st>>>(ws_absmax, nb, ng, p2, ws_tree);
     count_launch();
     dq_mean_kernel<<<1, 1024, 0, st>>>(ws_tree, ws_tree + p2, p2, nb, mu);
     count_launch();

@@ -39,12 +39,20 @@ def run_layer(inp, fwd_only=False, use_saved_u=True):
     return out
 
 
+_WHAT_CACHE = {}
+
+
 def oracle_what(orc, inp, qw):
-    ref = orc.nf4_quantize(inp.W)
-    got = nf4_to_host(qw)
-    np.testing.assert_array_equal(got["packed"], ref["packed"])
-    N, K = inp.W.shape
-    return orc.nf4_dequantize(ref["packed"], ref["qcode"], ref["c2"], ref["mu"], N, K)
+    key = (inp.meta.get("workload"), inp.meta.get("sub"), inp.W.shape, inp.W[:2, :8].tobytes(), inp.W[-1, -8:].tobytes())
+    if key not in _WHAT_CACHE:
+        ref = orc.nf4_quantize(inp.W)
+        N, K = inp.W.shape
+        if len(_WHAT_CACHE) >= 2:
+            _WHAT_CACHE.pop(next(iter(_WHAT_CACHE)))
+        _WHAT_CACHE[key] = (ref["packed"], orc.nf4_dequantize(ref["packed"], ref["qcode"], ref["c2"], ref["mu"], N, K))
+    packed, What = _WHAT_CACHE[key]
+    np.testing.assert_array_equal(nf4_to_host(qw)["packed"], packed)
+    return What
 
 
 def check_full(orc, inp, out, rows=None, jsel=None):
@@ -145,8 +153,8 @@ def test_llama8b_mlp(orc, mat):
     check_full(orc, inp, out, rows=rows, jsel=[0, 37, 63])
 
 
-@pytest.mark.parametrize("M", [1, 8, 32])
 @pytest.mark.parametrize("mat", [0, 1])
+@pytest.mark.parametrize("M", [1, 8, 32])
 def test_llama70b_decode(orc, M, mat):
     c = synth.LLAMA70B_DECODE
     name, N, K = c["mats"][mat]
