@@ -25,7 +25,7 @@
 
 namespace qlora {
 
-static constexpr int kStages = 4;
+static constexpr int kProjStages = 4;                 // skinny products
 static constexpr uint32_t kATileBytes = 128u * 128u;  // 128 rows x 64 bf16
 static constexpr uint32_t kCodesTileBytes = 4096u;    // 128 rows x 32 B or 64 rows x 64 B
 static constexpr uint32_t kScaleTileBytes = 512u;     // 128 (or 2 x 64) fp32 block scales
@@ -130,7 +130,7 @@ __device__ __forceinline__ UnitInfo unit_info(const FusedArgs &p, int u) {
     return ui;
 }
 
-template <bool kDX>
+template <bool kDX, int kStages>
 __global__ void __launch_bounds__(kFusedThreads, 1)
     nf4_lora_gemm_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant__ CUtensorMap map_scales,
                          const __grid_constant__ CUtensorMap map_act, const __grid_constant__ CUtensorMap map_lora,
@@ -418,9 +418,10 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
 
 // ---------------------------------------------------------------------------------------
 // Skinny LoRA products D[i, j] = sum_c P[i, c] Q[j, c] (N = r64 <= 256), split over the
-// contraction.  Each split writes its fp32 partial tile; the last CTA of a tile to finish
-// (a per-tile arrival counter) adds the partials in split order -- deterministic whatever
-// the finishing order -- and applies the finalize of the product.
+// contraction.  The `splits` CTAs of one 128-row tile form a thread-block cluster: each parks
+// its fp32 partial tile in its own shared memory, and after a cluster barrier every CTA sums a
+// slice of the rows over all partials in split order (distributed shared memory reads) --
+// deterministic, with no global scratch.
 // ---------------------------------------------------------------------------------------
 __device__ __forceinline__ void proj_store(const ProjArgs &a, int64_t i, int j, float v) {
     if (a.mode == 0) {
@@ -437,10 +438,30 @@ __device__ __forceinline__ void proj_store(const ProjArgs &a, int64_t i, int j, 
     }
 }
 
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ float4 ld_dsmem_f4(uint32_t local_addr, uint32_t rank) {
+    uint32_t ra;
+    float4 v;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(local_addr), "r"(rank));
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(ra)
+                 : "memory");
+    return v;
+}
+
 template <bool kPMN, bool kQMN>
 __global__ void __launch_bounds__(128, 1)
     lora_proj_kernel(const __grid_constant__ CUtensorMap map_p, const __grid_constant__ CUtensorMap map_q,
                      const ProjArgs a) {
+    constexpr int kStages = kProjStages;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -453,10 +474,10 @@ __global__ void __launch_bounds__(128, 1)
     uint64_t *done = empty + kStages;
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(done + 1);
     volatile uint32_t *s_abort = s_tmem + 1;
-    volatile uint32_t *s_last = s_tmem + 2;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int tile = blockIdx.x % a.tiles, split = blockIdx.x / a.tiles;
+    const int split = (int)cluster_ctarank();  // the cluster spans the splits of one tile
+    const int tile = blockIdx.x / a.splits;
     const int kt0 = (int)((int64_t)split * a.ktiles / a.splits);
     const int kt1 = (int)((int64_t)(split + 1) * a.ktiles / a.splits);
     const uint32_t ncols = r64 <= 64 ? 64u : (r64 <= 128 ? 128u : 256u);
@@ -468,7 +489,6 @@ __global__ void __launch_bounds__(128, 1)
         }
         mbar_init(done, 1);
         *s_abort = 0u;
-        *s_last = 0u;
         fence_mbar_init();
     }
     if (warp == 0) {
@@ -524,62 +544,55 @@ __global__ void __launch_bounds__(128, 1)
         umma_commit(done);  // also drains the MMAs on the error path
     }
     __syncwarp();
-    // epilogue: all four warps (warp w reads TMEM lanes 32w..32w+31)
-    const int64_t i = (int64_t)tile * 128 + warp * 32 + lane;
-    const bool ok = warp_wait(done, 0, s_abort);
-    if (ok) {
+    // TMEM -> this CTA's fp32 partial tile in shared memory (the pipeline buffers are free once
+    // `done` has completed).  Row stride r64 + 4 floats keeps the float4 stores conflict-free.
+    const int pstride = r64 + 4;
+    float *part = reinterpret_cast<float *>(smem);
+    const int row = warp * 32 + lane;  // warp w reads TMEM lanes 32w..32w+31
+    if (warp_wait(done, 0, s_abort)) {
         tc_fence_after();
         const uint32_t taddr = tmem_base + ((uint32_t)(warp * 32) << 16);
         for (int c = 0; c < r64 / 32; ++c) {
             uint32_t r[32];
             tmem_ld_32x32b_x32(taddr + (uint32_t)c * 32u, r);
             tmem_ld_wait();
-            if (i < a.Mp) {
-                if (a.splits == 1) {
+            float4 *dst = reinterpret_cast<float4 *>(part + row * pstride + c * 32);
 #pragma unroll
-                    for (int q = 0; q < 32; ++q) proj_store(a, i, c * 32 + q, __uint_as_float(r[q]));
-                } else {
-                    float4 *dst = reinterpret_cast<float4 *>(a.partial + ((int64_t)split * a.Mp + i) * r64 + c * 32);
-#pragma unroll
-                    for (int q = 0; q < 8; ++q)
-                        dst[q] = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
-                                             __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
-                }
-            }
+            for (int q = 0; q < 8; ++q)
+                dst[q] = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                                     __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
         }
     }
     tc_fence_before();
-    if (a.splits > 1) {
-        __threadfence();
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            const uint32_t prev = atomicAdd(a.counters + tile, 1u);
-            *s_last = (prev == (uint32_t)(a.splits - 1)) ? 1u : 0u;
-        }
-        __syncthreads();
-        if (*s_last) {
-            __threadfence();
-            if (i < a.Mp) {
-                for (int j4 = 0; j4 < r64; j4 += 4) {
-                    float4 acc = __ldcg(reinterpret_cast<const float4 *>(a.partial + i * r64 + j4));
-                    for (int sp = 1; sp < a.splits; ++sp) {
-                        const float4 v =
-                            __ldcg(reinterpret_cast<const float4 *>(a.partial + ((int64_t)sp * a.Mp + i) * r64 + j4));
-                        acc.x = __fadd_rn(acc.x, v.x);
-                        acc.y = __fadd_rn(acc.y, v.y);
-                        acc.z = __fadd_rn(acc.z, v.z);
-                        acc.w = __fadd_rn(acc.w, v.w);
-                    }
-                    proj_store(a, i, j4, acc.x);
-                    proj_store(a, i, j4 + 1, acc.y);
-                    proj_store(a, i, j4 + 2, acc.z);
-                    proj_store(a, i, j4 + 3, acc.w);
-                }
+    cluster_sync_all();
+    // Sum over the splits in split order; this CTA owns rows [r0, r1) of the tile.
+    {
+        const int rows_per = (128 + a.splits - 1) / a.splits;
+        const int r0 = split * rows_per, r1 = min(128, r0 + rows_per);
+        const int nrow = max(0, r1 - r0), nj4 = r64 / 4;
+        const uint32_t part_addr = smem_u32(part);
+        for (int idx = threadIdx.x; idx < nrow * nj4; idx += blockDim.x) {
+            // transposed output (mode 1): consecutive threads take consecutive rows
+            const int rr = (a.mode == 1) ? r0 + idx % nrow : r0 + idx / nj4;
+            const int j4 = ((a.mode == 1) ? idx / nrow : idx % nj4) * 4;
+            const int64_t i = (int64_t)tile * 128 + rr;
+            if (i >= a.Mp) continue;
+            const uint32_t off = part_addr + (uint32_t)(rr * pstride + j4) * 4u;
+            float4 acc = ld_dsmem_f4(off, 0);
+            for (int sp = 1; sp < a.splits; ++sp) {
+                const float4 v = ld_dsmem_f4(off, (uint32_t)sp);
+                acc.x = __fadd_rn(acc.x, v.x);
+                acc.y = __fadd_rn(acc.y, v.y);
+                acc.z = __fadd_rn(acc.z, v.z);
+                acc.w = __fadd_rn(acc.w, v.w);
             }
-            if (threadIdx.x == 0) a.counters[tile] = 0u;  // ready for the next call
+            proj_store(a, i, j4, acc.x);
+            proj_store(a, i, j4 + 1, acc.y);
+            proj_store(a, i, j4 + 2, acc.z);
+            proj_store(a, i, j4 + 3, acc.w);
         }
     }
-    __syncthreads();
+    cluster_sync_all();  // peers read this CTA's shared memory until here
     if (warp == 0) {
         tc_fence_after();
         tmem_dealloc(tmem_base, ncols);
@@ -645,19 +658,28 @@ __global__ void pad_2d_kernel(const uint16_t *__restrict__ src, int64_t rows_src
 // ---------------------------------------------------------------------------------------
 // Plans and launchers
 // ---------------------------------------------------------------------------------------
+// Pipeline depth of the fused kernel: as many stages (even, <= 8) as fit in ~220 KB, so that a
+// small token tile keeps enough codes in flight to cover HBM latency.
+static int fused_stages(int BN) {
+    const size_t per = kATileBytes + (size_t)BN * 128 + kCStageBytes;
+    int st = (int)((220u * 1024u) / per);
+    st = std::min(8, st) & ~1;
+    return std::max(4, st);
+}
 // The fused kernel allocates all 512 TMEM columns, so it must be alone on its SM: asking for
 // more than half of the SM's shared memory guarantees one resident CTA.
-static size_t fused_smem_bytes(int BN) {
-    const size_t need = 1024 + (size_t)kStages * (kATileBytes + (size_t)BN * 128 + kCStageBytes) + 256;
+static size_t fused_smem_bytes(int BN, int stages) {
+    const size_t need = 1024 + (size_t)stages * (kATileBytes + (size_t)BN * 128 + kCStageBytes) + 512;
     return std::max<size_t>(need, 120 * 1024);
 }
-static size_t proj_smem_bytes(int r64) { return 1024 + (size_t)kStages * (kATileBytes + (size_t)r64 * 128) + 128; }
+static size_t proj_smem_bytes(int r64) { return 1024 + (size_t)kProjStages * (kATileBytes + (size_t)r64 * 128) + 128; }
 
 FusedPlan plan_fused(int64_t M, int64_t wdim, int64_t kt_main, int r64, int num_sms) {
     FusedPlan pl{};
     int64_t bn = M >= 256 ? 256 : ((M + 31) / 32) * 32;
     if (bn < 32) bn = 32;
     pl.BN = (int)bn;
+    pl.stages = fused_stages(pl.BN);
     pl.m_tiles = (int)((M + bn - 1) / bn);
     pl.w_tiles = (int)((wdim + 127) / 128);
     pl.kt_main = (int)kt_main;
@@ -687,30 +709,39 @@ ProjPlan plan_proj(int64_t Mp, int64_t Kc, int r64, int num_sms) {
     pl.tiles = (int)((Mp + 127) / 128);
     pl.ktiles = (int)((Kc + 63) / 64);
     const int per_sm = r64 <= 64 ? 2 : 1;
-    // as many splits as fit in one wave of resident CTAs
+    // splits of a tile form one cluster (at most 8, the portable cluster size)
     int64_t s = std::max<int64_t>(1, ((int64_t)per_sm * num_sms) / pl.tiles);
-    s = std::max<int64_t>(1, std::min<int64_t>(s, std::min<int64_t>(pl.ktiles, 32)));
+    s = std::max<int64_t>(1, std::min<int64_t>(s, std::min<int64_t>(pl.ktiles, 8)));
     pl.splits = (int)s;
-    pl.partial_bytes = pl.splits > 1 ? (size_t)pl.splits * (size_t)Mp * (size_t)r64 * 4 : 0;
+    pl.partial_bytes = 0;
     return pl;
+}
+
+template <bool kDX, int kSt>
+static cudaError_t launch_fused_t(const CUtensorMap &mc, const CUtensorMap &ms, const CUtensorMap &ma,
+                                  const CUtensorMap &ml, const FusedArgs &args, const FusedPlan &plan, cudaStream_t st) {
+    const size_t smem = fused_smem_bytes(plan.BN, kSt);
+    cudaError_t e = cudaFuncSetAttribute(nf4_lora_gemm_kernel<kDX, kSt>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    nf4_lora_gemm_kernel<kDX, kSt><<<plan.grid, kFusedThreads, smem, st>>>(mc, ms, ma, ml, args);
+    return cudaSuccess;
 }
 
 cudaError_t launch_fused(bool dx, const CUtensorMap &map_codes, const CUtensorMap &map_scales,
                          const CUtensorMap &map_act, const CUtensorMap &map_lora, const FusedArgs &args,
                          const FusedPlan &plan, cudaStream_t st) {
-    const size_t smem = fused_smem_bytes(plan.BN);
     cudaError_t e;
-    if (dx) {
-        e = cudaFuncSetAttribute(nf4_lora_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        nf4_lora_gemm_kernel<true>
-            <<<plan.grid, kFusedThreads, smem, st>>>(map_codes, map_scales, map_act, map_lora, args);
-    } else {
-        e = cudaFuncSetAttribute(nf4_lora_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        nf4_lora_gemm_kernel<false>
-            <<<plan.grid, kFusedThreads, smem, st>>>(map_codes, map_scales, map_act, map_lora, args);
-    }
+    const int S = plan.stages;
+    if (dx)
+        e = S == 8   ? launch_fused_t<true, 8>(map_codes, map_scales, map_act, map_lora, args, plan, st)
+            : S == 6 ? launch_fused_t<true, 6>(map_codes, map_scales, map_act, map_lora, args, plan, st)
+                     : launch_fused_t<true, 4>(map_codes, map_scales, map_act, map_lora, args, plan, st);
+    else
+        e = S == 8   ? launch_fused_t<false, 8>(map_codes, map_scales, map_act, map_lora, args, plan, st)
+            : S == 6 ? launch_fused_t<false, 6>(map_codes, map_scales, map_act, map_lora, args, plan, st)
+                     : launch_fused_t<false, 4>(map_codes, map_scales, map_act, map_lora, args, plan, st);
+    if (e != cudaSuccess) return e;
     count_launch();
     return cudaGetLastError();
 }
@@ -728,22 +759,36 @@ cudaError_t launch_splitk_reduce(const float *partial, int splits, int64_t rows,
     return cudaGetLastError();
 }
 
+template <bool PM, bool QM>
+static cudaError_t launch_proj_t(const CUtensorMap &map_p, const CUtensorMap &map_q, const ProjArgs &args,
+                                 cudaStream_t st) {
+    const size_t smem = proj_smem_bytes(args.r64);
+    cudaError_t e =
+        cudaFuncSetAttribute(lora_proj_kernel<PM, QM>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)(args.tiles * args.splits));
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)args.splits;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, lora_proj_kernel<PM, QM>, map_p, map_q, args);
+}
+
 cudaError_t launch_proj(bool p_mn, bool q_mn, const CUtensorMap &map_p, const CUtensorMap &map_q, const ProjArgs &args,
                         cudaStream_t st) {
-    const size_t smem = proj_smem_bytes(args.r64);
-    const int grid = args.tiles * args.splits;
-#define QLORA_PROJ_CASE(PM, QM)                                                                                     \
-    if (p_mn == PM && q_mn == QM) {                                                                                 \
-        cudaError_t e =                                                                                             \
-            cudaFuncSetAttribute(lora_proj_kernel<PM, QM>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
-        if (e != cudaSuccess) return e;                                                                             \
-        lora_proj_kernel<PM, QM><<<grid, 128, smem, st>>>(map_p, map_q, args);                                       \
-    }
-    QLORA_PROJ_CASE(false, false)
-    QLORA_PROJ_CASE(false, true)
-    QLORA_PROJ_CASE(true, false)
-    QLORA_PROJ_CASE(true, true)
-#undef QLORA_PROJ_CASE
+    cudaError_t e;
+    if (!p_mn && !q_mn) e = launch_proj_t<false, false>(map_p, map_q, args, st);
+    else if (!p_mn && q_mn) e = launch_proj_t<false, true>(map_p, map_q, args, st);
+    else if (p_mn && !q_mn) e = launch_proj_t<true, false>(map_p, map_q, args, st);
+    else e = launch_proj_t<true, true>(map_p, map_q, args, st);
+    if (e != cudaSuccess) return e;
     count_launch();
     return cudaGetLastError();
 }

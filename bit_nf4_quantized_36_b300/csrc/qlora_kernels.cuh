@@ -42,7 +42,7 @@ struct FusedArgs {
 };
 
 struct FusedPlan {
-    int BN, w_tiles, m_tiles, splits, kt_main, kt_lora, grid;
+    int BN, stages, w_tiles, m_tiles, splits, kt_main, kt_lora, grid;
     size_t partial_bytes;
 };
 FusedPlan plan_fused(int64_t M, int64_t wdim, int64_t kt_main, int r64, int num_sms);

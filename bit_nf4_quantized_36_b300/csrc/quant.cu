@@ -56,16 +56,29 @@ __global__ void __launch_bounds__(256) nf4_quantize_blocks_kernel(const float4 *
 }
 
 // K2a: S_g = fp64 sum of the group's scales in index order; slots ng..p2-1 get +0.0.
+// One warp per 32 groups: the warp stages its groups' 32 x 256 scales in shared memory with
+// coalesced loads, then each lane runs its group's sequential fp64 chain out of shared memory.
 __global__ void __launch_bounds__(32) dq_group_sums_kernel(const float *__restrict__ absmax, int64_t nb, int64_t ng,
-                                                            int64_t p2, double *__restrict__ tree) {
-    for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < p2; g += (int64_t)gridDim.x * blockDim.x) {
-        double acc = 0.0;
-        if (g < ng) {
-            const int64_t b0 = g * kGroup;
-            const int64_t b1 = (b0 + kGroup < nb) ? b0 + kGroup : nb;
-            for (int64_t b = b0; b < b1; ++b) acc = __dadd_rn(acc, (double)absmax[b]);
+                                                           int64_t p2, double *__restrict__ tree) {
+    __shared__ float sv[32][kGroup + 1];
+    const int lane = threadIdx.x;
+    for (int64_t g0 = (int64_t)blockIdx.x * 32; g0 < p2; g0 += (int64_t)gridDim.x * 32) {
+        for (int e = lane; e < 32 * kGroup; e += 32) {
+            const int64_t b = g0 * kGroup + e;
+            sv[e / kGroup][e % kGroup] = (b < nb) ? absmax[b] : 0.0f;
         }
-        tree[g] = acc;
+        __syncwarp();
+        const int64_t g = g0 + lane;
+        if (g < p2) {
+            double acc = 0.0;
+            if (g < ng) {
+                const int64_t cnt = (g * kGroup + kGroup <= nb) ? kGroup : nb - g * kGroup;
+#pragma unroll 8
+                for (int k = 0; k < cnt; ++k) acc = __dadd_rn(acc, (double)sv[lane][k]);
+            }
+            tree[g] = acc;
+        }
+        __syncwarp();
     }
 }
 
