@@ -462,6 +462,38 @@ def hbm_extras(q, _lib, L, dev, peaks, flush):
     return out
 
 
+def run_ncu_target(args):
+    """A short, untimed run for profiler captures: three forward+backward passes of the layer on the
+    bench workload (--ncu-target fused) or three small-M forwards on a 70B MLP matrix
+    (--ncu-target decode)."""
+    import torch
+
+    import bit_nf4_quantized_36_b300 as q
+    from bit_nf4_quantized_36_b300 import synth
+    dev = torch.device("cuda")
+    if args.ncu_target == "fused":
+        c = synth.LLAMA8B_ATTN
+        M, N, K, r, alpha = c["M"], c["N"], c["K"], c["r"], c["alpha"]
+    else:
+        M, N, K, r, alpha = args.decode_m, 28672, 8192, 16, 32.0
+    g = torch.Generator(device=dev)
+    g.manual_seed(synth.SEED_BASE + 7)
+    W = torch.randn((N, K), generator=g, device=dev) * 0.02
+    X = torch.randn((M, K), generator=g, device=dev).to(torch.bfloat16)
+    A = (torch.randn((r, K), generator=g, device=dev) / K ** 0.5).to(torch.bfloat16)
+    B = (torch.randn((N, r), generator=g, device=dev) * 0.01).to(torch.bfloat16)
+    G = torch.randn((M, N), generator=g, device=dev).to(torch.bfloat16)
+    qw = q.nf4_quantize(W)
+    for _ in range(3):
+        Y, U = q.qlora_linear_fwd(qw, X, A, B, alpha)
+        if args.ncu_target == "fused":
+            q.qlora_linear_bwd(qw, X, A, B, alpha, G, U)
+    torch.cuda.synchronize()
+    q.check_device_error()
+    print(json.dumps({"ncu_target": args.ncu_target, "M": M, "N": N, "K": K, "r": r, "ok": True}))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -470,7 +502,12 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true")
+    ap.add_argument("--ncu-target", choices=["fused", "decode"], default=None,
+                    help="untimed short run of one kernel family, for profiler captures")
+    ap.add_argument("--decode-m", type=int, default=1)
     args = ap.parse_args()
+    if args.ncu_target:
+        return run_ncu_target(args)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":

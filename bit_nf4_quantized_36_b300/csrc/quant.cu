@@ -56,29 +56,48 @@ __global__ void __launch_bounds__(256) nf4_quantize_blocks_kernel(const float4 *
 }
 
 // K2a: S_g = fp64 sum of the group's scales in index order; slots ng..p2-1 get +0.0.
-// One warp per 32 groups: the warp stages its groups' 32 x 256 scales in shared memory with
-// coalesced loads, then each lane runs its group's sequential fp64 chain out of shared memory.
-__global__ void __launch_bounds__(32) dq_group_sums_kernel(const float *__restrict__ absmax, int64_t nb, int64_t ng,
-                                                           int64_t p2, double *__restrict__ tree) {
-    __shared__ float sv[32][kGroup + 1];
-    const int lane = threadIdx.x;
-    for (int64_t g0 = (int64_t)blockIdx.x * 32; g0 < p2; g0 += (int64_t)gridDim.x * 32) {
-        for (int e = lane; e < 32 * kGroup; e += 32) {
-            const int64_t b = g0 * kGroup + e;
-            sv[e / kGroup][e % kGroup] = (b < nb) ? absmax[b] : 0.0f;
+// One warp per group.  The scales are non-negative fp32 values; when the group's non-zero scales
+// span at most 2^21 in binary exponent, every partial sum is an integer multiple of the smallest
+// scale's ulp below 2^(24 + 21 + 8) of it, hence exact in fp64, so any summation order -- here a
+// warp tree -- gives the bit pattern of the sequential sum.  Other groups (rare: scales differing
+// by more than 2^21) take the sequential chain in index order.
+__global__ void __launch_bounds__(256) dq_group_sums_kernel(const float *__restrict__ absmax, int64_t nb, int64_t ng,
+                                                            int64_t p2, double *__restrict__ tree) {
+    const uint32_t lane = threadIdx.x & 31u;
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x / 32);
+    for (int64_t g = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32; g < p2; g += warps) {
+        if (g >= ng) {
+            if (lane == 0) tree[g] = 0.0;
+            continue;
         }
-        __syncwarp();
-        const int64_t g = g0 + lane;
-        if (g < p2) {
-            double acc = 0.0;
-            if (g < ng) {
-                const int64_t cnt = (g * kGroup + kGroup <= nb) ? kGroup : nb - g * kGroup;
-#pragma unroll 8
-                for (int k = 0; k < cnt; ++k) acc = __dadd_rn(acc, (double)sv[lane][k]);
+        float v[8];
+        int emin = 255, emax = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int64_t b = g * kGroup + i * 32 + lane;
+            v[i] = (b < nb) ? absmax[b] : 0.0f;
+            const int e = (int)((__float_as_uint(v[i]) >> 23) & 0xFFu);
+            if (v[i] != 0.0f) {
+                emin = min(emin, e);
+                emax = max(emax, e);
             }
-            tree[g] = acc;
         }
-        __syncwarp();
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            emin = min(emin, __shfl_xor_sync(0xffffffffu, emin, o));
+            emax = max(emax, __shfl_xor_sync(0xffffffffu, emax, o));
+        }
+        double acc = 0.0;
+        if (emax - emin <= 21) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc = __dadd_rn(acc, (double)v[i]);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) acc = __dadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, o));
+        } else if (lane == 0) {
+            const int64_t b1 = (g * kGroup + kGroup < nb) ? g * kGroup + kGroup : nb;
+            for (int64_t b = g * kGroup; b < b1; ++b) acc = __dadd_rn(acc, (double)absmax[b]);
+        }
+        if (lane == 0) tree[g] = acc;
     }
 }
 
@@ -179,8 +198,7 @@ cudaError_t launch_quantize(const float *W, int64_t n, uint8_t *codes, int8_t *q
     nf4_quantize_blocks_kernel<<<grid_for(nb, 16, num_sms, 8), 256, 0, st>>>(
         reinterpret_cast<const float4 *>(W), nb, reinterpret_cast<uint16_t *>(codes), ws_absmax, tab);
     count_launch();
-    // one thread per group (a sequential fp64 chain); small CTAs spread the chains over many SMs
-    dq_group_sums_kernel<<<grid_for(p2, 32, num_sms, 64), 32, 0, st>>>(ws_absmax, nb, ng, p2, ws_tree);
+    dq_group_sums_kernel<<<grid_for(p2, 8, num_sms, 16), 256, 0, st>>>(ws_absmax, nb, ng, p2, ws_tree);
     count_launch();
     dq_mean_kernel<<<1, 1024, 0, st>>>(ws_tree, ws_tree + p2, p2, nb, mu);
     count_launch();
