@@ -18,7 +18,7 @@ import torch
 
 from . import _lib
 
-__all__ = ["NF4Weight", "QLoRAError", "nf4_quantize", "nf4_dequantize", "qlora_linear_fwd", "qlora_linear_bwd",
+__all__ = ["NF4Weight", "QLoRAError", "nf4_quantize", "nf4_quantize_noalloc", "nf4_dequantize", "qlora_linear_fwd", "qlora_linear_bwd",
            "nf4_storage_bytes", "quantize_workspace_bytes", "fwd_workspace_bytes", "bwd_workspace_bytes",
            "check_device_error", "launch_count", "nf4_levels", "empty_nf4"]
 
@@ -129,6 +129,15 @@ def nf4_quantize(W: torch.Tensor, out: NF4Weight | None = None, workspace: torch
     st = out.struct()
     _check(L.nf4_quantize(_ptr(W), ctypes.byref(st), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
            "nf4_quantize")
+    return out
+
+
+def nf4_quantize_noalloc(W: torch.Tensor, out: NF4Weight, stream=None) -> NF4Weight:
+    """nf4_quantize with the library's fixed scratch area instead of a workspace (for callers that
+    may not allocate device memory; rows * cols <= 2**28).  `out` must be preallocated."""
+    _need(W, torch.float32, "W", (out.rows, out.cols))
+    st = out.struct()
+    _check(_lib.load().nf4_quantize_noalloc(_ptr(W), ctypes.byref(st), _stream(stream)), "nf4_quantize_noalloc")
     return out
 
 

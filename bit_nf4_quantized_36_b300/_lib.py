@@ -18,7 +18,7 @@ EXPORTS = (
     "qlora_nf4_storage_bytes", "qlora_quantize_workspace_bytes", "qlora_fwd_workspace_bytes",
     "qlora_bwd_workspace_bytes", "nf4_quantize", "nf4_dequantize", "qlora_linear_fwd", "qlora_linear_bwd",
     "qlora_check_device_error", "qlora_status_string", "qlora_launch_count", "qlora_nf4_levels",
-    "qlora_set_kernel_timer", "qlora_kernel_timer_count",
+    "qlora_set_kernel_timer", "qlora_kernel_timer_count", "nf4_quantize_noalloc",
 )
 
 
@@ -47,6 +47,7 @@ def load():
         "qlora_bwd_workspace_bytes": (SZ, [I64, I64, I64, I32]),
         "nf4_quantize": (ctypes.c_int, [P, ST, P, SZ, P]),
         "nf4_dequantize": (ctypes.c_int, [ST, P, P]),
+        "nf4_quantize_noalloc": (ctypes.c_int, [P, ST, P]),
         "qlora_linear_fwd": (ctypes.c_int, [ST, P, I64, P, P, I32, ctypes.c_float, P, P, P, SZ, P]),
         "qlora_linear_bwd": (ctypes.c_int, [ST, P, I64, P, P, I32, ctypes.c_float, P, P, P, P, P, P, SZ, P]),
         "qlora_check_device_error": (ctypes.c_int, [P]),

@@ -3,3 +3,4 @@
 #include "quant.cu"
 #include "gemm.cu"
 #include "api.cu"
+#include "noalloc.cu"

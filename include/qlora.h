@@ -94,6 +94,20 @@ size_t qlora_bwd_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t r);
 qlora_status nf4_quantize(const float *W, const qlora_nf4_tensor *out, void *ws, size_t ws_bytes,
                           void *stream);
 
+/* nf4_quantize without a workspace argument, for callers that cannot allocate device memory:
+ * for example a serving process or plugin host that reserves its whole device-memory budget at
+ * start-up and forbids later allocations, or an embedding runtime whose allocator must not be
+ * bypassed.  (The source pages have no counterpart: this is an interface convenience.)
+ * Same result, bit for bit, as nf4_quantize.  The scratch space lives in a fixed area inside the
+ * library's device module (16 MiB + 256 KiB, held on every device that loads the library until
+ * the process exits), which limits the matrix to rows * cols <= 2^28 weights; larger matrices
+ * return QLORA_ERR_UNSUPPORTED_SHAPE without launching anything.  The call allocates nothing.
+ * The first call on a device looks up the scratch area's device address for that device; make
+ * that first call before starting any stream capture.  All calls on a device share the one area,
+ * so calls whose kernels may overlap on the GPU (different streams, or other host threads) race:
+ * order them, e.g. on one stream.  No state carries from one call to the next. */
+qlora_status nf4_quantize_noalloc(const float *W, const qlora_nf4_tensor *out, void *stream);
+
 /* Dequantize to bf16: W_out[rows, cols] = bf16_rne(NF4[c] * s'_b) ("Cuantiles": w^ = NF4[c] *
  * absmax; glossary: dequantized to bfloat16 before the matmul).  No workspace. */
 qlora_status nf4_dequantize(const qlora_nf4_tensor *q, uint16_t *W_out, void *stream);
