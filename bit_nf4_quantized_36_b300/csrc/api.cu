@@ -362,7 +362,7 @@ qlora_status qlora_linear_fwd(const qlora_nf4_tensor *W, const uint16_t *X, int6
     CUtensorMap mX_k, mA_k, mCodes, mScales, mX_act, mU_act;
     if (!map_bf16(&mX_k, X, K, M, 64, 128) || !map_bf16(&mA_k, A, K, r, 64, w.r64) ||
         !map_codes(&mCodes, W->codes, N, K, false) || !map_scales(&mScales, scalesT, N, KB, false) ||
-        !map_bf16(&mX_act, X, K, M, 64, w.fp.BN) || !map_bf16(&mU_act, U, w.r8, M, 64, w.fp.BN))
+        !map_bf16(&mX_act, X, K, M, 64, w.fp.act_rows) || !map_bf16(&mU_act, U, w.r8, M, 64, w.fp.act_rows))
         return QLORA_ERR_CUDA;
 
     cudaError_t e;
@@ -418,7 +418,7 @@ qlora_status qlora_linear_bwd(const qlora_nf4_tensor *W, const uint16_t *X, int6
         !map_bf16(&mX_mn, X, K, M, 64, 64) || !map_bf16(&mV_mn, V, w.r8, M, 64, 64) ||
         !map_bf16(&mG_mn, dY, N, M, 64, 64) || !map_bf16(&mU_mn, Uq, ru, M, 64, 64) ||
         !map_codes(&mCodes, W->codes, N, K, true) || !map_scales(&mScales, scalesT, N, KB, true) ||
-        !map_bf16(&mG_act, dY, N, M, 64, w.fp.BN) || !map_bf16(&mV_act, V, w.r8, M, 64, w.fp.BN))
+        !map_bf16(&mG_act, dY, N, M, 64, w.fp.act_rows) || !map_bf16(&mV_act, V, w.r8, M, 64, w.fp.act_rows))
         return QLORA_ERR_CUDA;
 
     uint32_t *cnt_u = counters, *cnt_v = cnt_u + w.pu.tiles, *cnt_da = cnt_v + w.pv.tiles;

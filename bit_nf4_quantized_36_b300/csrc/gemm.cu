@@ -19,6 +19,7 @@
 //    dA = V^T X, dB = G^T U), split over the contraction with fp32 partials and a fixed-order
 //    finalize (deterministic).
 #include <algorithm>
+#include <mutex>
 
 #include "qlora_common.cuh"
 #include "qlora_kernels.cuh"
@@ -130,53 +131,69 @@ __device__ __forceinline__ UnitInfo unit_info(const FusedArgs &p, int u) {
     return ui;
 }
 
+// One unit = a 256-row weight tile (128 rows per CTA of the pair) x BN tokens x one split of
+// the contraction.  The pair (a cluster of two CTAs on neighbouring SMs) shares every MMA:
+//   - each CTA stages and decodes its own 128 weight rows and TMA-loads BN/2 of the tokens;
+//   - the even CTA ("leader") issues tcgen05.mma.cta_group::2 with M = 256, N = BN, reading A
+//     and B from both CTAs' shared memory and accumulating into both CTAs' TMEM;
+//   - MMA completion is multicast to both CTAs' barriers; the odd CTA's decode and epilogue
+//     warps report to the leader's barriers by remote arrive.
+// Per SM this halves the inbound activation bytes and the MMA-issue work of a 128 x BN tile.
 template <bool kDX, int kStages>
-__global__ void __launch_bounds__(kFusedThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFusedThreads, 1)
     nf4_lora_gemm_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant__ CUtensorMap map_scales,
                          const __grid_constant__ CUtensorMap map_act, const __grid_constant__ CUtensorMap map_lora,
                          const FusedArgs p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
-    const uint32_t b_bytes = (uint32_t)p.BN * 128u;
+    const uint32_t bh_rows = (uint32_t)p.BN / 2u;     // token rows this CTA loads
+    const uint32_t b_bytes = bh_rows * 128u;          // per stage, this CTA
     uint8_t *sA = smem;
     uint8_t *sB = sA + kStages * kATileBytes;
     uint8_t *sC = sB + kStages * b_bytes;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sC + kStages * kCStageBytes);
-    uint64_t *full_c = bars;                 // codes + scales landed (or LoRA k-step announced)
-    uint64_t *full_b = bars + kStages;       // activation tile landed
-    uint64_t *full_a = bars + 2 * kStages;   // decoded weight tile written
-    uint64_t *empty = bars + 3 * kStages;    // MMAs reading the stage finished
-    uint64_t *acc_full = bars + 4 * kStages; // [2]
-    uint64_t *acc_empty = acc_full + 2;      // [2]
-    uint64_t *drain = acc_empty + 2;         // [1]
+    uint64_t *full_c = bars;                 // codes + scales landed (or LoRA k-step announced); local
+    uint64_t *full_b = bars + kStages;       // leader: both CTAs' token tiles landed
+    uint64_t *full_a = bars + 2 * kStages;   // leader: both CTAs' decoded weight tiles written
+    // both: the pair MMAs reading stages s & ~1 and s | 1 finished.  Completion is committed once
+    // per two stages (on empty[s | 1]) to halve the MMA thread's commit work; empty[s & ~1] is unused.
+    uint64_t *empty = bars + 3 * kStages;
+    uint64_t *acc_full = bars + 4 * kStages; // both [2]: accumulator ready
+    uint64_t *acc_empty = acc_full + 2;      // leader [2]: both CTAs drained the accumulator
+    uint64_t *drain = acc_empty + 2;         // leader [1]
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(drain + 1);
     volatile uint32_t *s_abort = s_tmem + 1;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_rank();
+    const bool leader = rank == 0;
+    const int pair_id = blockIdx.x >> 1;
+    const int num_pairs = gridDim.x >> 1;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full_c[s], 1);
             mbar_init(&full_b[s], 1);
-            mbar_init(&full_a[s], 4);  // the four warps of the stage's decode group
+            mbar_init(&full_a[s], 8);  // the four warps of the stage's decode group, in both CTAs
             mbar_init(&empty[s], 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&acc_full[a], 1);
-            mbar_init(&acc_empty[a], 4);
+            mbar_init(&acc_empty[a], 8);  // four epilogue warps in both CTAs
         }
         mbar_init(drain, 1);
         *s_abort = 0u;
         fence_mbar_init();
     }
     if (warp == 1) {
-        tmem_alloc(s_tmem, kTmemCols);
-        tmem_relinquish();
+        tmem_alloc_pair(s_tmem, kTmemCols);
+        tmem_relinquish_pair();
     }
     tc_fence_before();
     __syncthreads();
+    cluster_barrier();  // the peer's barriers are initialised before any remote arrival
     tc_fence_after();
     const uint32_t tmem_base = *s_tmem;
 
@@ -189,73 +206,81 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
             tma_prefetch_desc(&map_scales);
             tma_prefetch_desc(&map_act);
             tma_prefetch_desc(&map_lora);
+            const uint32_t full_b_leader = mapa_shared(full_b, 0);
             int s = 0;
             uint32_t ph = 0;
             uint32_t issued_parity[kStages];
             bool issued[kStages];
             for (int i = 0; i < kStages; ++i) issued[i] = false, issued_parity[i] = 0;
             bool ok = true;
-            for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
+            for (int u = pair_id; u < total_units && ok; u += num_pairs) {
                 const UnitInfo ui = unit_info(p, u);
+                const int wt = ui.w_tile * 2 + (int)rank;  // this CTA's 128-row weight tile
+                const int m_row = ui.m_tile * p.BN + (int)(rank * bh_rows);
                 for (int j = 0; j < ui.nk; ++j) {
-                    if (!mbar_wait(&empty[s], ph ^ 1u, s_abort)) { ok = false; break; }
+                    if (!mbar_wait_cl(&empty[s | 1], ph ^ 1u, s_abort)) { ok = false; break; }
                     const bool lora = (ui.kt0 + j) >= ui.kt1;
+                    if (leader) mbar_arrive_expect_tx(&full_b[s], 2u * b_bytes);
                     if (!lora) {
                         const int kt = ui.kt0 + j;
                         uint8_t *dc = sC + s * kCStageBytes;
                         mbar_arrive_expect_tx(&full_c[s], kCStageBytes);
                         if (kDX) {
-                            tma_load_2d(dc, &map_codes, &full_c[s], ui.w_tile * 64, kt * 64);
-                            tma_load_2d(dc + kCodesTileBytes, &map_scales, &full_c[s], kt * 64, ui.w_tile * 2);
+                            tma_load_2d(dc, &map_codes, &full_c[s], wt * 64, kt * 64);
+                            tma_load_2d(dc + kCodesTileBytes, &map_scales, &full_c[s], kt * 64, wt * 2);
                         } else {
-                            tma_load_2d(dc, &map_codes, &full_c[s], kt * 32, ui.w_tile * 128);
-                            tma_load_2d(dc + kCodesTileBytes, &map_scales, &full_c[s], ui.w_tile * 128, kt);
+                            tma_load_2d(dc, &map_codes, &full_c[s], kt * 32, wt * 128);
+                            tma_load_2d(dc + kCodesTileBytes, &map_scales, &full_c[s], wt * 128, kt);
                         }
-                        mbar_arrive_expect_tx(&full_b[s], b_bytes);
-                        tma_load_2d(sB + s * b_bytes, &map_act, &full_b[s], kt * 64, ui.m_tile * p.BN);
+                        tma_load_2d_pair(sB + s * b_bytes, &map_act, full_b_leader + (uint32_t)s * 8u, kt * 64, m_row);
                     } else {
                         const int lt = j - (ui.kt1 - ui.kt0);
                         mbar_arrive(&full_c[s]);
-                        mbar_arrive_expect_tx(&full_b[s], b_bytes);
-                        tma_load_2d(sB + s * b_bytes, &map_lora, &full_b[s], lt * 64, ui.m_tile * p.BN);
+                        tma_load_2d_pair(sB + s * b_bytes, &map_lora, full_b_leader + (uint32_t)s * 8u, lt * 64, m_row);
                     }
                     issued[s] = true;
                     issued_parity[s] = ph;
                     if (++s == kStages) { s = 0; ph ^= 1u; }
                 }
             }
-            if (!ok) {
+            if (ok) {
+                // every MMA commit aimed at this CTA has arrived before it may exit.  A parity
+                // wait only sees a barrier's latest phase, so each stage pair is waited on once,
+                // for the pass in which it was last used: that of its even stage, which every
+                // pass uses first.
+                for (int i = 0; i < kStages; i += 2) {
+                    if (issued[i] && !mbar_wait_cl(&empty[i + 1], issued_parity[i], s_abort)) break;
+                }
+            } else {
                 // let copies already in flight land before the CTA can exit
                 for (int i = 0; i < kStages; ++i) {
                     if (!issued[i]) continue;
                     const uint64_t t0 = globaltimer_ns();
-                    while (!mbar_try_wait(&full_b[i], issued_parity[i]) && globaltimer_ns() - t0 < 10000000ull) {}
+                    if (leader) while (!mbar_try_wait_cl(&full_b[i], issued_parity[i]) && globaltimer_ns() - t0 < 10000000ull) {}
                     while (!mbar_try_wait(&full_c[i], issued_parity[i]) && globaltimer_ns() - t0 < 20000000ull) {}
                 }
             }
         }
         __syncwarp();
     } else if (warp == 1) {
-        // ------------------------------ MMA issuer ---------------------------------------
-        if (lane == 0) {
-            const uint32_t idesc = make_idesc_bf16((uint32_t)p.BN, kDX, false);
+        // ------------------------------ MMA issuer (leader) ------------------------------
+        if (lane == 0 && leader) {
+            const uint32_t idesc = make_idesc_bf16((uint32_t)p.BN, kDX, false, 256u);
             const uint32_t a_base = smem_u32(sA), b_base = smem_u32(sB);
             int s = 0;
             uint32_t ph = 0;
             int lt = 0;
             bool ok = true;
             bool any = false;
-            for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x, ++lt) {
+            for (int u = pair_id; u < total_units && ok; u += num_pairs, ++lt) {
                 const UnitInfo ui = unit_info(p, u);
                 const int a = lt & 1;
-                if (!mbar_wait(&acc_empty[a], ((lt >> 1) & 1) ^ 1u, s_abort)) { ok = false; break; }
+                if (!mbar_wait_cl(&acc_empty[a], ((lt >> 1) & 1) ^ 1u, s_abort)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)a * 256u;
                 for (int j = 0; j < ui.nk; ++j) {
-                    if (!mbar_wait(&full_a[s], ph, s_abort) || !mbar_wait(&full_b[s], ph, s_abort)) {
-                        ok = false;
-                        break;
-                    }
+                    // full_a completes only after the leader's decode group has also seen full_b
+                    if (!mbar_wait_cl(&full_a[s], ph, s_abort)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t a_addr = a_base + (uint32_t)s * kATileBytes;
                     const uint32_t b_addr = b_base + (uint32_t)s * b_bytes;
@@ -264,32 +289,39 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
                         const uint64_t adesc = kDX ? make_sw128_desc(a_addr + kk * 2048u, 8192u, 1024u)
                                                    : make_sw128_desc(a_addr + kk * 32u, 16u, 1024u);
                         const uint64_t bdesc = make_sw128_desc(b_addr + kk * 32u, 16u, 1024u);
-                        umma_bf16(d_tmem, adesc, bdesc, idesc, (j > 0 || kk > 0) ? 1u : 0u);
+                        umma_bf16_pair(d_tmem, adesc, bdesc, idesc, (j > 0 || kk > 0) ? 1u : 0u);
                     }
                     any = true;
-                    umma_commit(&empty[s]);
+                    if (s & 1) umma_commit_pair_mc(&empty[s], 0x3);
                     if (++s == kStages) { s = 0; ph ^= 1u; }
                 }
                 if (!ok) break;
-                umma_commit(&acc_full[a]);
+                umma_commit_pair_mc(&acc_full[a], 0x3);
             }
+            // the last stage used was even: release its pair too
+            if (ok && (s & 1)) umma_commit_pair_mc(&empty[s], 0x3);
             if (!ok && any) {
-                umma_commit(drain);
+                umma_commit_pair_mc(drain, 0x1);
                 const uint64_t t0 = globaltimer_ns();
-                while (!mbar_try_wait(drain, 0) && globaltimer_ns() - t0 < 20000000ull) {}
+                while (!mbar_try_wait_cl(drain, 0) && globaltimer_ns() - t0 < 20000000ull) {}
             }
         }
         __syncwarp();
     } else if (warp < kDecodeWarp0) {
         // ------------------------------ epilogue -----------------------------------------
         const int quarter = warp & 3;  // TMEM lanes this warp may access
+        const uint32_t acc_empty_leader = mapa_shared(acc_empty, 0);
         int lt = 0;
-        for (int u = blockIdx.x; u < total_units; u += gridDim.x, ++lt) {
+        for (int u = pair_id; u < total_units; u += num_pairs, ++lt) {
             const UnitInfo ui = unit_info(p, u);
             const int a = lt & 1;
-            if (!warp_wait(&acc_full[a], (lt >> 1) & 1, s_abort)) break;
+            uint32_t okw = 0;
+            if (lane == 0) okw = mbar_wait_cl(&acc_full[a], (lt >> 1) & 1, s_abort) ? 1u : 0u;
+            okw = __shfl_sync(0xffffffffu, okw, 0);
+            __syncwarp();
+            if (!okw) break;
             tc_fence_after();
-            const int64_t f = (int64_t)ui.w_tile * 128 + quarter * 32 + lane;
+            const int64_t f = ((int64_t)ui.w_tile * 2 + rank) * 128 + quarter * 32 + lane;
             const int m0 = ui.m_tile * p.BN;
             const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)a * 256u;
             for (int c = 0; c < p.BN / 32; ++c) {
@@ -317,7 +349,10 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&acc_empty[a]);
+            if (lane == 0) {
+                if (leader) mbar_arrive(&acc_empty[a]);
+                else mbar_arrive_remote(acc_empty_leader + (uint32_t)a * 8u);
+            }
         }
     } else {
         // ------------------------------ decode warps -------------------------------------
@@ -327,6 +362,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         const int t = (threadIdx.x - kDecodeWarp0 * 32) & 127;  // row slot 0..127
         const int group = (threadIdx.x - kDecodeWarp0 * 32) >> 7;
         const uint32_t a_base = smem_u32(sA);
+        const uint32_t full_a_leader = mapa_shared(full_a, 0);
         const bool lora_vec = (p.lora_ld % 8) == 0;
         // per-thread geometry of the 128-row A tile
         uint32_t row_off, code_off, scale_off;
@@ -346,10 +382,11 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         int s = 0;
         uint32_t ph = 0;
         bool ok = true;
-        for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
+        for (int u = pair_id; u < total_units && ok; u += num_pairs) {
             const UnitInfo ui = unit_info(p, u);
-            const int64_t n_fwd = (int64_t)ui.w_tile * 128 + t;  // forward: weight row of this thread
-            const int kblock = ui.w_tile * 2 + kbl;              // backward: 64-column block along K
+            const int wt = ui.w_tile * 2 + (int)rank;
+            const int64_t n_fwd = (int64_t)wt * 128 + t;  // forward: weight row of this thread
+            const int kblock = wt * 2 + kbl;              // backward: 64-column block along K
             for (int j = 0; j < ui.nk; ++j) {
                 const int my_stage = (s & 1) == group;
                 if (my_stage) {
@@ -373,8 +410,12 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
                             for (int i = 0; i < 8; ++i) lv[i] = __ldg(src + i);
                         }
                     }
-                    if (!warp_wait(&empty[s], ph ^ 1u, s_abort)) { ok = false; break; }
-                    if (!warp_wait(&full_c[s], ph, s_abort)) { ok = false; break; }
+                    uint32_t okw = 0;
+                    if (lane == 0)
+                        okw = (mbar_wait_cl(&empty[s | 1], ph ^ 1u, s_abort) && mbar_wait(&full_c[s], ph, s_abort)) ? 1u : 0u;
+                    okw = __shfl_sync(0xffffffffu, okw, 0);
+                    __syncwarp();
+                    if (!okw) { ok = false; break; }
                     const uint32_t row_addr = a_base + (uint32_t)s * kATileBytes + row_off;
                     if (!valid) {
 #pragma unroll
@@ -401,7 +442,18 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
                     }
                     fence_proxy_async_smem();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&full_a[s]);
+                    if (lane == 0) {
+                        // the leader's group also waits for the pair's token tiles, so that the
+                        // MMA thread has a single barrier to wait on
+                        if (leader) {
+                            if (!mbar_wait_cl(&full_b[s], ph, s_abort)) ok = false;
+                            mbar_arrive(&full_a[s]);
+                        } else {
+                            mbar_arrive_remote(full_a_leader + (uint32_t)s * 8u);
+                        }
+                    }
+                    ok = __shfl_sync(0xffffffffu, ok ? 1u : 0u, 0) != 0;
+                    if (!ok) break;
                 }
                 if (++s == kStages) { s = 0; ph ^= 1u; }
             }
@@ -410,9 +462,10 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
 
     tc_fence_before();
     __syncthreads();
+    cluster_barrier();  // neither CTA leaves while the pair's MMAs or remote arrivals may still touch it
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, kTmemCols);
+        tmem_dealloc_pair(tmem_base, kTmemCols);
     }
 }
 
@@ -438,14 +491,6 @@ __device__ __forceinline__ void proj_store(const ProjArgs &a, int64_t i, int j, 
     }
 }
 
-__device__ __forceinline__ void cluster_sync_all() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
 __device__ __forceinline__ float4 ld_dsmem_f4(uint32_t local_addr, uint32_t rank) {
     uint32_t ra;
     float4 v;
@@ -476,7 +521,7 @@ __global__ void __launch_bounds__(128, 1)
     volatile uint32_t *s_abort = s_tmem + 1;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int split = (int)cluster_ctarank();  // the cluster spans the splits of one tile
+    const int split = (int)cluster_rank();  // the cluster spans the splits of one tile
     const int tile = blockIdx.x / a.splits;
     const int kt0 = (int)((int64_t)split * a.ktiles / a.splits);
     const int kt1 = (int)((int64_t)(split + 1) * a.ktiles / a.splits);
@@ -564,7 +609,7 @@ __global__ void __launch_bounds__(128, 1)
         }
     }
     tc_fence_before();
-    cluster_sync_all();
+    cluster_barrier();
     // Sum over the splits in split order; this CTA owns rows [r0, r1) of the tile.
     {
         const int rows_per = (128 + a.splits - 1) / a.splits;
@@ -592,7 +637,7 @@ __global__ void __launch_bounds__(128, 1)
             proj_store(a, i, j4 + 3, acc.w);
         }
     }
-    cluster_sync_all();  // peers read this CTA's shared memory until here
+    cluster_barrier();  // peers read this CTA's shared memory until here
     if (warp == 0) {
         tc_fence_after();
         tmem_dealloc(tmem_base, ncols);
@@ -659,17 +704,18 @@ __global__ void pad_2d_kernel(const uint16_t *__restrict__ src, int64_t rows_src
 // Plans and launchers
 // ---------------------------------------------------------------------------------------
 // Pipeline depth of the fused kernel: as many stages (even, <= 8) as fit in ~220 KB, so that a
-// small token tile keeps enough codes in flight to cover HBM latency.
+// small token tile keeps enough codes in flight to cover HBM latency.  Each CTA of the pair
+// holds BN/2 token rows per stage.
+static size_t fused_stage_bytes(int BN) { return kATileBytes + (size_t)(BN / 2) * 128 + kCStageBytes; }
 static int fused_stages(int BN) {
-    const size_t per = kATileBytes + (size_t)BN * 128 + kCStageBytes;
-    int st = (int)((220u * 1024u) / per);
+    int st = (int)((220u * 1024u) / fused_stage_bytes(BN));
     st = std::min(8, st) & ~1;
     return std::max(4, st);
 }
 // The fused kernel allocates all 512 TMEM columns, so it must be alone on its SM: asking for
 // more than half of the SM's shared memory guarantees one resident CTA.
 static size_t fused_smem_bytes(int BN, int stages) {
-    const size_t need = 1024 + (size_t)stages * (kATileBytes + (size_t)BN * 128 + kCStageBytes) + 512;
+    const size_t need = 1024 + (size_t)stages * fused_stage_bytes(BN) + 512;
     return std::max<size_t>(need, 120 * 1024);
 }
 static size_t proj_smem_bytes(int r64) { return 1024 + (size_t)kProjStages * (kATileBytes + (size_t)r64 * 128) + 128; }
@@ -679,27 +725,29 @@ FusedPlan plan_fused(int64_t M, int64_t wdim, int64_t kt_main, int r64, int num_
     int64_t bn = M >= 256 ? 256 : ((M + 31) / 32) * 32;
     if (bn < 32) bn = 32;
     pl.BN = (int)bn;
+    pl.act_rows = pl.BN / 2;
     pl.stages = fused_stages(pl.BN);
     pl.m_tiles = (int)((M + bn - 1) / bn);
-    pl.w_tiles = (int)((wdim + 127) / 128);
+    pl.w_tiles = (int)((wdim + 255) / 256);  // 256-row tiles, one per CTA pair
     pl.kt_main = (int)kt_main;
     pl.kt_lora = r64 / 64;
     pl.splits = 1;
+    const int pairs = std::max(1, num_sms / 2);
     const int64_t units = (int64_t)pl.w_tiles * pl.m_tiles;
-    if (pl.m_tiles == 1 && units < 2LL * num_sms) {
+    if (pl.m_tiles == 1 && units < 2LL * pairs) {
         // small token count: split the contraction so that the units fill whole waves
         int best = 1;
         double best_eff = 0.0;
         for (int s = 1; s <= 16 && s <= kt_main / 4; ++s) {
             const int64_t us = units * s;
-            const double eff = (double)us / (double)(((us + num_sms - 1) / num_sms) * num_sms);
+            const double eff = (double)us / (double)(((us + pairs - 1) / pairs) * pairs);
             if (eff > best_eff + 1e-9) { best_eff = eff; best = s; }
             if (eff >= 0.9) break;
         }
         pl.splits = best;
     }
     const int64_t total = units * pl.splits;
-    pl.grid = (int)std::min<int64_t>(total, num_sms);
+    pl.grid = 2 * (int)std::min<int64_t>(total, pairs);
     pl.partial_bytes = pl.splits > 1 ? (size_t)pl.splits * (size_t)M * (size_t)wdim * 4 : 0;
     return pl;
 }
@@ -717,6 +765,33 @@ ProjPlan plan_proj(int64_t Mp, int64_t Kc, int r64, int num_sms) {
     return pl;
 }
 
+// Clusters of two that can be resident at once for a given kernel and shared-memory size
+// (normally one per SM pair), cached per configuration.
+template <bool kDX, int kSt>
+static int max_pairs(size_t smem, int fallback) {
+    static std::mutex mu;
+    static size_t cached_smem = 0;
+    static int cached = 0;
+    static int cached_dev = -1;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return fallback;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cached_smem == smem && cached_dev == dev) return cached;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(2 * (unsigned)fallback, 1, 1);
+    cfg.blockDim = dim3(kFusedThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, nf4_lora_gemm_kernel<kDX, kSt>, &cfg) != cudaSuccess || n <= 0) {
+        (void)cudaGetLastError();
+        return fallback;
+    }
+    cached_smem = smem;
+    cached_dev = dev;
+    cached = n;
+    return n;
+}
+
 template <bool kDX, int kSt>
 static cudaError_t launch_fused_t(const CUtensorMap &mc, const CUtensorMap &ms, const CUtensorMap &ma,
                                   const CUtensorMap &ml, const FusedArgs &args, const FusedPlan &plan, cudaStream_t st) {
@@ -724,7 +799,10 @@ static cudaError_t launch_fused_t(const CUtensorMap &mc, const CUtensorMap &ms, 
     cudaError_t e = cudaFuncSetAttribute(nf4_lora_gemm_kernel<kDX, kSt>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
-    nf4_lora_gemm_kernel<kDX, kSt><<<plan.grid, kFusedThreads, smem, st>>>(mc, ms, ma, ml, args);
+    // units are dealt to pairs round-robin, so any even grid is correct; more pairs than can be
+    // resident would only run as a second, serial wave
+    const int grid = 2 * std::max(1, std::min(plan.grid / 2, max_pairs<kDX, kSt>(smem, plan.grid / 2)));
+    nf4_lora_gemm_kernel<kDX, kSt><<<grid, kFusedThreads, smem, st>>>(mc, ms, ma, ml, args);
     return cudaSuccess;
 }
 

@@ -32,7 +32,8 @@ struct FusedArgs {
     int64_t lora_ld;       // row stride of lora_src in elements (r or K)
     int32_t r;             // LoRA rank
     int32_t BN;            // token tile = MMA N (multiple of 32, <= 256)
-    int32_t w_tiles, m_tiles, splits;
+    int32_t w_tiles;       // 256-row weight tiles (one per CTA pair; 128 rows per CTA)
+    int32_t m_tiles, splits;
     int32_t kt_main;       // k-tiles of 64 over the main contraction (K or ceil(N / 64))
     int32_t kt_lora;       // ceil(r / 64)
     uint16_t *out;         // [M, wdim] bf16 (splits == 1)
@@ -42,15 +43,18 @@ struct FusedArgs {
 };
 
 struct FusedPlan {
-    int BN, stages, w_tiles, m_tiles, splits, kt_main, kt_lora, grid;
+    int BN;        // token tile = MMA N
+    int act_rows;  // token rows each CTA of the pair loads (BN / 2): the token maps' box height
+    int stages, w_tiles, m_tiles, splits, kt_main, kt_lora;
+    int grid;      // CTAs (even: clusters of two)
     size_t partial_bytes;
 };
 FusedPlan plan_fused(int64_t M, int64_t wdim, int64_t kt_main, int r64, int num_sms);
 
 // map_codes : codes as a 2-D byte tensor {K/2, N}; box {32, 128} (forward) or {64, 64} (backward)
 // map_scales: rebuilt block scales, fp32 {N, KB} (transposed, [KB][N]); box {128, 1} or {64, 2}
-// map_act   : X [M, K] (forward) or G [M, N] (backward), bf16, box {64, BN}, 128-byte swizzle
-// map_lora  : U or V [M, ld] bf16, box {64, BN}, 128-byte swizzle (columns >= r read as 0)
+// map_act   : X [M, K] (forward) or G [M, N] (backward), bf16, box {64, BN/2}, 128-byte swizzle
+// map_lora  : U or V [M, ld] bf16, box {64, BN/2}, 128-byte swizzle (columns >= r read as 0)
 cudaError_t launch_fused(bool dx, const CUtensorMap &map_codes, const CUtensorMap &map_scales,
                          const CUtensorMap &map_act, const CUtensorMap &map_lora, const FusedArgs &args,
                          const FusedPlan &plan, cudaStream_t st);
