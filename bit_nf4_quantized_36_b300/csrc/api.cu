@@ -24,7 +24,8 @@ static int32_t g_timer_cap = 0;
 static std::atomic<int32_t> g_timer_n{0};
 
 static cudaError_t timed_fused(bool dx, const CUtensorMap &mc, const CUtensorMap &ms, const CUtensorMap &ma,
-                               const CUtensorMap &ml, const FusedArgs &fa, const FusedPlan &fp, cudaStream_t st) {
+                               const CUtensorMap &ml, const CUtensorMap &mo, const FusedArgs &fa, const FusedPlan &fp,
+                               cudaStream_t st) {
     void **ev = g_timer_events;
     int32_t i = -1;
     if (ev) {
@@ -36,7 +37,7 @@ static cudaError_t timed_fused(bool dx, const CUtensorMap &mc, const CUtensorMap
         cudaGetLastError();
         i = -1;
     }
-    cudaError_t e = launch_fused(dx, mc, ms, ma, ml, fa, fp, st);
+    cudaError_t e = launch_fused(dx, mc, ms, ma, ml, mo, fa, fp, st);
     if (i >= 0 && cudaEventRecord(static_cast<cudaEvent_t>(ev[2 * i + 1]), st) != cudaSuccess) cudaGetLastError();
     return e;
 }
@@ -129,6 +130,11 @@ static bool make_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, i
 static bool map_bf16(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, uint32_t bi, uint32_t bo) {
     return make_map(m, base, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, inner, outer, inner, bi, bo, true);
 }
+// the fused kernel's bf16 output [rows, cols], stored through TMA in [32][128] tiles
+static bool map_out(CUtensorMap *m, const void *out, int64_t rows, int64_t cols) {
+    return make_map(m, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)cols, (uint64_t)rows, (uint64_t)cols, 128u,
+                    32u, false);
+}
 static bool map_codes(CUtensorMap *m, const void *codes, int64_t N, int64_t K, bool dx) {
     return make_map(m, codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)K / 2, (uint64_t)N, (uint64_t)K / 2,
                     dx ? 64u : 32u, dx ? 64u : 128u, false);
@@ -164,8 +170,7 @@ struct LayerWs {
     int r8, r64;
     FusedPlan fp;
     ProjPlan pu, pv, pda, pdb;
-    int ncounters;
-    size_t off_scales, off_counters, off_u, off_v, off_bpad, off_proj, off_main, total;
+    size_t off_scales, off_u, off_v, off_bpad, off_main, total;
 };
 static LayerWs layer_ws(int64_t M, int64_t N, int64_t K, int r, bool bwd, int num_sms) {
     LayerWs w{};
@@ -173,31 +178,23 @@ static LayerWs layer_ws(int64_t M, int64_t N, int64_t K, int r, bool bwd, int nu
     w.r64 = ((r + 63) / 64) * 64;
     const int64_t KB = K / 64;
     w.pu = plan_proj(M, K, w.r64, num_sms);
-    size_t proj = w.pu.partial_bytes;
-    w.ncounters = w.pu.tiles;
     if (bwd) {
         w.pv = plan_proj(M, N, w.r64, num_sms);
         w.pda = plan_proj(K, M, w.r64, num_sms);
         w.pdb = plan_proj(N, M, w.r64, num_sms);
-        proj = std::max(std::max(proj, w.pv.partial_bytes), std::max(w.pda.partial_bytes, w.pdb.partial_bytes));
-        w.ncounters += w.pv.tiles + w.pda.tiles + w.pdb.tiles;
         w.fp = plan_fused(M, K, (N + 63) / 64, w.r64, num_sms);
     } else {
         w.fp = plan_fused(M, N, K / 64, w.r64, num_sms);
     }
     size_t off = 0;
-    w.off_scales = off;
-    off += align256((size_t)KB * N * 4);
-    w.off_counters = off;
-    off += align256((size_t)w.ncounters * 4);
+    w.off_scales = off;  // rebuilt block scales, for the CTA-pair kernel only
+    if (!w.fp.small) off += align256((size_t)KB * N * 4);
     w.off_u = off;
     off += align256((size_t)M * w.r8 * 2);
     w.off_v = off;
     if (bwd) off += align256((size_t)M * w.r8 * 2);
     w.off_bpad = off;
     if (bwd && r % 8 != 0) off += align256((size_t)N * w.r8 * 2);
-    w.off_proj = off;
-    off += align256(proj);
     w.off_main = off;
     off += align256(w.fp.partial_bytes);
     w.total = off;
@@ -300,8 +297,7 @@ qlora_status nf4_dequantize(const qlora_nf4_tensor *q, uint16_t *W_out, void *st
                                        W_out, tables(), num_sms_current(), static_cast<cudaStream_t>(stream)));
 }
 
-static ProjArgs proj_args(const ProjPlan &pl, int64_t Mp, const LayerWs &w, int r, int mode, float scale,
-                          float *partial, uint32_t *counters) {
+static ProjArgs proj_args(const ProjPlan &pl, int64_t Mp, const LayerWs &w, int r, int mode, float scale) {
     ProjArgs a{};
     a.Mp = (int)Mp;
     a.r64 = w.r64;
@@ -311,8 +307,6 @@ static ProjArgs proj_args(const ProjPlan &pl, int64_t Mp, const LayerWs &w, int 
     a.ktiles = pl.ktiles;
     a.mode = mode;
     a.scale = scale;
-    a.partial = partial;
-    a.counters = counters;
     return a;
 }
 
@@ -335,6 +329,9 @@ static FusedArgs fused_args(const qlora_nf4_tensor *W, int64_t M, const LayerWs 
     fa.out = out;
     fa.partial = partial;
     fa.wdim = wdim;
+    fa.scale_q = W->scale_codes;
+    fa.scale_c2 = W->scale_scales;
+    fa.scale_mu = W->scale_offset;
     fa.tab = tables();
     return fa;
 }
@@ -353,31 +350,32 @@ qlora_status qlora_linear_fwd(const qlora_nf4_tensor *W, const uint16_t *X, int6
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     uint8_t *base = static_cast<uint8_t *>(ws);
     float *scalesT = reinterpret_cast<float *>(base + w.off_scales);
-    uint32_t *counters = reinterpret_cast<uint32_t *>(base + w.off_counters);
     uint16_t *U = reinterpret_cast<uint16_t *>(base + w.off_u);
-    float *proj = reinterpret_cast<float *>(base + w.off_proj);
     float *mainp = reinterpret_cast<float *>(base + w.off_main);
     const float scale = alpha / (float)r;
 
-    CUtensorMap mX_k, mA_k, mCodes, mScales, mX_act, mU_act;
+    CUtensorMap mX_k, mA_k, mCodes, mScales, mX_act, mU_act, mY;
+    std::memset(&mScales, 0, sizeof(mScales));
     if (!map_bf16(&mX_k, X, K, M, 64, 128) || !map_bf16(&mA_k, A, K, r, 64, w.r64) ||
-        !map_codes(&mCodes, W->codes, N, K, false) || !map_scales(&mScales, scalesT, N, KB, false) ||
-        !map_bf16(&mX_act, X, K, M, 64, w.fp.act_rows) || !map_bf16(&mU_act, U, w.r8, M, 64, w.fp.act_rows))
+        !map_codes(&mCodes, W->codes, N, K, false) ||
+        (!w.fp.small && !map_scales(&mScales, scalesT, N, KB, false)) ||
+        !map_bf16(&mX_act, X, K, M, 64, w.fp.act_rows) || !map_bf16(&mU_act, U, w.r8, M, 64, w.fp.act_rows) ||
+        !map_out(&mY, Y, M, N))
         return QLORA_ERR_CUDA;
 
     cudaError_t e;
-    if ((e = launch_dq_scales_t(W->scale_codes, W->scale_scales, W->scale_offset, N, (int)KB, scalesT, counters,
-                                w.ncounters, st)) != cudaSuccess)
+    if (!w.fp.small && (e = launch_dq_scales_t(W->scale_codes, W->scale_scales, W->scale_offset, N, (int)KB, scalesT,
+                                               st)) != cudaSuccess)
         return from_cuda(e);
     // U = bf16(s * X A^T)  [M, r8] (+ U_save [M, r])
-    ProjArgs pu = proj_args(w.pu, M, w, r, 0, scale, proj, counters);
+    ProjArgs pu = proj_args(w.pu, M, w, r, 0, scale);
     pu.out_h = U;
     pu.ld_h = w.r8;
     pu.out_h2 = U_save;
     if ((e = launch_proj(false, false, mX_k, mA_k, pu, st)) != cudaSuccess) return from_cuda(e);
     // Y = X W^T + U B^T
     const FusedArgs fa = fused_args(W, M, w, r, B, r, Y, mainp, N);
-    if ((e = timed_fused(false, mCodes, mScales, mX_act, mU_act, fa, w.fp, st)) != cudaSuccess) return from_cuda(e);
+    if ((e = timed_fused(false, mCodes, mScales, mX_act, mU_act, mY, fa, w.fp, st)) != cudaSuccess) return from_cuda(e);
     if (w.fp.splits > 1 && (e = launch_splitk_reduce(mainp, w.fp.splits, M, N, Y, sms, st)) != cudaSuccess)
         return from_cuda(e);
     return QLORA_OK;
@@ -398,11 +396,9 @@ qlora_status qlora_linear_bwd(const qlora_nf4_tensor *W, const uint16_t *X, int6
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     uint8_t *base = static_cast<uint8_t *>(ws);
     float *scalesT = reinterpret_cast<float *>(base + w.off_scales);
-    uint32_t *counters = reinterpret_cast<uint32_t *>(base + w.off_counters);
     uint16_t *U = reinterpret_cast<uint16_t *>(base + w.off_u);
     uint16_t *V = reinterpret_cast<uint16_t *>(base + w.off_v);
     uint16_t *Bpad = reinterpret_cast<uint16_t *>(base + w.off_bpad);
-    float *proj = reinterpret_cast<float *>(base + w.off_proj);
     float *mainp = reinterpret_cast<float *>(base + w.off_main);
     const float scale = alpha / (float)r;
     const bool r_vec = (r % 8) == 0;
@@ -412,47 +408,47 @@ qlora_status qlora_linear_bwd(const qlora_nf4_tensor *W, const uint16_t *X, int6
     const uint16_t *Bq = r_vec ? B : Bpad;
     const int64_t rb = r_vec ? r : w.r8;
 
-    CUtensorMap mX_k, mA_k, mG_k, mB_mn, mX_mn, mV_mn, mG_mn, mU_mn, mCodes, mScales, mG_act, mV_act;
+    CUtensorMap mX_k, mA_k, mG_k, mB_mn, mX_mn, mV_mn, mG_mn, mU_mn, mCodes, mScales, mG_act, mV_act, mDX;
+    std::memset(&mScales, 0, sizeof(mScales));
     if (!map_bf16(&mX_k, X, K, M, 64, 128) || !map_bf16(&mA_k, A, K, r, 64, w.r64) ||
         !map_bf16(&mG_k, dY, N, M, 64, 128) || !map_bf16(&mB_mn, Bq, rb, N, 64, 64) ||
         !map_bf16(&mX_mn, X, K, M, 64, 64) || !map_bf16(&mV_mn, V, w.r8, M, 64, 64) ||
         !map_bf16(&mG_mn, dY, N, M, 64, 64) || !map_bf16(&mU_mn, Uq, ru, M, 64, 64) ||
-        !map_codes(&mCodes, W->codes, N, K, true) || !map_scales(&mScales, scalesT, N, KB, true) ||
-        !map_bf16(&mG_act, dY, N, M, 64, w.fp.act_rows) || !map_bf16(&mV_act, V, w.r8, M, 64, w.fp.act_rows))
+        !map_codes(&mCodes, W->codes, N, K, true) || (!w.fp.small && !map_scales(&mScales, scalesT, N, KB, true)) ||
+        !map_bf16(&mG_act, dY, N, M, 64, w.fp.act_rows) || !map_bf16(&mV_act, V, w.r8, M, 64, w.fp.act_rows) ||
+        !map_out(&mDX, dX, M, K))
         return QLORA_ERR_CUDA;
 
-    uint32_t *cnt_u = counters, *cnt_v = cnt_u + w.pu.tiles, *cnt_da = cnt_v + w.pv.tiles;
-    uint32_t *cnt_db = cnt_da + w.pda.tiles;
     cudaError_t e;
-    if ((e = launch_dq_scales_t(W->scale_codes, W->scale_scales, W->scale_offset, N, (int)KB, scalesT, counters,
-                                w.ncounters, st)) != cudaSuccess)
+    if (!w.fp.small && (e = launch_dq_scales_t(W->scale_codes, W->scale_scales, W->scale_offset, N, (int)KB, scalesT,
+                                               st)) != cudaSuccess)
         return from_cuda(e);
     if (!r_vec && (e = launch_pad_2d(B, N, r, Bpad, N, w.r8, sms, st)) != cudaSuccess) return from_cuda(e);
     // U: the forward's saved copy, or recomputed
     if (U_saved) {
         if (!r_vec && (e = launch_pad_2d(U_saved, M, r, U, M, w.r8, sms, st)) != cudaSuccess) return from_cuda(e);
     } else {
-        ProjArgs pu = proj_args(w.pu, M, w, r, 0, scale, proj, cnt_u);
+        ProjArgs pu = proj_args(w.pu, M, w, r, 0, scale);
         pu.out_h = U;
         pu.ld_h = w.r8;
         if ((e = launch_proj(false, false, mX_k, mA_k, pu, st)) != cudaSuccess) return from_cuda(e);
     }
     // V = bf16(s * G B)  [M, r8]
-    ProjArgs pv = proj_args(w.pv, M, w, r, 0, scale, proj, cnt_v);
+    ProjArgs pv = proj_args(w.pv, M, w, r, 0, scale);
     pv.out_h = V;
     pv.ld_h = w.r8;
     if ((e = launch_proj(false, true, mG_k, mB_mn, pv, st)) != cudaSuccess) return from_cuda(e);
     // dX = G W^ + V A
     const FusedArgs fa = fused_args(W, M, w, r, A, K, dX, mainp, K);
-    if ((e = timed_fused(true, mCodes, mScales, mG_act, mV_act, fa, w.fp, st)) != cudaSuccess) return from_cuda(e);
+    if ((e = timed_fused(true, mCodes, mScales, mG_act, mV_act, mDX, fa, w.fp, st)) != cudaSuccess) return from_cuda(e);
     if (w.fp.splits > 1 && (e = launch_splitk_reduce(mainp, w.fp.splits, M, K, dX, sms, st)) != cudaSuccess)
         return from_cuda(e);
     // dA = V^T X  (D[k, j] = sum_m X[m, k] V[m, j], stored transposed)
-    ProjArgs pa = proj_args(w.pda, K, w, r, 1, 1.0f, proj, cnt_da);
+    ProjArgs pa = proj_args(w.pda, K, w, r, 1, 1.0f);
     pa.out_f = dA;
     if ((e = launch_proj(true, true, mX_mn, mV_mn, pa, st)) != cudaSuccess) return from_cuda(e);
     // dB = G^T U  (D[n, j] = sum_m G[m, n] U[m, j])
-    ProjArgs pb = proj_args(w.pdb, N, w, r, 2, 1.0f, proj, cnt_db);
+    ProjArgs pb = proj_args(w.pdb, N, w, r, 2, 1.0f);
     pb.out_f = dB;
     if ((e = launch_proj(true, true, mG_mn, mU_mn, pb, st)) != cudaSuccess) return from_cuda(e);
     return QLORA_OK;
@@ -476,7 +472,8 @@ qlora_status qlora_check_device_error(void *stream) {
     uint32_t word = 0, zero = 0;
     if (cudaMemcpyFromSymbol(&word, g_error_word, sizeof(word)) != cudaSuccess) return QLORA_ERR_CUDA;
     if (word && cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero)) != cudaSuccess) return QLORA_ERR_CUDA;
-    return (word & kErrTimeout) ? QLORA_ERR_TIMEOUT : QLORA_OK;
+    if (word & kErrTimeout) return QLORA_ERR_TIMEOUT;
+    return (word & kErrLayout) ? QLORA_ERR_CUDA : QLORA_OK;
 }
 
 }  // extern "C"

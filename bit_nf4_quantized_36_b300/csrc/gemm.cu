@@ -35,6 +35,7 @@ static constexpr int kFusedThreads = 448;              // 14 warps
 static constexpr int kDecodeWarp0 = 6;                 // warps 6..13 decode
 static constexpr int kEpiWarp0 = 2;                    // warps 2..5 epilogue
 static constexpr uint32_t kTmemCols = 512;             // two accumulators of up to 256 columns
+static constexpr uint32_t kOutStageBytes = 2u * 32u * 128u * 2u;  // two [32][128] bf16 store tiles
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     uint32_t d;
@@ -59,25 +60,26 @@ __device__ __forceinline__ void build_table(float s, const NF4Tables &tab, uint3
     }
 }
 
-// Look up 4 codes held in the low 16 bits of q, in nibble order (c1, c0, c3, c2) (the packing
-// puts element 2j in the high nibble of byte j), and return the bf16 pairs (e0 | e1 << 16) and
-// (e2 | e3 << 16).  The low 3 bits of each code select within 8-entry halves; bit 3 picks
-// the half.
-__device__ __forceinline__ void lookup4(uint32_t q, const uint32_t (&lo)[4], const uint32_t (&hi)[4], uint32_t &o0,
-                                        uint32_t &o1) {
-    const uint32_t sel = q & 0x7777u;
-    const uint32_t sel2 = ((q >> 1) & 0x4444u) | 0x3210u;
+// Look up 4 codes in nibble order (c1, c0, c3, c2) (the packing puts element 2j in the high
+// nibble of byte j) with selectors prepared by decode8, and return the bf16 pairs
+// (e0 | e1 << 16) and (e2 | e3 << 16).  The low 3 bits of each code select within 8-entry
+// halves (sel); bit 3 picks the half (sel2).
+__device__ __forceinline__ void lookup4(uint32_t sel, uint32_t sel2, const uint32_t (&lo)[4], const uint32_t (&hi)[4],
+                                        uint32_t &o0, uint32_t &o1) {
     const uint32_t l4 = prmt(prmt(lo[0], lo[1], sel), prmt(lo[2], lo[3], sel), sel2);
     const uint32_t h4 = prmt(prmt(hi[0], hi[1], sel), prmt(hi[2], hi[3], sel), sel2);
     o0 = prmt(l4, h4, 0x4051u);
     o1 = prmt(l4, h4, 0x6273u);
 }
 
-// 8 codes (one 32-bit word, elements 0..7) -> 4 words of bf16 pairs.
+// 8 codes (one 32-bit word, elements 0..7) -> 4 words of bf16 pairs.  The selectors of all 8
+// codes are formed at once (the byte permute reads only the low 16 bits of its selector).
 __device__ __forceinline__ uint4 decode8(uint32_t x, const uint32_t (&lo)[4], const uint32_t (&hi)[4]) {
+    const uint32_t sel = x & 0x77777777u;
+    const uint32_t sel2 = ((x >> 1) & 0x44444444u) | 0x32103210u;
     uint4 o;
-    lookup4(x, lo, hi, o.x, o.y);
-    lookup4(x >> 16, lo, hi, o.z, o.w);
+    lookup4(sel, sel2, lo, hi, o.x, o.y);
+    lookup4(sel >> 16, sel2 >> 16, lo, hi, o.z, o.w);
     return o;
 }
 
@@ -139,31 +141,51 @@ __device__ __forceinline__ UnitInfo unit_info(const FusedArgs &p, int u) {
 //   - MMA completion is multicast to both CTAs' barriers; the odd CTA's decode and epilogue
 //     warps report to the leader's barriers by remote arrive.
 // Per SM this halves the inbound activation bytes and the MMA-issue work of a 128 x BN tile.
-template <bool kDX, int kStages>
+//
+// kMT token tiles of BN per unit: with kMT = 2 every decoded weight tile feeds two MMAs (512
+// tokens), halving the decode work per FLOP -- the decode (integer-pipe byte permutes) is what
+// bounds a unit with one tile.  Two accumulators of 256 columns then fill the TMEM, so they are
+// not double-buffered: the next unit's MMAs wait for the epilogue (kMT = 1 keeps two buffers).
+template <bool kDX, int kStages, int kMT>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFusedThreads, 1)
     nf4_lora_gemm_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant__ CUtensorMap map_scales,
                          const __grid_constant__ CUtensorMap map_act, const __grid_constant__ CUtensorMap map_lora,
-                         const FusedArgs p) {
-    extern __shared__ uint8_t smem_raw[];
-    const uint32_t raw_addr = smem_u32(smem_raw);
-    uint8_t *smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
-    const uint32_t bh_rows = (uint32_t)p.BN / 2u;     // token rows this CTA loads
-    const uint32_t b_bytes = bh_rows * 128u;          // per stage, this CTA
+                         const __grid_constant__ CUtensorMap map_out, const FusedArgs p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // The 128-byte-swizzled tiles need 1024-byte alignment.  The dynamic shared memory of a
+    // kernel without static shared memory starts aligned, and the launch requests no slack for
+    // re-aligning (two-tile units use all 227 KB); should that not hold, every CTA (the layout
+    // is the same in all of them) reports it and does no work.
+    if (smem_u32(smem_raw) & 1023u) {
+        if (threadIdx.x == 0) atomicOr(&g_error_word, kErrLayout);
+        return;
+    }
+    uint8_t *smem = smem_raw;
+    const uint32_t bh_rows = (uint32_t)p.BN / 2u;     // token rows this CTA loads per tile
+    const uint32_t b_bytes = bh_rows * 128u;          // per token tile and stage, this CTA
+    const uint32_t bs_bytes = kMT * b_bytes;          // per stage, this CTA
+    constexpr int kBufs = kMT == 1 ? 2 : 1;           // accumulator buffers
+    // kMT == 2: stage completion is committed every stage (the MMA thread has slack at two
+    // MMAs per k16); kMT == 1: once per two stages, on empty[s | 1]
+    constexpr int kPairMask = kMT == 1 ? 1 : 0;
     uint8_t *sA = smem;
     uint8_t *sB = sA + kStages * kATileBytes;
-    uint8_t *sC = sB + kStages * b_bytes;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sC + kStages * kCStageBytes);
+    uint8_t *sC = sB + kStages * bs_bytes;
+    // kMT == 2: two [32 tokens][128 features] bf16 tiles staging the epilogue's TMA stores
+    uint8_t *sOut = sC + kStages * kCStageBytes;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sOut + (kMT == 2 ? kOutStageBytes : 0));
     uint64_t *full_c = bars;                 // codes + scales landed (or LoRA k-step announced); local
     uint64_t *full_b = bars + kStages;       // leader: both CTAs' token tiles landed
     uint64_t *full_a = bars + 2 * kStages;   // leader: both CTAs' decoded weight tiles written
     // both: the pair MMAs reading stages s & ~1 and s | 1 finished.  Completion is committed once
     // per two stages (on empty[s | 1]) to halve the MMA thread's commit work; empty[s & ~1] is unused.
     uint64_t *empty = bars + 3 * kStages;
-    uint64_t *acc_full = bars + 4 * kStages; // both [2]: accumulator ready
-    uint64_t *acc_empty = acc_full + 2;      // leader [2]: both CTAs drained the accumulator
+    uint64_t *acc_full = bars + 4 * kStages; // both [kBufs]: accumulator ready
+    uint64_t *acc_empty = acc_full + 2;      // leader [kBufs]: both CTAs drained the accumulator
     uint64_t *drain = acc_empty + 2;         // leader [1]
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(drain + 1);
     volatile uint32_t *s_abort = s_tmem + 1;
+    volatile uint32_t *s_epi_ok = s_tmem + 2;  // epilogue: the accumulator wait's outcome
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -216,11 +238,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFusedThreads, 1)
             for (int u = pair_id; u < total_units && ok; u += num_pairs) {
                 const UnitInfo ui = unit_info(p, u);
                 const int wt = ui.w_tile * 2 + (int)rank;  // this CTA's 128-row weight tile
-                const int m_row = ui.m_tile * p.BN + (int)(rank * bh_rows);
+                const int m_row = ui.m_tile * kMT * p.BN + (int)(rank * bh_rows);  // first tile's rows
                 for (int j = 0; j < ui.nk; ++j) {
-                    if (!mbar_wait_cl(&empty[s | 1], ph ^ 1u, s_abort)) { ok = false; break; }
+                    if (!mbar_wait_cl(&empty[s | kPairMask], ph ^ 1u, s_abort)) { ok = false; break; }
                     const bool lora = (ui.kt0 + j) >= ui.kt1;
-                    if (leader) mbar_arrive_expect_tx(&full_b[s], 2u * b_bytes);
+                    if (leader) mbar_arrive_expect_tx(&full_b[s], 2u * bs_bytes);
                     if (!lora) {
                         const int kt = ui.kt0 + j;
                         uint8_t *dc = sC + s * kCStageBytes;
@@ -232,11 +254,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFusedThreads, 1)
                             tma_load_2d(dc, &map_codes, &full_c[s], kt * 32, wt * 128);
                             tma_load_2d(dc + kCodesTileBytes, &map_scales, &full_c[s], wt * 128, kt);
                         }
-                        tma_load_2d_pair(sB + s * b_bytes, &map_act, full_b_leader + (uint32_t)s * 8u, kt * 64, m_row);
+#pragma unroll
+                        for (int i = 0; i < kMT; ++i)
+                            tma_load_2d_pair(sB + s * bs_bytes + i * b_bytes, &map_act, full_b_leader + (uint32_t)s * 8u,
+                                             kt * 64, m_row + i * p.BN);
                     } else {
                         const int lt = j - (ui.kt1 - ui.kt0);
                         mbar_arrive(&full_c[s]);
-                        tma_load_2d_pair(sB + s * b_bytes, &map_lora, full_b_leader + (uint32_t)s * 8u, lt * 64, m_row);
+#pragma unroll
+                        for (int i = 0; i < kMT; ++i)
+                            tma_load_2d_pair(sB + s * bs_bytes + i * b_bytes, &map_lora, full_b_leader + (uint32_t)s * 8u,
+                                             lt * 64, m_row + i * p.BN);
                     }
                     issued[s] = true;
                     issued_parity[s] = ph;
@@ -248,8 +276,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFusedThreads, 1)
                 // wait only sees a barrier's latest phase, so each stage pair is waited on once,
                 // for the pass in which it was last used: that of its even stage, which every
                 // pass uses first.
-                for (int i = 0; i < kStages; i += 2) {
-                    if (issued[i] && !mbar_wait_cl(&empty[i + 1], issued_parity[i], s_abort)) break;
+                for (int i = 0; i < kStages; i += 1 + kPairMask) {
+                    if (issued[i] && !mbar_wait_cl(&empty[i | kPairMask], issued_parity[i], s_abort)) break;
                 }
             } else {
                 // let copies already in flight land before the CTA can exit
@@ -274,32 +302,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFusedThreads, 1)
             bool any = false;
             for (int u = pair_id; u < total_units && ok; u += num_pairs, ++lt) {
                 const UnitInfo ui = unit_info(p, u);
-                const int a = lt & 1;
-                if (!mbar_wait_cl(&acc_empty[a], ((lt >> 1) & 1) ^ 1u, s_abort)) { ok = false; break; }
+                const int a = lt % kBufs;
+                if (!mbar_wait_cl(&acc_empty[a], ((lt / kBufs) & 1) ^ 1u, s_abort)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + (uint32_t)a * 256u;
+                const uint32_t d_tmem = tmem_base + (uint32_t)a * 256u;  // tile i at + i * 256
                 for (int j = 0; j < ui.nk; ++j) {
                     // full_a completes only after the leader's decode group has also seen full_b
                     if (!mbar_wait_cl(&full_a[s], ph, s_abort)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t a_addr = a_base + (uint32_t)s * kATileBytes;
-                    const uint32_t b_addr = b_base + (uint32_t)s * b_bytes;
+                    const uint32_t b_addr = b_base + (uint32_t)s * bs_bytes;
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t adesc = kDX ? make_sw128_desc(a_addr + kk * 2048u, 8192u, 1024u)
-                                                   : make_sw128_desc(a_addr + kk * 32u, 16u, 1024u);
-                        const uint64_t bdesc = make_sw128_desc(b_addr + kk * 32u, 16u, 1024u);
-                        umma_bf16_pair(d_tmem, adesc, bdesc, idesc, (j > 0 || kk > 0) ? 1u : 0u);
+                    for (int i = 0; i < kMT; ++i) {
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint64_t adesc = kDX ? make_sw128_desc(a_addr + kk * 2048u, 8192u, 1024u)
+                                                       : make_sw128_desc(a_addr + kk * 32u, 16u, 1024u);
+                            const uint64_t bdesc = make_sw128_desc(b_addr + i * b_bytes + kk * 32u, 16u, 1024u);
+                            umma_bf16_pair(d_tmem + (uint32_t)i * 256u, adesc, bdesc, idesc, (j > 0 || kk > 0) ? 1u : 0u);
+                        }
                     }
                     any = true;
-                    if (s & 1) umma_commit_pair_mc(&empty[s], 0x3);
+                    if ((s & kPairMask) == kPairMask) umma_commit_pair_mc(&empty[s], 0x3);
                     if (++s == kStages) { s = 0; ph ^= 1u; }
                 }
                 if (!ok) break;
                 umma_commit_pair_mc(&acc_full[a], 0x3);
             }
-            // the last stage used was even: release its pair too
-            if (ok && (s & 1)) umma_commit_pair_mc(&empty[s], 0x3);
+            // paired commits, and the last stage used was even: release its pair too
+            if (kPairMask && ok && (s & 1)) umma_commit_pair_mc(&empty[s], 0x3);
             if (!ok && any) {
                 umma_commit_pair_mc(drain, 0x1);
                 const uint64_t t0 = globaltimer_ns();
@@ -314,20 +345,59 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFusedThreads, 1)
         int lt = 0;
         for (int u = pair_id; u < total_units; u += num_pairs, ++lt) {
             const UnitInfo ui = unit_info(p, u);
-            const int a = lt & 1;
+            const int a = lt % kBufs;
             uint32_t okw = 0;
-            if (lane == 0) okw = mbar_wait_cl(&acc_full[a], (lt >> 1) & 1, s_abort) ? 1u : 0u;
-            okw = __shfl_sync(0xffffffffu, okw, 0);
-            __syncwarp();
+            if (kMT == 2) {
+                // one outcome for the four warps, which meet at named barriers below
+                if (threadIdx.x == kEpiWarp0 * 32) *s_epi_ok = mbar_wait_cl(&acc_full[a], (lt / kBufs) & 1, s_abort) ? 1u : 0u;
+                named_barrier_sync(2, 128);
+                okw = *s_epi_ok;
+                named_barrier_sync(2, 128);
+            } else {
+                if (lane == 0) okw = mbar_wait_cl(&acc_full[a], (lt / kBufs) & 1, s_abort) ? 1u : 0u;
+                okw = __shfl_sync(0xffffffffu, okw, 0);
+                __syncwarp();
+            }
             if (!okw) break;
             tc_fence_after();
             const int64_t f = ((int64_t)ui.w_tile * 2 + rank) * 128 + quarter * 32 + lane;
-            const int m0 = ui.m_tile * p.BN;
             const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)a * 256u;
-            for (int c = 0; c < p.BN / 32; ++c) {
+            const int nchunks = kMT * p.BN / 32;
+            for (int cc = 0; cc < nchunks; ++cc) {
+                const int i = cc / (p.BN / 32), c = cc % (p.BN / 32);  // token tile, 32-column chunk
+                const int m0 = (ui.m_tile * kMT + i) * p.BN;
                 uint32_t r[32];
-                tmem_ld_32x32b_x32(taddr + (uint32_t)c * 32u, r);
+                tmem_ld_32x32b_x32(taddr + (uint32_t)i * 256u + (uint32_t)c * 32u, r);
                 tmem_ld_wait();
+                if (kMT == 2 && p.splits == 1) {
+                    if (cc == nchunks - 1) {
+                        // the accumulator is read out: the next unit's MMAs may start
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) {
+                            if (leader) mbar_arrive(&acc_empty[a]);
+                            else mbar_arrive_remote(acc_empty_leader + (uint32_t)a * 8u);
+                        }
+                    }
+                    // [32 tokens][128 features] through shared memory, one TMA store per chunk
+                    const int et = threadIdx.x - kEpiWarp0 * 32;
+                    uint8_t *buf = sOut + (cc & 1) * (kOutStageBytes / 2);
+                    if (et == 0) bulk_wait_group_read<1>();  // the store two chunks back has read buf
+                    named_barrier_sync(1, 128);
+                    const uint32_t col = (uint32_t)(quarter * 32 + lane) * 2u;
+#pragma unroll
+                    for (int jj = 0; jj < 32; ++jj) {
+                        __nv_bfloat16 h = __float2bfloat16_rn(__uint_as_float(r[jj]));
+                        *reinterpret_cast<__nv_bfloat16 *>(buf + jj * 256 + col) = h;
+                    }
+                    fence_proxy_async_smem();
+                    named_barrier_sync(1, 128);
+                    if (et == 0) {
+                        tma_store_2d(&map_out, buf, (int)(((int64_t)ui.w_tile * 2 + rank) * 128), m0 + c * 32);
+                        bulk_commit_group();
+                    }
+                    continue;
+                }
                 if (f < p.wdim) {
                     if (p.splits == 1) {
 #pragma unroll
@@ -347,6 +417,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFusedThreads, 1)
                     }
                 }
             }
+            if (kMT == 2 && p.splits == 1) continue;  // released after the last TMEM read
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
@@ -354,6 +425,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFusedThreads, 1)
                 else mbar_arrive_remote(acc_empty_leader + (uint32_t)a * 8u);
             }
         }
+        // the output stores have completed before the CTA exits
+        if (kMT == 2 && threadIdx.x == kEpiWarp0 * 32) bulk_wait_group_all();
     } else {
         // ------------------------------ decode warps -------------------------------------
         // Two groups of four warps take alternate pipeline stages (stage s always goes to
@@ -412,7 +485,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFusedThreads, 1)
                     }
                     uint32_t okw = 0;
                     if (lane == 0)
-                        okw = (mbar_wait_cl(&empty[s | 1], ph ^ 1u, s_abort) && mbar_wait(&full_c[s], ph, s_abort)) ? 1u : 0u;
+                        okw = (mbar_wait_cl(&empty[s | kPairMask], ph ^ 1u, s_abort) && mbar_wait(&full_c[s], ph, s_abort)) ? 1u : 0u;
                     okw = __shfl_sync(0xffffffffu, okw, 0);
                     __syncwarp();
                     if (!okw) { ok = false; break; }
@@ -466,6 +539,318 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFusedThreads, 1)
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc_pair(tmem_base, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------------------------------
+// Small token counts (M <= 32, e.g. decoding).  Each weight is used by at most 32 tokens, so the
+// call is bound by streaming the packed codes and by the decode arithmetic, not by tensor FLOPs.
+// Differences from the pair kernel above:
+//   - single-CTA MMAs (M = 128, N = BN in {16, 32}): a pair MMA costs about twice the issue
+//     time per weight at this N;
+//   - two issuer warps take alternate k-steps into separate accumulators (the per-instruction
+//     issue cost, not the tensor pipe, bounds one issuer at small N); the epilogue adds them;
+//   - three decode groups (12 warps) over a 9-stage ring: the decode ALU work per byte of codes
+//     is the binding cost, so more warps hide the lookup latency;
+//   - codes, tokens and (for LoRA k-steps) U share one full barrier per stage;
+//   - the decode threads rebuild each block scale s'_b = fmaf(q_b, fl(c2_g / 127), mu) from the
+//     int8 code and the group constant themselves (bit-identical to nf4_dequantize), so the call
+//     reads 1 byte of scale per 64 weights instead of a rebuilt fp32 copy written beforehand.
+// ---------------------------------------------------------------------------------------
+static constexpr int kSmallIssuers = 2;
+static constexpr int kSmallGroups = 3;
+static constexpr int kSmallStages = 9;            // a multiple of kSmallGroups
+static constexpr int kSmallEpiWarp0 = 1 + kSmallIssuers;   // warps 3..6
+static constexpr int kSmallDecodeWarp0 = kSmallEpiWarp0 + 4;  // warps 7..18
+static constexpr int kSmallThreads = (kSmallDecodeWarp0 + 4 * kSmallGroups) * 32;  // 608
+static constexpr uint32_t kSmallTmemCols = 128;   // 2 buffers x 2 issuers x BN (<= 32)
+
+// s'_b of block b = row * KB + kb; the group constant fl(c2_g / 127) is cached across calls while
+// the group does not change.
+__device__ __forceinline__ float block_scale(const FusedArgs &p, float mu, int64_t row, int64_t kb, int64_t &g_cached,
+                                             float &k_cached) {
+    const int64_t b = row * p.KB + kb;
+    const int64_t g = b >> 8;
+    if (g != g_cached) {
+        g_cached = g;
+        k_cached = __fdiv_rn(__ldg(p.scale_c2 + g), 127.0f);
+    }
+    return __fmaf_rn((float)__ldg(p.scale_q + b), k_cached, mu);
+}
+
+template <bool kDX, int kBN>
+__global__ void __launch_bounds__(kSmallThreads, 1)
+    nf4_lora_gemm_small_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant__ CUtensorMap map_act,
+                               const __grid_constant__ CUtensorMap map_lora, const FusedArgs p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+    constexpr uint32_t b_bytes = (uint32_t)kBN * 128u;
+    uint8_t *sA = smem;
+    uint8_t *sB = sA + kSmallStages * kATileBytes;
+    uint8_t *sC = sB + kSmallStages * b_bytes;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sC + kSmallStages * kCodesTileBytes);
+    uint64_t *full = bars;                        // codes + tokens landed (TMA transaction count)
+    uint64_t *full_a = bars + kSmallStages;       // decoded weight tile written (4 warps)
+    uint64_t *empty = bars + 2 * kSmallStages;    // MMAs reading the stage finished
+    uint64_t *acc_full = bars + 3 * kSmallStages; // [2], one commit per issuer
+    uint64_t *acc_empty = acc_full + 2;           // [2], four epilogue warps
+    uint64_t *drain = acc_empty + 2;              // [kSmallIssuers]
+    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(drain + kSmallIssuers);
+    volatile uint32_t *s_abort = s_tmem + 1;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kSmallStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&full_a[s], 4);
+            mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&acc_full[a], kSmallIssuers);
+            mbar_init(&acc_empty[a], 4);
+        }
+        for (int i = 0; i < kSmallIssuers; ++i) mbar_init(&drain[i], 1);
+        *s_abort = 0u;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(s_tmem, kSmallTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *s_tmem;
+    const int total_units = p.w_tiles * p.m_tiles * p.splits;
+
+    if (warp == 0) {
+        // ------------------------------ TMA producer ------------------------------------
+        if (lane == 0) {
+            tma_prefetch_desc(&map_codes);
+            tma_prefetch_desc(&map_act);
+            tma_prefetch_desc(&map_lora);
+            int s = 0;
+            uint32_t ph = 0;
+            uint32_t issued_parity[kSmallStages];
+            bool issued[kSmallStages];
+            for (int i = 0; i < kSmallStages; ++i) issued[i] = false, issued_parity[i] = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
+                const UnitInfo ui = unit_info(p, u);
+                for (int j = 0; j < ui.nk; ++j) {
+                    if (!mbar_wait(&empty[s], ph ^ 1u, s_abort)) { ok = false; break; }
+                    const bool lora = (ui.kt0 + j) >= ui.kt1;
+                    if (!lora) {
+                        const int kt = ui.kt0 + j;
+                        mbar_arrive_expect_tx(&full[s], kCodesTileBytes + b_bytes);
+                        if (kDX) tma_load_2d(sC + s * kCodesTileBytes, &map_codes, &full[s], ui.w_tile * 64, kt * 64);
+                        else tma_load_2d(sC + s * kCodesTileBytes, &map_codes, &full[s], kt * 32, ui.w_tile * 128);
+                        tma_load_2d(sB + s * b_bytes, &map_act, &full[s], kt * 64, ui.m_tile * kBN);
+                    } else {
+                        const int lt = j - (ui.kt1 - ui.kt0);
+                        mbar_arrive_expect_tx(&full[s], b_bytes);
+                        tma_load_2d(sB + s * b_bytes, &map_lora, &full[s], lt * 64, ui.m_tile * kBN);
+                    }
+                    issued[s] = true;
+                    issued_parity[s] = ph;
+                    if (++s == kSmallStages) { s = 0; ph ^= 1u; }
+                }
+            }
+            if (!ok) {
+                for (int i = 0; i < kSmallStages; ++i) {
+                    if (!issued[i]) continue;
+                    const uint64_t t0 = globaltimer_ns();
+                    while (!mbar_try_wait(&full[i], issued_parity[i]) && globaltimer_ns() - t0 < 20000000ull) {}
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp <= kSmallIssuers) {
+        // ------------------------------ MMA issuers --------------------------------------
+        // Issuer i takes the k-steps g with g % kSmallIssuers == i of the CTA's step sequence
+        // and accumulates into its own TMEM columns.
+        const int me = warp - 1;
+        if (lane == 0) {
+            const uint32_t idesc = make_idesc_bf16((uint32_t)kBN, kDX, false);
+            const uint32_t a_base = smem_u32(sA), b_base = smem_u32(sB);
+            int s = 0, gstep = 0;
+            uint32_t ph = 0;
+            int lt = 0;
+            bool ok = true, any = false;
+            for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x, ++lt) {
+                const UnitInfo ui = unit_info(p, u);
+                const int a = lt & 1;
+                const uint32_t d_tmem = tmem_base + (uint32_t)((a * kSmallIssuers + me) * kBN);
+                bool first = true;
+                for (int j = 0; j < ui.nk; ++j, ++gstep) {
+                    if (gstep % kSmallIssuers == me) {
+                        if (first && !mbar_wait(&acc_empty[a], ((lt >> 1) & 1) ^ 1u, s_abort)) { ok = false; break; }
+                        if (!mbar_wait(&full_a[s], ph, s_abort)) { ok = false; break; }
+                        tc_fence_after();
+                        const uint32_t a_addr = a_base + (uint32_t)s * kATileBytes;
+                        const uint32_t b_addr = b_base + (uint32_t)s * b_bytes;
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint64_t adesc = kDX ? make_sw128_desc(a_addr + kk * 2048u, 8192u, 1024u)
+                                                       : make_sw128_desc(a_addr + kk * 32u, 16u, 1024u);
+                            const uint64_t bdesc = make_sw128_desc(b_addr + kk * 32u, 16u, 1024u);
+                            umma_bf16(d_tmem, adesc, bdesc, idesc, (!first || kk > 0) ? 1u : 0u);
+                        }
+                        first = false;
+                        any = true;
+                        umma_commit(&empty[s]);
+                    }
+                    if (++s == kSmallStages) { s = 0; ph ^= 1u; }
+                }
+                if (!ok) break;
+                umma_commit(&acc_full[a]);  // units have at least kSmallIssuers k-steps
+            }
+            if (!ok && any) {
+                umma_commit(&drain[me]);
+                const uint64_t t0 = globaltimer_ns();
+                while (!mbar_try_wait(&drain[me], 0) && globaltimer_ns() - t0 < 20000000ull) {}
+            }
+        }
+        __syncwarp();
+    } else if (warp < kSmallDecodeWarp0) {
+        // ------------------------------ epilogue -----------------------------------------
+        const int quarter = warp & 3;
+        int lt = 0;
+        for (int u = blockIdx.x; u < total_units; u += gridDim.x, ++lt) {
+            const UnitInfo ui = unit_info(p, u);
+            const int a = lt & 1;
+            if (!warp_wait(&acc_full[a], (lt >> 1) & 1, s_abort)) break;
+            tc_fence_after();
+            const int64_t f = (int64_t)ui.w_tile * 128 + quarter * 32 + lane;
+            const int m0 = ui.m_tile * kBN;
+            const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(a * kSmallIssuers * kBN);
+            float acc[kBN];
+#pragma unroll
+            for (int c = 0; c < kBN / 16; ++c) {
+                uint32_t r0[16], r1[16];
+                tmem_ld_32x32b_x16(taddr + (uint32_t)(c * 16), r0);
+                tmem_ld_32x32b_x16(taddr + (uint32_t)(kBN + c * 16), r1);
+                tmem_ld_wait();
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) acc[c * 16 + jj] = __fadd_rn(__uint_as_float(r0[jj]), __uint_as_float(r1[jj]));
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[a]);
+            if (f < p.wdim) {
+#pragma unroll
+                for (int jj = 0; jj < kBN; ++jj) {
+                    const int m = m0 + jj;
+                    if (m >= p.M) break;
+                    if (p.splits == 1) {
+                        __nv_bfloat16 h = __float2bfloat16_rn(acc[jj]);
+                        p.out[(int64_t)m * p.wdim + f] = *reinterpret_cast<uint16_t *>(&h);
+                    } else {
+                        p.partial[((int64_t)ui.split * p.M + m) * p.wdim + f] = acc[jj];
+                    }
+                }
+            }
+        }
+    } else {
+        // ------------------------------ decode warps -------------------------------------
+        // Group g (4 warps, one 128-byte A row per thread) takes the stages s with
+        // s % kSmallGroups == g; the ring length is a multiple of kSmallGroups.
+        const int t = (threadIdx.x - kSmallDecodeWarp0 * 32) & 127;
+        const int group = (threadIdx.x - kSmallDecodeWarp0 * 32) >> 7;
+        const uint32_t a_base = smem_u32(sA);
+        const bool lora_vec = (p.lora_ld % 8) == 0;
+        uint32_t row_off, code_off;
+        int nl = 0, kbl = 0;
+        if (!kDX) {
+            row_off = (uint32_t)t * 128u;
+            code_off = (uint32_t)t * 32u;
+        } else {
+            nl = t >> 1;
+            kbl = t & 1;
+            row_off = (uint32_t)kbl * 8192u + (uint32_t)nl * 128u;
+            code_off = (uint32_t)nl * 64u + (uint32_t)kbl * 32u;
+        }
+        const uint32_t r7 = (row_off >> 7) & 7u;
+        int64_t g_cached = -1;
+        float k_cached = 0.0f;
+        const float mu = __ldg(p.scale_mu);
+        int s = 0;
+        uint32_t ph = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
+            const UnitInfo ui = unit_info(p, u);
+            const int64_t n_fwd = (int64_t)ui.w_tile * 128 + t;
+            const int kblock = ui.w_tile * 2 + kbl;
+            for (int j = 0; j < ui.nk; ++j) {
+                if (s % kSmallGroups == group) {
+                    const bool lora = (ui.kt0 + j) >= ui.kt1;
+                    const int kt = lora ? j - (ui.kt1 - ui.kt0) : ui.kt0 + j;
+                    bool valid;
+                    int64_t srow = 0, skb = 0;
+                    uint4 lv[8];
+                    if (!kDX) {
+                        valid = n_fwd < p.N;
+                        srow = n_fwd;
+                        skb = kt;
+                        if (lora && valid) {
+                            const uint16_t *row = p.lora_src + n_fwd * p.lora_ld;
+                            load_row32(row, (int64_t)kt * 64, p.r, lora_vec, *reinterpret_cast<uint4(*)[4]>(&lv[0]));
+                            load_row32(row, (int64_t)kt * 64 + 32, p.r, lora_vec, *reinterpret_cast<uint4(*)[4]>(&lv[4]));
+                        }
+                    } else {
+                        const int64_t n = (int64_t)kt * 64 + nl;
+                        valid = kblock < p.KB && n < (lora ? (int64_t)p.r : p.N);
+                        srow = n;
+                        skb = kblock;
+                        if (lora && valid) {
+                            const uint4 *src = reinterpret_cast<const uint4 *>(p.lora_src + n * p.lora_ld + (int64_t)kblock * 64);
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) lv[i] = __ldg(src + i);
+                        }
+                    }
+                    // the block scale does not depend on the stage: fetch it before waiting
+                    const float sc = (valid && !lora) ? block_scale(p, mu, srow, skb, g_cached, k_cached) : 0.0f;
+                    if (!warp_wait(&empty[s], ph ^ 1u, s_abort)) { ok = false; break; }
+                    if (!warp_wait(&full[s], ph, s_abort)) { ok = false; break; }
+                    const uint32_t row_addr = a_base + (uint32_t)s * kATileBytes + row_off;
+                    if (!valid) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) st_shared_v4(row_addr + (((uint32_t)i ^ r7) << 4), make_uint4(0, 0, 0, 0));
+                    } else if (!lora) {
+                        const uint8_t *cst = sC + s * kCodesTileBytes;
+                        const uint4 c0 = *reinterpret_cast<const uint4 *>(cst + code_off);
+                        const uint4 c1 = *reinterpret_cast<const uint4 *>(cst + code_off + 16);
+                        uint32_t lo[4], hi[4];
+                        build_table(sc, p.tab, lo, hi);
+                        st_shared_v4(row_addr + ((0u ^ r7) << 4), decode8(c0.x, lo, hi));
+                        st_shared_v4(row_addr + ((1u ^ r7) << 4), decode8(c0.y, lo, hi));
+                        st_shared_v4(row_addr + ((2u ^ r7) << 4), decode8(c0.z, lo, hi));
+                        st_shared_v4(row_addr + ((3u ^ r7) << 4), decode8(c0.w, lo, hi));
+                        st_shared_v4(row_addr + ((4u ^ r7) << 4), decode8(c1.x, lo, hi));
+                        st_shared_v4(row_addr + ((5u ^ r7) << 4), decode8(c1.y, lo, hi));
+                        st_shared_v4(row_addr + ((6u ^ r7) << 4), decode8(c1.z, lo, hi));
+                        st_shared_v4(row_addr + ((7u ^ r7) << 4), decode8(c1.w, lo, hi));
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) st_shared_v4(row_addr + (((uint32_t)i ^ r7) << 4), lv[i]);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&full_a[s]);
+                }
+                if (++s == kSmallStages) { s = 0; ph ^= 1u; }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kSmallTmemCols);
     }
 }
 
@@ -647,12 +1032,11 @@ __global__ void __launch_bounds__(128, 1)
 // ---------------------------------------------------------------------------------------
 // Rebuilt block scales for the fused kernel: out[kb, n] = fmaf(q_b, fl32(c2_g / 127), mu) for
 // block b = n * KB + kb (transposed, so that a weight tile's scales are one contiguous TMA
-// box).  Block (0, 0) also zeroes the split-reduction counters of the call.
+// box).  Used by the CTA-pair kernel; the small-M kernel rebuilds the scales itself.
 // ---------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) dq_scales_t_kernel(const int8_t *__restrict__ q, const float *__restrict__ c2,
                                                           const float *__restrict__ mu_p, int64_t N, int KB,
-                                                          float *__restrict__ out, uint32_t *__restrict__ zero,
-                                                          int nzero) {
+                                                          float *__restrict__ out) {
     __shared__ float tile[32][33];
     const float mu = *mu_p;
     const int64_t n0 = (int64_t)blockIdx.x * 32;
@@ -674,8 +1058,6 @@ __global__ void __launch_bounds__(256) dq_scales_t_kernel(const int8_t *__restri
         const int64_t n = n0 + tx;
         if (n < N && kb < KB) out[(int64_t)kb * N + n] = tile[tx][i];
     }
-    if (blockIdx.x == 0 && blockIdx.y == 0)
-        for (int k = threadIdx.x; k < nzero; k += blockDim.x) zero[k] = 0u;
 }
 
 // ---------------------------------------------------------------------------------------
@@ -706,31 +1088,71 @@ __global__ void pad_2d_kernel(const uint16_t *__restrict__ src, int64_t rows_src
 // Pipeline depth of the fused kernel: as many stages (even, <= 8) as fit in ~220 KB, so that a
 // small token tile keeps enough codes in flight to cover HBM latency.  Each CTA of the pair
 // holds BN/2 token rows per stage.
-static size_t fused_stage_bytes(int BN) { return kATileBytes + (size_t)(BN / 2) * 128 + kCStageBytes; }
-static int fused_stages(int BN) {
-    int st = (int)((220u * 1024u) / fused_stage_bytes(BN));
+static size_t fused_stage_bytes(int BN, int mt) {
+    return kATileBytes + (size_t)mt * (BN / 2) * 128 + kCStageBytes;
+}
+static int fused_stages(int BN, int mt) {
+    int st = (int)((220u * 1024u) / fused_stage_bytes(BN, mt));
     st = std::min(8, st) & ~1;
     return std::max(4, st);
 }
 // The fused kernel allocates all 512 TMEM columns, so it must be alone on its SM: asking for
 // more than half of the SM's shared memory guarantees one resident CTA.
-static size_t fused_smem_bytes(int BN, int stages) {
-    const size_t need = 1024 + (size_t)stages * fused_stage_bytes(BN) + 512;
+static size_t fused_smem_bytes(int BN, int mt, int stages) {
+    const size_t need = (size_t)stages * fused_stage_bytes(BN, mt) + (mt == 2 ? kOutStageBytes : 0) + 512;
     return std::max<size_t>(need, 120 * 1024);
 }
 static size_t proj_smem_bytes(int r64) { return 1024 + (size_t)kProjStages * (kATileBytes + (size_t)r64 * 128) + 128; }
 
+static size_t small_smem_bytes(int BN) {
+    return 1024 + (size_t)kSmallStages * (kATileBytes + (size_t)BN * 128 + kCodesTileBytes) + 512;
+}
+
+// Small-M plan: 128-row tiles, all tokens in one tile, and the contraction split so that the
+// units fill whole waves.  Cost per SM, in bytes streamed: waves x codes per unit, plus the fp32
+// partials written and re-read by the split reduction (spread over all SMs) and a fixed charge
+// for the extra launch.
+static void plan_small(FusedPlan &pl, int64_t M, int64_t wdim, int64_t kt_main, int num_sms) {
+    pl.small = true;
+    pl.mt = 1;
+    pl.BN = M <= 16 ? 16 : 32;
+    pl.act_rows = pl.BN;
+    pl.stages = kSmallStages;
+    pl.m_tiles = 1;
+    pl.w_tiles = (int)((wdim + 127) / 128);
+    int best = 1;
+    double best_cost = 0.0;
+    // every split keeps at least kSmallIssuers main k-steps so that each issuer has work
+    const int64_t smax = std::max<int64_t>(1, std::min<int64_t>(32, kt_main / kSmallIssuers));
+    for (int64_t sp = 1; sp <= smax; ++sp) {
+        const int64_t units = (int64_t)pl.w_tiles * sp;
+        const int64_t waves = (units + num_sms - 1) / num_sms;
+        double cost = (double)waves * (double)((kt_main + sp - 1) / sp) * (double)kCodesTileBytes;
+        if (sp > 1) cost += 8.0 * (double)sp * (double)M * (double)wdim / (double)num_sms + 65536.0;
+        if (sp == 1 || cost < best_cost) { best_cost = cost; best = (int)sp; }
+    }
+    pl.splits = best;
+    pl.grid = (int)std::min<int64_t>((int64_t)pl.w_tiles * pl.splits, num_sms);
+    pl.partial_bytes = pl.splits > 1 ? (size_t)pl.splits * (size_t)M * (size_t)wdim * 4 : 0;
+}
+
 FusedPlan plan_fused(int64_t M, int64_t wdim, int64_t kt_main, int r64, int num_sms) {
     FusedPlan pl{};
+    pl.kt_main = (int)kt_main;
+    pl.kt_lora = r64 / 64;
+    if (M <= 32) {
+        plan_small(pl, M, wdim, kt_main, num_sms);
+        return pl;
+    }
+    pl.small = false;
     int64_t bn = M >= 256 ? 256 : ((M + 31) / 32) * 32;
     if (bn < 32) bn = 32;
     pl.BN = (int)bn;
+    pl.mt = M >= 512 ? 2 : 1;  // two 256-token tiles per decoded weight tile
     pl.act_rows = pl.BN / 2;
-    pl.stages = fused_stages(pl.BN);
-    pl.m_tiles = (int)((M + bn - 1) / bn);
+    pl.stages = fused_stages(pl.BN, pl.mt);
+    pl.m_tiles = (int)((M + bn * pl.mt - 1) / (bn * pl.mt));
     pl.w_tiles = (int)((wdim + 255) / 256);  // 256-row tiles, one per CTA pair
-    pl.kt_main = (int)kt_main;
-    pl.kt_lora = r64 / 64;
     pl.splits = 1;
     const int pairs = std::max(1, num_sms / 2);
     const int64_t units = (int64_t)pl.w_tiles * pl.m_tiles;
@@ -761,13 +1183,12 @@ ProjPlan plan_proj(int64_t Mp, int64_t Kc, int r64, int num_sms) {
     int64_t s = std::max<int64_t>(1, ((int64_t)per_sm * num_sms) / pl.tiles);
     s = std::max<int64_t>(1, std::min<int64_t>(s, std::min<int64_t>(pl.ktiles, 8)));
     pl.splits = (int)s;
-    pl.partial_bytes = 0;
     return pl;
 }
 
 // Clusters of two that can be resident at once for a given kernel and shared-memory size
 // (normally one per SM pair), cached per configuration.
-template <bool kDX, int kSt>
+template <bool kDX, int kSt, int kMT>
 static int max_pairs(size_t smem, int fallback) {
     static std::mutex mu;
     static size_t cached_smem = 0;
@@ -782,7 +1203,7 @@ static int max_pairs(size_t smem, int fallback) {
     cfg.blockDim = dim3(kFusedThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, nf4_lora_gemm_kernel<kDX, kSt>, &cfg) != cudaSuccess || n <= 0) {
+    if (cudaOccupancyMaxActiveClusters(&n, nf4_lora_gemm_kernel<kDX, kSt, kMT>, &cfg) != cudaSuccess || n <= 0) {
         (void)cudaGetLastError();
         return fallback;
     }
@@ -792,33 +1213,55 @@ static int max_pairs(size_t smem, int fallback) {
     return n;
 }
 
-template <bool kDX, int kSt>
+template <bool kDX, int kSt, int kMT = 1>
 static cudaError_t launch_fused_t(const CUtensorMap &mc, const CUtensorMap &ms, const CUtensorMap &ma,
-                                  const CUtensorMap &ml, const FusedArgs &args, const FusedPlan &plan, cudaStream_t st) {
-    const size_t smem = fused_smem_bytes(plan.BN, kSt);
-    cudaError_t e = cudaFuncSetAttribute(nf4_lora_gemm_kernel<kDX, kSt>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+                                  const CUtensorMap &ml, const CUtensorMap &mo, const FusedArgs &args,
+                                  const FusedPlan &plan, cudaStream_t st) {
+    const size_t smem = fused_smem_bytes(plan.BN, kMT, kSt);
+    cudaError_t e = cudaFuncSetAttribute(nf4_lora_gemm_kernel<kDX, kSt, kMT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     // units are dealt to pairs round-robin, so any even grid is correct; more pairs than can be
     // resident would only run as a second, serial wave
-    const int grid = 2 * std::max(1, std::min(plan.grid / 2, max_pairs<kDX, kSt>(smem, plan.grid / 2)));
-    nf4_lora_gemm_kernel<kDX, kSt><<<grid, kFusedThreads, smem, st>>>(mc, ms, ma, ml, args);
+    const int grid = 2 * std::max(1, std::min(plan.grid / 2, max_pairs<kDX, kSt, kMT>(smem, plan.grid / 2)));
+    nf4_lora_gemm_kernel<kDX, kSt, kMT><<<grid, kFusedThreads, smem, st>>>(mc, ms, ma, ml, mo, args);
+    return cudaSuccess;
+}
+
+template <bool kDX, int kBN>
+static cudaError_t launch_small_t(const CUtensorMap &mc, const CUtensorMap &ma, const CUtensorMap &ml,
+                                  const FusedArgs &args, const FusedPlan &plan, cudaStream_t st) {
+    const size_t smem = small_smem_bytes(kBN);
+    cudaError_t e = cudaFuncSetAttribute(nf4_lora_gemm_small_kernel<kDX, kBN>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    nf4_lora_gemm_small_kernel<kDX, kBN><<<plan.grid, kSmallThreads, smem, st>>>(mc, ma, ml, args);
     return cudaSuccess;
 }
 
 cudaError_t launch_fused(bool dx, const CUtensorMap &map_codes, const CUtensorMap &map_scales,
-                         const CUtensorMap &map_act, const CUtensorMap &map_lora, const FusedArgs &args,
-                         const FusedPlan &plan, cudaStream_t st) {
+                         const CUtensorMap &map_act, const CUtensorMap &map_lora, const CUtensorMap &map_out,
+                         const FusedArgs &args, const FusedPlan &plan, cudaStream_t st) {
     cudaError_t e;
     const int S = plan.stages;
-    if (dx)
-        e = S == 8   ? launch_fused_t<true, 8>(map_codes, map_scales, map_act, map_lora, args, plan, st)
-            : S == 6 ? launch_fused_t<true, 6>(map_codes, map_scales, map_act, map_lora, args, plan, st)
-                     : launch_fused_t<true, 4>(map_codes, map_scales, map_act, map_lora, args, plan, st);
+    if (plan.small) {
+        if (dx)
+            e = plan.BN == 16 ? launch_small_t<true, 16>(map_codes, map_act, map_lora, args, plan, st)
+                              : launch_small_t<true, 32>(map_codes, map_act, map_lora, args, plan, st);
+        else
+            e = plan.BN == 16 ? launch_small_t<false, 16>(map_codes, map_act, map_lora, args, plan, st)
+                              : launch_small_t<false, 32>(map_codes, map_act, map_lora, args, plan, st);
+    } else if (plan.mt == 2) {
+        e = dx ? launch_fused_t<true, 4, 2>(map_codes, map_scales, map_act, map_lora, map_out, args, plan, st)
+               : launch_fused_t<false, 4, 2>(map_codes, map_scales, map_act, map_lora, map_out, args, plan, st);
+    } else if (dx)
+        e = S == 8   ? launch_fused_t<true, 8>(map_codes, map_scales, map_act, map_lora, map_out, args, plan, st)
+            : S == 6 ? launch_fused_t<true, 6>(map_codes, map_scales, map_act, map_lora, map_out, args, plan, st)
+                     : launch_fused_t<true, 4>(map_codes, map_scales, map_act, map_lora, map_out, args, plan, st);
     else
-        e = S == 8   ? launch_fused_t<false, 8>(map_codes, map_scales, map_act, map_lora, args, plan, st)
-            : S == 6 ? launch_fused_t<false, 6>(map_codes, map_scales, map_act, map_lora, args, plan, st)
-                     : launch_fused_t<false, 4>(map_codes, map_scales, map_act, map_lora, args, plan, st);
+        e = S == 8   ? launch_fused_t<false, 8>(map_codes, map_scales, map_act, map_lora, map_out, args, plan, st)
+            : S == 6 ? launch_fused_t<false, 6>(map_codes, map_scales, map_act, map_lora, map_out, args, plan, st)
+                     : launch_fused_t<false, 4>(map_codes, map_scales, map_act, map_lora, map_out, args, plan, st);
     if (e != cudaSuccess) return e;
     count_launch();
     return cudaGetLastError();
@@ -872,9 +1315,9 @@ cudaError_t launch_proj(bool p_mn, bool q_mn, const CUtensorMap &map_p, const CU
 }
 
 cudaError_t launch_dq_scales_t(const int8_t *q, const float *c2, const float *mu, int64_t N, int KB, float *out,
-                               uint32_t *zero, int nzero, cudaStream_t st) {
+                               cudaStream_t st) {
     dim3 grid((unsigned)((N + 31) / 32), (unsigned)((KB + 31) / 32));
-    dq_scales_t_kernel<<<grid, 256, 0, st>>>(q, c2, mu, N, KB, out, zero, nzero);
+    dq_scales_t_kernel<<<grid, 256, 0, st>>>(q, c2, mu, N, KB, out);
     count_launch();
     return cudaGetLastError();
 }

@@ -32,19 +32,27 @@ struct FusedArgs {
     int64_t lora_ld;       // row stride of lora_src in elements (r or K)
     int32_t r;             // LoRA rank
     int32_t BN;            // token tile = MMA N (multiple of 32, <= 256)
-    int32_t w_tiles;       // 256-row weight tiles (one per CTA pair; 128 rows per CTA)
-    int32_t m_tiles, splits;
+    int32_t w_tiles;       // weight tiles: 256 rows (CTA pairs) or 128 rows (small kernel)
+    int32_t m_tiles;       // units along the tokens (each mt token tiles of BN)
+    int32_t splits;
     int32_t kt_main;       // k-tiles of 64 over the main contraction (K or ceil(N / 64))
     int32_t kt_lora;       // ceil(r / 64)
     uint16_t *out;         // [M, wdim] bf16 (splits == 1)
     float *partial;        // [splits, M, wdim] fp32 (splits > 1)
     int64_t wdim;          // output features: N (forward) or K (backward)
+    // the NF4 tensor's own scale data, read by the small-M kernel (which rebuilds s'_b itself)
+    const int8_t *scale_q;   // [N * KB] int8 block-scale codes
+    const float *scale_c2;   // [ng] group constants
+    const float *scale_mu;   // [1] scale offset
     NF4Tables tab;
 };
 
 struct FusedPlan {
+    bool small;    // M <= 32: single-CTA small-token kernel (else CTA pairs)
     int BN;        // token tile = MMA N
-    int act_rows;  // token rows each CTA of the pair loads (BN / 2): the token maps' box height
+    int mt;        // token tiles per unit (CTA pairs: 2 when M >= 512)
+    int act_rows;  // token rows each CTA loads (BN / 2 for pairs, BN for the small kernel): the
+                   // token maps' box height
     int stages, w_tiles, m_tiles, splits, kt_main, kt_lora;
     int grid;      // CTAs (even: clusters of two)
     size_t partial_bytes;
@@ -55,22 +63,24 @@ FusedPlan plan_fused(int64_t M, int64_t wdim, int64_t kt_main, int r64, int num_
 // map_scales: rebuilt block scales, fp32 {N, KB} (transposed, [KB][N]); box {128, 1} or {64, 2}
 // map_act   : X [M, K] (forward) or G [M, N] (backward), bf16, box {64, BN/2}, 128-byte swizzle
 // map_lora  : U or V [M, ld] bf16, box {64, BN/2}, 128-byte swizzle (columns >= r read as 0)
+// map_out   : the output [M, wdim] bf16, box {128, 32}, no swizzle (two-tile pair units store
+//             through it)
 cudaError_t launch_fused(bool dx, const CUtensorMap &map_codes, const CUtensorMap &map_scales,
-                         const CUtensorMap &map_act, const CUtensorMap &map_lora, const FusedArgs &args,
-                         const FusedPlan &plan, cudaStream_t st);
+                         const CUtensorMap &map_act, const CUtensorMap &map_lora, const CUtensorMap &map_out,
+                         const FusedArgs &args, const FusedPlan &plan, cudaStream_t st);
 cudaError_t launch_splitk_reduce(const float *partial, int splits, int64_t rows, int64_t cols, uint16_t *out,
                                  int num_sms, cudaStream_t st);
-// out[kb, n] = fmaf(q[n*KB + kb], fl32(c2 / 127), mu); also zeroes zero[0..nzero)
+// out[kb, n] = fmaf(q[n*KB + kb], fl32(c2 / 127), mu)
 cudaError_t launch_dq_scales_t(const int8_t *q, const float *c2, const float *mu, int64_t N, int KB, float *out,
-                               uint32_t *zero, int nzero, cudaStream_t st);
+                               cudaStream_t st);
 
 // ---- skinny LoRA products D[i, j] = sum_c P[i, c] Q[j, c], j < r64 (gemm.cu) -------------
 // P: K-major ([Mp, Kc] row-major, map dims {Kc, Mp}, box {64, 128}) or
 //    MN-major ([Kc, Mp] row-major, map dims {Mp, Kc}, box {64, 64}).
 // Q: K-major ([r, Kc], map dims {Kc, r}, box {64, r64}) or
 //    MN-major ([Kc, r], map dims {r, Kc}, box {64, 64}); rows/columns >= r read as zero.
-// Split over the contraction; the last CTA of each 128-row tile sums the fp32 partials in
-// split order and stores:
+// Split over the contraction across the CTAs of one cluster, whose fp32 partial tiles are summed
+// in split order through distributed shared memory, and stored:
 //   mode 0: out_h[i, j] = bf16(scale * D) for j < ld_h; out_h2[i, j] (nullable) for j < r
 //   mode 1: out_f[j, i] = D for j < r  (transposed fp32)
 //   mode 2: out_f[i, j] = D for j < r  (fp32)
@@ -78,8 +88,6 @@ struct ProjArgs {
     int Mp, r64, r, tiles, splits, ktiles;
     int mode;
     float scale;
-    float *partial;        // [splits, Mp, r64] when splits > 1
-    uint32_t *counters;    // [tiles], zero before the launch (left zero after it)
     uint16_t *out_h;
     int ld_h;
     uint16_t *out_h2;
@@ -87,7 +95,6 @@ struct ProjArgs {
 };
 struct ProjPlan {
     int tiles, splits, ktiles;
-    size_t partial_bytes;
 };
 ProjPlan plan_proj(int64_t Mp, int64_t Kc, int r64, int num_sms);
 cudaError_t launch_proj(bool p_mn, bool q_mn, const CUtensorMap &map_p, const CUtensorMap &map_q, const ProjArgs &args,
