@@ -219,6 +219,18 @@ def run_reference(args):
 # ---------------------------------------------------------------------------------------
 # Our arm
 # ---------------------------------------------------------------------------------------
+def fused_kernel_source_sha():
+    """sha256 of the fused kernel's source: gemm.cu from its first device helper up to the skinny
+    LoRA products (the decode helpers and nf4_lora_gemm_kernel), so that edits elsewhere in the file
+    do not void a profile taken of this kernel."""
+    src = open(os.path.join(ROOT, "bit_nf4_quantized_36_b300", "csrc", "gemm.cu")).read()
+    a = src.find("__device__ __forceinline__ uint32_t prmt(")
+    b = src.find("// Skinny LoRA products")
+    if a < 0 or b < a:
+        return None
+    return hashlib.sha256(src[a:b].encode()).hexdigest()
+
+
 def traffic_from_profile(gemm_src_sha):
     """DRAM bytes per fused-kernel launch from the committed ncu summary, if that summary was
     taken on the current kernel source; otherwise None."""
@@ -330,8 +342,7 @@ def run_ours(args):
     fl_fwd = 2.0 * M * N * K + 2.0 * M * N * r
     fl_dx = 2.0 * M * N * K + 2.0 * M * K * r
     achieved = (fl_fwd + fl_dx) / ((t_fwd + t_dx) * 1e-3) / 1e12
-    gemm_src = os.path.join(ROOT, "bit_nf4_quantized_36_b300", "csrc", "gemm.cu")
-    src_sha = hashlib.sha256(open(gemm_src, "rb").read()).hexdigest()
+    src_sha = fused_kernel_source_sha()
     roofline = {"kernel": "nf4_lora_gemm_kernel (fused NF4-dequant tcgen05 GEMM; forward and dX launches)",
                 "bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": achieved / peaks["bf16_tflops"], "traffic": traffic_from_profile(src_sha),
@@ -455,7 +466,8 @@ def hbm_extras(q, _lib, L, dev, peaks, flush):
         L.qlora_set_kernel_timer(None, 0)
         tk = statistics.median(kev[2 * i].elapsed_time(kev[2 * i + 1]) for i in range(10))
         byt = storage + 2 * r * (rows + cols) + 2 * M * (rows + cols)
-        dec[f"M={M}"] = {"call_ms": t, "fused_kernel_ms": tk, "GB/s_kernel": byt / tk / 1e6,
+        dec[f"M={M}"] = {"call_ms": t, "kernel": "nf4_gemv_kernel + gemv_finish_kernel" if M <= 2
+                         else "nf4_lora_gemm_small_kernel", "kernel_ms": tk, "GB/s_kernel": byt / tk / 1e6,
                          "frac_hbm_kernel": byt / tk / 1e6 / peaks["hbm_gbs"], "GB/s_call": byt / t / 1e6}
     out["decode_forward_28672x8192_r16"] = dec
     out["hbm_peak_GB/s"] = f"{peaks['hbm_gbs']} ({peaks['source']})"

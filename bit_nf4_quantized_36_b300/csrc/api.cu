@@ -18,27 +18,37 @@ namespace qlora {
 static std::atomic<uint64_t> g_launches{0};
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
-// optional event pairs around the fused kernel (benchmark instrumentation)
+// optional event pairs around the weight-streaming step of a call (benchmark instrumentation)
 static void **g_timer_events = nullptr;
 static int32_t g_timer_cap = 0;
 static std::atomic<int32_t> g_timer_n{0};
 
+// Records the opening event of a timed step; returns its slot, or -1 when not timing.  A failed
+// record (e.g. a NULL handle) must not be reported as the kernel's launch error.
+static int32_t timer_open(cudaStream_t st) {
+    void **ev = g_timer_events;
+    if (!ev) return -1;
+    int32_t i = g_timer_n.fetch_add(1);
+    if (i >= g_timer_cap) return -1;
+    if (cudaEventRecord(static_cast<cudaEvent_t>(ev[2 * i]), st) != cudaSuccess) {
+        cudaGetLastError();
+        return -1;
+    }
+    return i;
+}
+static void timer_close(int32_t i, cudaStream_t st) {
+    void **ev = g_timer_events;
+    if (i >= 0 && ev && cudaEventRecord(static_cast<cudaEvent_t>(ev[2 * i + 1]), st) != cudaSuccess) cudaGetLastError();
+}
+
+// the fused GEMM and, when the contraction is split, the reduction of its partials
 static cudaError_t timed_fused(bool dx, const CUtensorMap &mc, const CUtensorMap &ms, const CUtensorMap &ma,
                                const CUtensorMap &ml, const CUtensorMap &mo, const FusedArgs &fa, const FusedPlan &fp,
-                               cudaStream_t st) {
-    void **ev = g_timer_events;
-    int32_t i = -1;
-    if (ev) {
-        i = g_timer_n.fetch_add(1);
-        if (i >= g_timer_cap) i = -1;
-    }
-    // a failed record (e.g. a NULL handle) must not be reported as the kernel's launch error
-    if (i >= 0 && cudaEventRecord(static_cast<cudaEvent_t>(ev[2 * i]), st) != cudaSuccess) {
-        cudaGetLastError();
-        i = -1;
-    }
+                               int num_sms, cudaStream_t st) {
+    const int32_t i = timer_open(st);
     cudaError_t e = launch_fused(dx, mc, ms, ma, ml, mo, fa, fp, st);
-    if (i >= 0 && cudaEventRecord(static_cast<cudaEvent_t>(ev[2 * i + 1]), st) != cudaSuccess) cudaGetLastError();
+    if (e == cudaSuccess && fp.splits > 1) e = launch_splitk_reduce(fa.partial, fp.splits, fa.M, fa.wdim, fa.out, num_sms, st);
+    timer_close(i, st);
     return e;
 }
 
@@ -168,6 +178,7 @@ static QuantWs quant_ws(int64_t rows, int64_t cols) {
 
 struct LayerWs {
     int r8, r64;
+    bool gemv;  // forward with M <= 2: the CUDA-core GEMV instead of the fused kernel
     FusedPlan fp;
     ProjPlan pu, pv, pda, pdb;
     size_t off_scales, off_u, off_v, off_bpad, off_main, total;
@@ -185,10 +196,11 @@ static LayerWs layer_ws(int64_t M, int64_t N, int64_t K, int r, bool bwd, int nu
         w.fp = plan_fused(M, K, (N + 63) / 64, w.r64, num_sms);
     } else {
         w.fp = plan_fused(M, N, K / 64, w.r64, num_sms);
+        w.gemv = M <= 2;
     }
     size_t off = 0;
     w.off_scales = off;  // rebuilt block scales, for the CTA-pair kernel only
-    if (!w.fp.small) off += align256((size_t)KB * N * 4);
+    if (!w.fp.small && !w.gemv) off += align256((size_t)KB * N * 4);
     w.off_u = off;
     off += align256((size_t)M * w.r8 * 2);
     w.off_v = off;
@@ -196,7 +208,7 @@ static LayerWs layer_ws(int64_t M, int64_t N, int64_t K, int r, bool bwd, int nu
     w.off_bpad = off;
     if (bwd && r % 8 != 0) off += align256((size_t)N * w.r8 * 2);
     w.off_main = off;
-    off += align256(w.fp.partial_bytes);
+    off += align256(w.gemv ? (size_t)gemv_slices(K) * M * N * 4 : w.fp.partial_bytes);
     w.total = off;
     return w;
 }
@@ -373,10 +385,16 @@ qlora_status qlora_linear_fwd(const qlora_nf4_tensor *W, const uint16_t *X, int6
     pu.ld_h = w.r8;
     pu.out_h2 = U_save;
     if ((e = launch_proj(false, false, mX_k, mA_k, pu, st)) != cudaSuccess) return from_cuda(e);
+    if (w.gemv) {
+        const int32_t ti = timer_open(st);
+        e = launch_gemv(W->codes, W->scale_codes, W->scale_scales, W->scale_offset, X, (int)M, N, K, mainp, U, w.r8, B,
+                        r, Y, tables(), sms, st);
+        timer_close(ti, st);
+        return from_cuda(e);
+    }
     // Y = X W^T + U B^T
     const FusedArgs fa = fused_args(W, M, w, r, B, r, Y, mainp, N);
-    if ((e = timed_fused(false, mCodes, mScales, mX_act, mU_act, mY, fa, w.fp, st)) != cudaSuccess) return from_cuda(e);
-    if (w.fp.splits > 1 && (e = launch_splitk_reduce(mainp, w.fp.splits, M, N, Y, sms, st)) != cudaSuccess)
+    if ((e = timed_fused(false, mCodes, mScales, mX_act, mU_act, mY, fa, w.fp, sms, st)) != cudaSuccess)
         return from_cuda(e);
     return QLORA_OK;
 }
@@ -440,8 +458,7 @@ qlora_status qlora_linear_bwd(const qlora_nf4_tensor *W, const uint16_t *X, int6
     if ((e = launch_proj(false, true, mG_k, mB_mn, pv, st)) != cudaSuccess) return from_cuda(e);
     // dX = G W^ + V A
     const FusedArgs fa = fused_args(W, M, w, r, A, K, dX, mainp, K);
-    if ((e = timed_fused(true, mCodes, mScales, mG_act, mV_act, mDX, fa, w.fp, st)) != cudaSuccess) return from_cuda(e);
-    if (w.fp.splits > 1 && (e = launch_splitk_reduce(mainp, w.fp.splits, M, K, dX, sms, st)) != cudaSuccess)
+    if ((e = timed_fused(true, mCodes, mScales, mG_act, mV_act, mDX, fa, w.fp, sms, st)) != cudaSuccess)
         return from_cuda(e);
     // dA = V^T X  (D[k, j] = sum_m X[m, k] V[m, j], stored transposed)
     ProjArgs pa = proj_args(w.pda, K, w, r, 1, 1.0f);

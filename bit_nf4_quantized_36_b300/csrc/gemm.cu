@@ -1,13 +1,14 @@
 // gemm.cu -- tensor-core kernels of the QLoRA linear layer (sm_103a, tcgen05 + TMEM + TMA).
 //
-// 1. nf4_lora_gemm_kernel<dx>: the fused NF4-dequant GEMM.  The weight side is the MMA's
-//    128-row A operand ("swap-AB": weights are the M side, tokens the N side), so that each
-//    expanded weight is reused by up to 256 tokens.  TMA stages the packed nibbles and the
-//    activation tile; eight decode warps expand nibbles to bf16 through a per-block 16-entry
-//    register table (byte-permute lookups) straight into the 128-byte-swizzled smem layout the
-//    MMA reads; one thread issues tcgen05.mma into a double-buffered TMEM accumulator; four
-//    epilogue warps drain TMEM while the next tile is computed.  The rank-r LoRA term is
-//    appended as extra K-steps (weights side: zero-padded B or A rows; token side: U or V).
+// 1. nf4_lora_gemm_kernel<dx, stages, mt>: the fused NF4-dequant GEMM for M > 32.  The weight
+//    side is the MMA's A operand ("swap-AB": weights are the M side, tokens the N side), so that
+//    each expanded weight is reused by up to mt x 256 tokens.  A cluster of two CTAs shares every
+//    MMA (tcgen05.mma.cta_group::2, M = 256 weight rows): each CTA TMA-stages the packed nibbles
+//    of its 128 rows and half of each token tile; eight decode warps expand the nibbles to bf16
+//    through a per-block 16-entry register table (byte-permute lookups) straight into the
+//    128-byte-swizzled smem layout the MMA reads; one thread of the even CTA issues the MMAs;
+//    four epilogue warps per CTA drain TMEM.  The rank-r LoRA term is appended as extra K-steps
+//    (weights side: zero-padded B or A rows; token side: U or V).
 //      forward : A = W^ tile (K-major: rows = out features, 64 k per row)
 //      backward: A = W^^T tile (MN-major: each 128-byte row holds 64 consecutive k of one
 //                weight row n, the contraction index), so the same decode routine serves both.
@@ -16,8 +17,9 @@
 //    rebuilt on every pass ("QLoRA" glossary, ultralytics: dequantized to bfloat16 right before
 //    the matmul, in the forward and in backprop).
 // 2. lora_proj_kernel<p_mn, q_mn>: skinny products with N = r64 <= 256 (U = X A^T, V = G B,
-//    dA = V^T X, dB = G^T U), split over the contraction with fp32 partials and a fixed-order
-//    finalize (deterministic).
+//    dA = V^T X, dB = G^T U), split over the contraction across the CTAs of a cluster, whose
+//    fp32 partial tiles are summed in split order through distributed shared memory.
+// The small-M variant of 1. is in gemm_small.cu; M <= 2 forwards use the GEMV in gemv.cu.
 #include <algorithm>
 #include <mutex>
 
@@ -543,318 +545,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFusedThreads, 1)
 }
 
 // ---------------------------------------------------------------------------------------
-// Small token counts (M <= 32, e.g. decoding).  Each weight is used by at most 32 tokens, so the
-// call is bound by streaming the packed codes and by the decode arithmetic, not by tensor FLOPs.
-// Differences from the pair kernel above:
-//   - single-CTA MMAs (M = 128, N = BN in {16, 32}): a pair MMA costs about twice the issue
-//     time per weight at this N;
-//   - two issuer warps take alternate k-steps into separate accumulators (the per-instruction
-//     issue cost, not the tensor pipe, bounds one issuer at small N); the epilogue adds them;
-//   - three decode groups (12 warps) over a 9-stage ring: the decode ALU work per byte of codes
-//     is the binding cost, so more warps hide the lookup latency;
-//   - codes, tokens and (for LoRA k-steps) U share one full barrier per stage;
-//   - the decode threads rebuild each block scale s'_b = fmaf(q_b, fl(c2_g / 127), mu) from the
-//     int8 code and the group constant themselves (bit-identical to nf4_dequantize), so the call
-//     reads 1 byte of scale per 64 weights instead of a rebuilt fp32 copy written beforehand.
-// ---------------------------------------------------------------------------------------
-static constexpr int kSmallIssuers = 2;
-static constexpr int kSmallGroups = 3;
-static constexpr int kSmallStages = 9;            // a multiple of kSmallGroups
-static constexpr int kSmallEpiWarp0 = 1 + kSmallIssuers;   // warps 3..6
-static constexpr int kSmallDecodeWarp0 = kSmallEpiWarp0 + 4;  // warps 7..18
-static constexpr int kSmallThreads = (kSmallDecodeWarp0 + 4 * kSmallGroups) * 32;  // 608
-static constexpr uint32_t kSmallTmemCols = 128;   // 2 buffers x 2 issuers x BN (<= 32)
-
-// s'_b of block b = row * KB + kb; the group constant fl(c2_g / 127) is cached across calls while
-// the group does not change.
-__device__ __forceinline__ float block_scale(const FusedArgs &p, float mu, int64_t row, int64_t kb, int64_t &g_cached,
-                                             float &k_cached) {
-    const int64_t b = row * p.KB + kb;
-    const int64_t g = b >> 8;
-    if (g != g_cached) {
-        g_cached = g;
-        k_cached = __fdiv_rn(__ldg(p.scale_c2 + g), 127.0f);
-    }
-    return __fmaf_rn((float)__ldg(p.scale_q + b), k_cached, mu);
-}
-
-template <bool kDX, int kBN>
-__global__ void __launch_bounds__(kSmallThreads, 1)
-    nf4_lora_gemm_small_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant__ CUtensorMap map_act,
-                               const __grid_constant__ CUtensorMap map_lora, const FusedArgs p) {
-    extern __shared__ uint8_t smem_raw[];
-    const uint32_t raw_addr = smem_u32(smem_raw);
-    uint8_t *smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
-    constexpr uint32_t b_bytes = (uint32_t)kBN * 128u;
-    uint8_t *sA = smem;
-    uint8_t *sB = sA + kSmallStages * kATileBytes;
-    uint8_t *sC = sB + kSmallStages * b_bytes;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sC + kSmallStages * kCodesTileBytes);
-    uint64_t *full = bars;                        // codes + tokens landed (TMA transaction count)
-    uint64_t *full_a = bars + kSmallStages;       // decoded weight tile written (4 warps)
-    uint64_t *empty = bars + 2 * kSmallStages;    // MMAs reading the stage finished
-    uint64_t *acc_full = bars + 3 * kSmallStages; // [2], one commit per issuer
-    uint64_t *acc_empty = acc_full + 2;           // [2], four epilogue warps
-    uint64_t *drain = acc_empty + 2;              // [kSmallIssuers]
-    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(drain + kSmallIssuers);
-    volatile uint32_t *s_abort = s_tmem + 1;
-
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < kSmallStages; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&full_a[s], 4);
-            mbar_init(&empty[s], 1);
-        }
-        for (int a = 0; a < 2; ++a) {
-            mbar_init(&acc_full[a], kSmallIssuers);
-            mbar_init(&acc_empty[a], 4);
-        }
-        for (int i = 0; i < kSmallIssuers; ++i) mbar_init(&drain[i], 1);
-        *s_abort = 0u;
-        fence_mbar_init();
-    }
-    if (warp == 1) {
-        tmem_alloc(s_tmem, kSmallTmemCols);
-        tmem_relinquish();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem_base = *s_tmem;
-    const int total_units = p.w_tiles * p.m_tiles * p.splits;
-
-    if (warp == 0) {
-        // ------------------------------ TMA producer ------------------------------------
-        if (lane == 0) {
-            tma_prefetch_desc(&map_codes);
-            tma_prefetch_desc(&map_act);
-            tma_prefetch_desc(&map_lora);
-            int s = 0;
-            uint32_t ph = 0;
-            uint32_t issued_parity[kSmallStages];
-            bool issued[kSmallStages];
-            for (int i = 0; i < kSmallStages; ++i) issued[i] = false, issued_parity[i] = 0;
-            bool ok = true;
-            for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
-                const UnitInfo ui = unit_info(p, u);
-                for (int j = 0; j < ui.nk; ++j) {
-                    if (!mbar_wait(&empty[s], ph ^ 1u, s_abort)) { ok = false; break; }
-                    const bool lora = (ui.kt0 + j) >= ui.kt1;
-                    if (!lora) {
-                        const int kt = ui.kt0 + j;
-                        mbar_arrive_expect_tx(&full[s], kCodesTileBytes + b_bytes);
-                        if (kDX) tma_load_2d(sC + s * kCodesTileBytes, &map_codes, &full[s], ui.w_tile * 64, kt * 64);
-                        else tma_load_2d(sC + s * kCodesTileBytes, &map_codes, &full[s], kt * 32, ui.w_tile * 128);
-                        tma_load_2d(sB + s * b_bytes, &map_act, &full[s], kt * 64, ui.m_tile * kBN);
-                    } else {
-                        const int lt = j - (ui.kt1 - ui.kt0);
-                        mbar_arrive_expect_tx(&full[s], b_bytes);
-                        tma_load_2d(sB + s * b_bytes, &map_lora, &full[s], lt * 64, ui.m_tile * kBN);
-                    }
-                    issued[s] = true;
-                    issued_parity[s] = ph;
-                    if (++s == kSmallStages) { s = 0; ph ^= 1u; }
-                }
-            }
-            if (!ok) {
-                for (int i = 0; i < kSmallStages; ++i) {
-                    if (!issued[i]) continue;
-                    const uint64_t t0 = globaltimer_ns();
-                    while (!mbar_try_wait(&full[i], issued_parity[i]) && globaltimer_ns() - t0 < 20000000ull) {}
-                }
-            }
-        }
-        __syncwarp();
-    } else if (warp <= kSmallIssuers) {
-        // ------------------------------ MMA issuers --------------------------------------
-        // Issuer i takes the k-steps g with g % kSmallIssuers == i of the CTA's step sequence
-        // and accumulates into its own TMEM columns.
-        const int me = warp - 1;
-        if (lane == 0) {
-            const uint32_t idesc = make_idesc_bf16((uint32_t)kBN, kDX, false);
-            const uint32_t a_base = smem_u32(sA), b_base = smem_u32(sB);
-            int s = 0, gstep = 0;
-            uint32_t ph = 0;
-            int lt = 0;
-            bool ok = true, any = false;
-            for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x, ++lt) {
-                const UnitInfo ui = unit_info(p, u);
-                const int a = lt & 1;
-                const uint32_t d_tmem = tmem_base + (uint32_t)((a * kSmallIssuers + me) * kBN);
-                bool first = true;
-                for (int j = 0; j < ui.nk; ++j, ++gstep) {
-                    if (gstep % kSmallIssuers == me) {
-                        if (first && !mbar_wait(&acc_empty[a], ((lt >> 1) & 1) ^ 1u, s_abort)) { ok = false; break; }
-                        if (!mbar_wait(&full_a[s], ph, s_abort)) { ok = false; break; }
-                        tc_fence_after();
-                        const uint32_t a_addr = a_base + (uint32_t)s * kATileBytes;
-                        const uint32_t b_addr = b_base + (uint32_t)s * b_bytes;
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            const uint64_t adesc = kDX ? make_sw128_desc(a_addr + kk * 2048u, 8192u, 1024u)
-                                                       : make_sw128_desc(a_addr + kk * 32u, 16u, 1024u);
-                            const uint64_t bdesc = make_sw128_desc(b_addr + kk * 32u, 16u, 1024u);
-                            umma_bf16(d_tmem, adesc, bdesc, idesc, (!first || kk > 0) ? 1u : 0u);
-                        }
-                        first = false;
-                        any = true;
-                        umma_commit(&empty[s]);
-                    }
-                    if (++s == kSmallStages) { s = 0; ph ^= 1u; }
-                }
-                if (!ok) break;
-                umma_commit(&acc_full[a]);  // units have at least kSmallIssuers k-steps
-            }
-            if (!ok && any) {
-                umma_commit(&drain[me]);
-                const uint64_t t0 = globaltimer_ns();
-                while (!mbar_try_wait(&drain[me], 0) && globaltimer_ns() - t0 < 20000000ull) {}
-            }
-        }
-        __syncwarp();
-    } else if (warp < kSmallDecodeWarp0) {
-        // ------------------------------ epilogue -----------------------------------------
-        const int quarter = warp & 3;
-        int lt = 0;
-        for (int u = blockIdx.x; u < total_units; u += gridDim.x, ++lt) {
-            const UnitInfo ui = unit_info(p, u);
-            const int a = lt & 1;
-            if (!warp_wait(&acc_full[a], (lt >> 1) & 1, s_abort)) break;
-            tc_fence_after();
-            const int64_t f = (int64_t)ui.w_tile * 128 + quarter * 32 + lane;
-            const int m0 = ui.m_tile * kBN;
-            const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(a * kSmallIssuers * kBN);
-            float acc[kBN];
-#pragma unroll
-            for (int c = 0; c < kBN / 16; ++c) {
-                uint32_t r0[16], r1[16];
-                tmem_ld_32x32b_x16(taddr + (uint32_t)(c * 16), r0);
-                tmem_ld_32x32b_x16(taddr + (uint32_t)(kBN + c * 16), r1);
-                tmem_ld_wait();
-#pragma unroll
-                for (int jj = 0; jj < 16; ++jj) acc[c * 16 + jj] = __fadd_rn(__uint_as_float(r0[jj]), __uint_as_float(r1[jj]));
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&acc_empty[a]);
-            if (f < p.wdim) {
-#pragma unroll
-                for (int jj = 0; jj < kBN; ++jj) {
-                    const int m = m0 + jj;
-                    if (m >= p.M) break;
-                    if (p.splits == 1) {
-                        __nv_bfloat16 h = __float2bfloat16_rn(acc[jj]);
-                        p.out[(int64_t)m * p.wdim + f] = *reinterpret_cast<uint16_t *>(&h);
-                    } else {
-                        p.partial[((int64_t)ui.split * p.M + m) * p.wdim + f] = acc[jj];
-                    }
-                }
-            }
-        }
-    } else {
-        // ------------------------------ decode warps -------------------------------------
-        // Group g (4 warps, one 128-byte A row per thread) takes the stages s with
-        // s % kSmallGroups == g; the ring length is a multiple of kSmallGroups.
-        const int t = (threadIdx.x - kSmallDecodeWarp0 * 32) & 127;
-        const int group = (threadIdx.x - kSmallDecodeWarp0 * 32) >> 7;
-        const uint32_t a_base = smem_u32(sA);
-        const bool lora_vec = (p.lora_ld % 8) == 0;
-        uint32_t row_off, code_off;
-        int nl = 0, kbl = 0;
-        if (!kDX) {
-            row_off = (uint32_t)t * 128u;
-            code_off = (uint32_t)t * 32u;
-        } else {
-            nl = t >> 1;
-            kbl = t & 1;
-            row_off = (uint32_t)kbl * 8192u + (uint32_t)nl * 128u;
-            code_off = (uint32_t)nl * 64u + (uint32_t)kbl * 32u;
-        }
-        const uint32_t r7 = (row_off >> 7) & 7u;
-        int64_t g_cached = -1;
-        float k_cached = 0.0f;
-        const float mu = __ldg(p.scale_mu);
-        int s = 0;
-        uint32_t ph = 0;
-        bool ok = true;
-        for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
-            const UnitInfo ui = unit_info(p, u);
-            const int64_t n_fwd = (int64_t)ui.w_tile * 128 + t;
-            const int kblock = ui.w_tile * 2 + kbl;
-            for (int j = 0; j < ui.nk; ++j) {
-                if (s % kSmallGroups == group) {
-                    const bool lora = (ui.kt0 + j) >= ui.kt1;
-                    const int kt = lora ? j - (ui.kt1 - ui.kt0) : ui.kt0 + j;
-                    bool valid;
-                    int64_t srow = 0, skb = 0;
-                    uint4 lv[8];
-                    if (!kDX) {
-                        valid = n_fwd < p.N;
-                        srow = n_fwd;
-                        skb = kt;
-                        if (lora && valid) {
-                            const uint16_t *row = p.lora_src + n_fwd * p.lora_ld;
-                            load_row32(row, (int64_t)kt * 64, p.r, lora_vec, *reinterpret_cast<uint4(*)[4]>(&lv[0]));
-                            load_row32(row, (int64_t)kt * 64 + 32, p.r, lora_vec, *reinterpret_cast<uint4(*)[4]>(&lv[4]));
-                        }
-                    } else {
-                        const int64_t n = (int64_t)kt * 64 + nl;
-                        valid = kblock < p.KB && n < (lora ? (int64_t)p.r : p.N);
-                        srow = n;
-                        skb = kblock;
-                        if (lora && valid) {
-                            const uint4 *src = reinterpret_cast<const uint4 *>(p.lora_src + n * p.lora_ld + (int64_t)kblock * 64);
-#pragma unroll
-                            for (int i = 0; i < 8; ++i) lv[i] = __ldg(src + i);
-                        }
-                    }
-                    // the block scale does not depend on the stage: fetch it before waiting
-                    const float sc = (valid && !lora) ? block_scale(p, mu, srow, skb, g_cached, k_cached) : 0.0f;
-                    if (!warp_wait(&empty[s], ph ^ 1u, s_abort)) { ok = false; break; }
-                    if (!warp_wait(&full[s], ph, s_abort)) { ok = false; break; }
-                    const uint32_t row_addr = a_base + (uint32_t)s * kATileBytes + row_off;
-                    if (!valid) {
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) st_shared_v4(row_addr + (((uint32_t)i ^ r7) << 4), make_uint4(0, 0, 0, 0));
-                    } else if (!lora) {
-                        const uint8_t *cst = sC + s * kCodesTileBytes;
-                        const uint4 c0 = *reinterpret_cast<const uint4 *>(cst + code_off);
-                        const uint4 c1 = *reinterpret_cast<const uint4 *>(cst + code_off + 16);
-                        uint32_t lo[4], hi[4];
-                        build_table(sc, p.tab, lo, hi);
-                        st_shared_v4(row_addr + ((0u ^ r7) << 4), decode8(c0.x, lo, hi));
-                        st_shared_v4(row_addr + ((1u ^ r7) << 4), decode8(c0.y, lo, hi));
-                        st_shared_v4(row_addr + ((2u ^ r7) << 4), decode8(c0.z, lo, hi));
-                        st_shared_v4(row_addr + ((3u ^ r7) << 4), decode8(c0.w, lo, hi));
-                        st_shared_v4(row_addr + ((4u ^ r7) << 4), decode8(c1.x, lo, hi));
-                        st_shared_v4(row_addr + ((5u ^ r7) << 4), decode8(c1.y, lo, hi));
-                        st_shared_v4(row_addr + ((6u ^ r7) << 4), decode8(c1.z, lo, hi));
-                        st_shared_v4(row_addr + ((7u ^ r7) << 4), decode8(c1.w, lo, hi));
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) st_shared_v4(row_addr + (((uint32_t)i ^ r7) << 4), lv[i]);
-                    }
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&full_a[s]);
-                }
-                if (++s == kSmallStages) { s = 0; ph ^= 1u; }
-            }
-        }
-    }
-
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 1) {
-        tc_fence_after();
-        tmem_dealloc(tmem_base, kSmallTmemCols);
-    }
-}
-
-// ---------------------------------------------------------------------------------------
 // Skinny LoRA products D[i, j] = sum_c P[i, c] Q[j, c] (N = r64 <= 256), split over the
 // contraction.  The `splits` CTAs of one 128-row tile form a thread-block cluster: each parks
 // its fp32 partial tile in its own shared memory, and after a cluster barrier every CTA sums a
@@ -1104,38 +794,6 @@ static size_t fused_smem_bytes(int BN, int mt, int stages) {
 }
 static size_t proj_smem_bytes(int r64) { return 1024 + (size_t)kProjStages * (kATileBytes + (size_t)r64 * 128) + 128; }
 
-static size_t small_smem_bytes(int BN) {
-    return 1024 + (size_t)kSmallStages * (kATileBytes + (size_t)BN * 128 + kCodesTileBytes) + 512;
-}
-
-// Small-M plan: 128-row tiles, all tokens in one tile, and the contraction split so that the
-// units fill whole waves.  Cost per SM, in bytes streamed: waves x codes per unit, plus the fp32
-// partials written and re-read by the split reduction (spread over all SMs) and a fixed charge
-// for the extra launch.
-static void plan_small(FusedPlan &pl, int64_t M, int64_t wdim, int64_t kt_main, int num_sms) {
-    pl.small = true;
-    pl.mt = 1;
-    pl.BN = M <= 16 ? 16 : 32;
-    pl.act_rows = pl.BN;
-    pl.stages = kSmallStages;
-    pl.m_tiles = 1;
-    pl.w_tiles = (int)((wdim + 127) / 128);
-    int best = 1;
-    double best_cost = 0.0;
-    // every split keeps at least kSmallIssuers main k-steps so that each issuer has work
-    const int64_t smax = std::max<int64_t>(1, std::min<int64_t>(32, kt_main / kSmallIssuers));
-    for (int64_t sp = 1; sp <= smax; ++sp) {
-        const int64_t units = (int64_t)pl.w_tiles * sp;
-        const int64_t waves = (units + num_sms - 1) / num_sms;
-        double cost = (double)waves * (double)((kt_main + sp - 1) / sp) * (double)kCodesTileBytes;
-        if (sp > 1) cost += 8.0 * (double)sp * (double)M * (double)wdim / (double)num_sms + 65536.0;
-        if (sp == 1 || cost < best_cost) { best_cost = cost; best = (int)sp; }
-    }
-    pl.splits = best;
-    pl.grid = (int)std::min<int64_t>((int64_t)pl.w_tiles * pl.splits, num_sms);
-    pl.partial_bytes = pl.splits > 1 ? (size_t)pl.splits * (size_t)M * (size_t)wdim * 4 : 0;
-}
-
 FusedPlan plan_fused(int64_t M, int64_t wdim, int64_t kt_main, int r64, int num_sms) {
     FusedPlan pl{};
     pl.kt_main = (int)kt_main;
@@ -1228,29 +886,13 @@ static cudaError_t launch_fused_t(const CUtensorMap &mc, const CUtensorMap &ms, 
     return cudaSuccess;
 }
 
-template <bool kDX, int kBN>
-static cudaError_t launch_small_t(const CUtensorMap &mc, const CUtensorMap &ma, const CUtensorMap &ml,
-                                  const FusedArgs &args, const FusedPlan &plan, cudaStream_t st) {
-    const size_t smem = small_smem_bytes(kBN);
-    cudaError_t e = cudaFuncSetAttribute(nf4_lora_gemm_small_kernel<kDX, kBN>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    nf4_lora_gemm_small_kernel<kDX, kBN><<<plan.grid, kSmallThreads, smem, st>>>(mc, ma, ml, args);
-    return cudaSuccess;
-}
-
 cudaError_t launch_fused(bool dx, const CUtensorMap &map_codes, const CUtensorMap &map_scales,
                          const CUtensorMap &map_act, const CUtensorMap &map_lora, const CUtensorMap &map_out,
                          const FusedArgs &args, const FusedPlan &plan, cudaStream_t st) {
     cudaError_t e;
     const int S = plan.stages;
     if (plan.small) {
-        if (dx)
-            e = plan.BN == 16 ? launch_small_t<true, 16>(map_codes, map_act, map_lora, args, plan, st)
-                              : launch_small_t<true, 32>(map_codes, map_act, map_lora, args, plan, st);
-        else
-            e = plan.BN == 16 ? launch_small_t<false, 16>(map_codes, map_act, map_lora, args, plan, st)
-                              : launch_small_t<false, 32>(map_codes, map_act, map_lora, args, plan, st);
+        e = launch_small(dx, map_codes, map_act, map_lora, args, plan, st);
     } else if (plan.mt == 2) {
         e = dx ? launch_fused_t<true, 4, 2>(map_codes, map_scales, map_act, map_lora, map_out, args, plan, st)
                : launch_fused_t<false, 4, 2>(map_codes, map_scales, map_act, map_lora, map_out, args, plan, st);

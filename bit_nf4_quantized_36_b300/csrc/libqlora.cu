@@ -2,5 +2,7 @@
 // kernels that set it must live in one device module without relocatable device code).
 #include "quant.cu"
 #include "gemm.cu"
+#include "gemm_small.cu"
+#include "gemv.cu"
 #include "api.cu"
 #include "noalloc.cu"

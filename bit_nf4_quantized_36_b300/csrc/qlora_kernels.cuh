@@ -58,6 +58,10 @@ struct FusedPlan {
     size_t partial_bytes;
 };
 FusedPlan plan_fused(int64_t M, int64_t wdim, int64_t kt_main, int r64, int num_sms);
+// the small-M kernel (gemm_small.cu): its plan (called by plan_fused for M <= 32) and launch
+void plan_small(FusedPlan &pl, int64_t M, int64_t wdim, int64_t kt_main, int num_sms);
+cudaError_t launch_small(bool dx, const CUtensorMap &map_codes, const CUtensorMap &map_act, const CUtensorMap &map_lora,
+                         const FusedArgs &args, const FusedPlan &plan, cudaStream_t st);
 
 // map_codes : codes as a 2-D byte tensor {K/2, N}; box {32, 128} (forward) or {64, 64} (backward)
 // map_scales: rebuilt block scales, fp32 {N, KB} (transposed, [KB][N]); box {128, 1} or {64, 2}
@@ -99,6 +103,14 @@ struct ProjPlan {
 ProjPlan plan_proj(int64_t Mp, int64_t Kc, int r64, int num_sms);
 cudaError_t launch_proj(bool p_mn, bool q_mn, const CUtensorMap &map_p, const CUtensorMap &map_q, const ProjArgs &args,
                         cudaStream_t st);
+
+// ---- forward for M <= 2 on the CUDA cores (gemv.cu) --------------------------------------
+// Y[m, n] = bf16(sum_k X[m, k] W^[n, k] + sum_j U[m, j] B[n, j]) for m < M (1 or 2), with W^ decoded
+// from the NF4 tensor's codes and int8 scale codes; partial: [gemv_slices(K), M, N] fp32.
+int gemv_slices(int64_t K);
+cudaError_t launch_gemv(const uint8_t *codes, const int8_t *scale_q, const float *scale_c2, const float *scale_mu,
+                        const uint16_t *X, int M, int64_t N, int64_t K, float *partial, const uint16_t *U, int ldu,
+                        const uint16_t *B, int r, uint16_t *Y, const NF4Tables &tab, int num_sms, cudaStream_t st);
 
 // dst[rows_dst, cols_dst] = src[rows_src, cols_src] where both indices are in range, else 0
 cudaError_t launch_pad_2d(const uint16_t *src, int64_t rows_src, int64_t cols_src, uint16_t *dst, int64_t rows_dst,

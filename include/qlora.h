@@ -151,14 +151,17 @@ void qlora_nf4_levels(float out[16]);
 
 /* Benchmark instrumentation (not needed for normal use).  `events` holds 2*capacity
  * cudaEvent_t handles created by the caller; from now on the library records events[2i] just
- * before and events[2i+1] just after the i-th launch of its fused NF4-dequant GEMM kernel
- * (forward or backward dX), on the launch stream, until `capacity` launches are recorded.
+ * before and events[2i+1] just after the i-th weight-streaming step of a layer call: the
+ * launch of the fused NF4-dequant GEMM kernel (forward or backward dX, with the reduction of its
+ * partials when the contraction is split), or, for a forward of
+ * one or two tokens, the CUDA-core GEMV and its finishing kernel; on the launch stream, until
+ * `capacity` steps are recorded.
  * events == NULL switches the recording off.  Process-wide; do not change it while calls are
  * in flight on other host threads.  Returns QLORA_ERR_INVALID_ARG for capacity < 0 or a NULL
  * handle among the 2*capacity events. */
 qlora_status qlora_set_kernel_timer(void **events, int32_t capacity);
 
-/* Number of fused-kernel launches recorded since the last qlora_set_kernel_timer call. */
+/* Number of weight-streaming steps recorded since the last qlora_set_kernel_timer call. */
 int32_t qlora_kernel_timer_count(void);
 
 #ifdef __cplusplus

@@ -89,6 +89,8 @@ def test_tiny_workload(orc):
     (300, 128, 128, 72),   # r64 = 128 (two LoRA k-steps)
     (40, 256, 512, 256),   # maximum rank
     (257, 520, 640, 16),   # token tile 256 + 1, weight tiles 4 + ragged
+    (2, 264, 4160, 16),    # two tokens: contraction of 2 full 2048-slices and a 64-wide tail
+    (1, 136, 2112, 3),     # one token, odd rank, ragged rows
 ])
 def test_shapes(orc, M, N, K, r):
     inp = synth.layer_inputs(100 + r, M, N, K, r, 2.0 * r, b_std=0.3)
