@@ -74,6 +74,9 @@ def _declare(L):
     L.orc_layer_adapter_grads_cols.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _I64, _D, _P, _I64, _P, _P]
     L.orc_nf4_storage_bytes.argtypes = [_I64, _I64]
     L.orc_nf4_storage_bytes.restype = _I64
+    L.orc_bf16_round_d.argtypes = [_D]
+    L.orc_bf16_round_d.restype = ctypes.c_uint16
+    L.orc_merge.argtypes = [_P, _P, _P, _I64, _I64, _I64, _D, _P]
 
 
 def _c(a: np.ndarray, dtype) -> np.ndarray:
@@ -262,3 +265,19 @@ def layer_adapter_grads_cols(X, A, B, G, alpha: float, jsel):
 
 def nf4_storage_bytes(rows: int, cols: int) -> int:
     return int(lib().orc_nf4_storage_bytes(rows, cols))
+
+
+def bf16_round_d(x: float) -> int:
+    """bf16 bit pattern of the fp64 value x, rounded once (nearest, ties to even)."""
+    return int(lib().orc_bf16_round_d(float(x)))
+
+
+def merge(What, A, B, alpha: float) -> np.ndarray:
+    """bf16 bit patterns of W_m = bf16(W^ + (alpha/r) B A), shape [N, K], from bf16 bit patterns
+    What [N, K], A [r, K], B [N, r]."""
+    What, A, B = (_c(t, np.uint16) for t in (What, A, B))
+    N, K = What.shape
+    r = A.shape[0]
+    out = np.zeros((N, K), dtype=np.uint16)
+    lib().orc_merge(_ptr(What), _ptr(A), _ptr(B), N, K, r, float(alpha), _ptr(out))
+    return out

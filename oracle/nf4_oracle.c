@@ -285,6 +285,35 @@ uint16_t orc_bf16_round(float x)
     return (uint16_t)(pick >> 16);
 }
 
+/* The same rounding applied once to an fp64 value (no intermediate fp32 rounding): the two bf16
+ * values around x are found from its binary exponent, and the nearer one is taken, ties to the
+ * even significand.  Values below the smallest normal use the subnormal spacing 2^-133; past the
+ * largest finite bf16 the result is infinity (IEEE round-to-nearest overflow rule). */
+uint16_t orc_bf16_round_d(double x)
+{
+    if (isnan(x)) return 0x7FC0;
+    const uint16_t sign = (x < 0) ? 0x8000 : 0;
+    double a = fabs(x);
+    if (a == 0.0) return sign;
+    int e;
+    frexp(a, &e);                              /* a = m 2^e, m in [0.5, 1) */
+    int q = e - 8;                             /* spacing of 8-bit significands at this binade */
+    if (q < -133) q = -133;                    /* bf16 subnormal spacing */
+    double step = ldexp(1.0, q);
+    double lo = floor(a / step) * step;        /* exact: a / step only shifts the exponent */
+    double hi = lo + step;
+    double dlo = a - lo, dhi = hi - a;
+    double pick;
+    if (dlo < dhi) pick = lo;
+    else if (dhi < dlo) pick = hi;
+    else pick = (fmod(lo / step, 2.0) == 0.0) ? lo : hi;  /* tie: even significand */
+    if (pick >= ldexp(1.0, 128)) return (uint16_t)(sign | 0x7F80);
+    float f = (float)pick;                     /* exact: pick has at most 8 significant bits */
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    return (uint16_t)(sign | ((u >> 16) & 0x7FFF));
+}
+
 double orc_bf16_to_double(uint16_t h)
 {
     uint32_t u = (uint32_t)h << 16;
@@ -490,4 +519,25 @@ void orc_layer_adapter_grads_cols(const uint16_t *X, const uint16_t *A, const ui
     }
     free(u);
     free(v);
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* Adapter merge ([QLoRA-ultralytics], "Compromissos" and "QLoRA e metodos relacionados":  */
+/* to merge the adapters the base weight is first dequantized to 16 bits, and the merged   */
+/* model keeps 16-bit weights):                                                            */
+/*   W_m[n, k] = bf16(W^[n, k] + s sum_j B[n, j] A[j, k]),  s = alpha / r,                 */
+/* with W^ the bf16 dequantized weight, the sum exact in fp64 from the bf16 adapters, and  */
+/* one rounding to bf16 at the end (READING: the pages give no rounding order).            */
+/* ------------------------------------------------------------------------------------ */
+void orc_merge(const uint16_t *What, const uint16_t *A, const uint16_t *B, int64_t N, int64_t K, int64_t r,
+               double alpha, uint16_t *out)
+{
+    double s = alpha / (double)r;
+    for (int64_t n = 0; n < N; ++n) {
+        for (int64_t k = 0; k < K; ++k) {
+            double acc = 0.0;
+            for (int64_t j = 0; j < r; ++j) acc += orc_bf16_to_double(B[n * r + j]) * orc_bf16_to_double(A[j * K + k]);
+            out[n * K + k] = orc_bf16_round_d(orc_bf16_to_double(What[n * K + k]) + s * acc);
+        }
+    }
 }

@@ -399,3 +399,87 @@ def test_sampled_adapter_grads_match_full(orc):
     dAs, dBt = orc.layer_adapter_grads_cols(X, A, B, G, 3.0, js)
     np.testing.assert_allclose(dAs, dA[js], rtol=1e-13)
     np.testing.assert_allclose(dBt, dB[:, js].T, rtol=1e-13)
+
+
+# ---------------------------------------------------------------------------------------
+# Adapter merge: "QLoRA" (ultralytics), "Compromissos": to merge the adapters the base weight is
+# first dequantized to 16 bits; W_m = bf16(W^ + (alpha/r) B A), rounded once.
+# ---------------------------------------------------------------------------------------
+
+def _bf16_of_fraction(x):
+    """Round an exact rational to bf16 (nearest, ties to even), independently of the oracle:
+    exact rational arithmetic on the two 8-bit-significand neighbours."""
+    from fractions import Fraction
+    x = Fraction(x)
+    if x == 0:
+        return 0
+    sign = 0x8000 if x < 0 else 0
+    a = abs(x)
+    e = 0
+    while a >= 2 ** (e + 1):
+        e += 1
+    while a < Fraction(2) ** e:
+        e -= 1
+    step = Fraction(2) ** (e - 7)          # 8 significant bits in [2^e, 2^(e+1))
+    m = a // step                          # integer in [128, 256)
+    lo, hi = m * step, (m + 1) * step
+    if a - lo < hi - a or (a - lo == hi - a and m % 2 == 0):
+        v = lo
+    else:
+        v = hi
+    bits = np.array([float(v)], dtype=np.float32).view(np.uint32)[0]
+    return sign | int(bits >> 16)
+
+
+def test_bf16_round_d_agrees_with_fp32_rounding(orc):
+    rng = np.random.default_rng(7)
+    xs = np.concatenate([rng.standard_normal(3000).astype(np.float32) * 0.02,
+                         rng.standard_normal(1000).astype(np.float32) * 1e30,
+                         (rng.standard_normal(500) * 1e-39).astype(np.float32),
+                         np.array([1.0, -1.0, 3.0e38, 1.00390625, 1.01171875], dtype=np.float32)])
+    for x in xs:
+        assert orc.bf16_round_d(float(x)) == orc.bf16_round(float(x))
+
+
+def test_bf16_round_d_rounds_once(orc):
+    # 1 + 2^-8 + 2^-30: fp32 would round it to the tie 1 + 2^-8 (then bf16 -> 1.0); one rounding
+    # from the exact value gives 1 + 2^-7.
+    assert orc.bf16_round_d(1.0 + 2.0 ** -8 + 2.0 ** -30) == 0x3F81
+    assert orc.bf16_round_d(1.0 + 2.0 ** -8) == 0x3F80           # tie -> even significand
+    assert orc.bf16_round_d(1.0 + 3 * 2.0 ** -8) == 0x3F82       # tie -> even significand
+
+
+def test_merge_with_zero_adapter_is_the_dequantized_weight(orc):
+    rng = np.random.default_rng(11)
+    W = (rng.standard_normal((8, 128)) * 0.02).astype(np.float32)
+    q = orc.nf4_quantize(W)
+    What = orc.nf4_dequantize(q["packed"], q["qcode"], q["c2"], q["mu"], 8, 128)
+    A = orc.bf16_round_array(rng.standard_normal((4, 128)).astype(np.float32))
+    B = np.zeros((8, 4), dtype=np.uint16)
+    assert np.array_equal(orc.merge(What, A, B, 8.0), What)
+
+
+def test_merge_closed_form(orc):
+    from fractions import Fraction
+    rng = np.random.default_rng(12)
+    W = (rng.standard_normal((6, 64)) * 0.5).astype(np.float32)
+    q = orc.nf4_quantize(W)
+    What = orc.nf4_dequantize(q["packed"], q["qcode"], q["c2"], q["mu"], 6, 64)
+    r = 4
+    A = np.full((r, 64), 0x3F80, dtype=np.uint16)                                  # 1.0
+    B = np.array([[orc.bf16_round(2.0 ** -(j + 4)) for j in range(r)]] * 6, dtype=np.uint16)
+    for alpha, delta in ((4.0, Fraction(15, 128)), (8.0, Fraction(15, 64))):     # s = 1, 2
+        got = orc.merge(What, A, B, alpha)
+        for n in range(6):
+            for k in range(64):
+                w = Fraction(float(orc.bf16_to_f64(What[n, k:k + 1])[0]))
+                assert got[n, k] == _bf16_of_fraction(w + delta)
+
+
+def test_merge_ties_round_to_even(orc):
+    What = np.full((1, 64), 0x3F80, dtype=np.uint16)                     # 1.0
+    A = np.full((1, 64), 0x3F80, dtype=np.uint16)
+    B1 = np.array([[orc.bf16_round(2.0 ** -8)]], dtype=np.uint16)         # s B A = 2^-8: a tie
+    assert np.all(orc.merge(What, A, B1, 1.0) == 0x3F80)
+    B3 = np.array([[orc.bf16_round(3 * 2.0 ** -8)]], dtype=np.uint16)     # 1 + 3 2^-8: a tie
+    assert np.all(orc.merge(What, A, B3, 1.0) == 0x3F82)
