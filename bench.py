@@ -410,7 +410,7 @@ def run_ours(args):
 
 def hbm_extras(q, _lib, L, dev, peaks, flush):
     """Secondary numbers for the HBM-bound kernels on a Llama-70B MLP matrix (28672 x 8192):
-    nf4_dequantize and nf4_quantize GB/s, and the small-M forward (decode) GB/s."""
+    nf4_dequantize, nf4_quantize and adapter-merge GB/s, and the small-M forward (decode) GB/s."""
     import torch
     from bit_nf4_quantized_36_b300 import synth
     rows, cols = 28672, 8192
@@ -443,6 +443,14 @@ def hbm_extras(q, _lib, L, dev, peaks, flush):
     byt = 4 * n + storage
     out["quantize"] = {"matrix": f"{rows}x{cols}", "ms": t, "GB/s": byt / t / 1e6,
                        "frac_hbm": byt / t / 1e6 / peaks["hbm_gbs"], "algorithmic_bytes": byt}
+    # adapter merge W_m = bf16(W^ + (alpha/r) B A): codes and scales read, bf16 written
+    for r_m in (16, 64):
+        Am = (torch.randn((r_m, cols), device=dev) / cols ** 0.5).to(torch.bfloat16)
+        Bm = (torch.randn((rows, r_m), device=dev) * 0.01).to(torch.bfloat16)
+        t = timed(lambda: q.qlora_merge(qw, Am, Bm, 2.0 * r_m, out=What))
+        byt = storage + 2 * n + 2 * r_m * (rows + cols)
+        out[f"merge_r{r_m}"] = {"matrix": f"{rows}x{cols}", "ms": t, "GB/s": byt / t / 1e6,
+                                "frac_hbm": byt / t / 1e6 / peaks["hbm_gbs"], "algorithmic_bytes": byt}
     del W, What
     # decode-like forward: M tokens through the up projection (N = 28672, K = 8192), r = 16
     r = 16

@@ -19,7 +19,8 @@ import torch
 from . import _lib
 
 __all__ = ["NF4Weight", "QLoRAError", "nf4_quantize", "nf4_quantize_noalloc", "nf4_dequantize", "qlora_linear_fwd", "qlora_linear_bwd",
-           "nf4_storage_bytes", "quantize_workspace_bytes", "fwd_workspace_bytes", "bwd_workspace_bytes",
+           "qlora_merge", "nf4_storage_bytes", "quantize_workspace_bytes", "fwd_workspace_bytes", "bwd_workspace_bytes",
+           "merge_workspace_bytes",
            "check_device_error", "launch_count", "nf4_levels", "empty_nf4"]
 
 
@@ -86,6 +87,10 @@ def fwd_workspace_bytes(M: int, N: int, K: int, r: int) -> int:
 
 def bwd_workspace_bytes(M: int, N: int, K: int, r: int) -> int:
     return int(_lib.load().qlora_bwd_workspace_bytes(M, N, K, r))
+
+
+def merge_workspace_bytes(N: int, K: int, r: int) -> int:
+    return int(_lib.load().qlora_merge_workspace_bytes(N, K, r))
 
 
 def launch_count() -> int:
@@ -212,6 +217,26 @@ def qlora_linear_bwd(q: NF4Weight, X: torch.Tensor, A: torch.Tensor, B: torch.Te
                               _stream(stream)),
            "qlora_linear_bwd")
     return dX, dA, dB
+
+
+def qlora_merge(q: NF4Weight, A: torch.Tensor, B: torch.Tensor, alpha: float, out: torch.Tensor | None = None,
+                workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """bf16 W_m [rows, cols] = bf16(W^ + (alpha/r) B A): the adapters merged into the base weight."""
+    r = A.shape[0]
+    _need(A, torch.bfloat16, "A", (r, q.cols))
+    _need(B, torch.bfloat16, "B", (q.rows, r))
+    if out is None:
+        out = torch.empty((q.rows, q.cols), dtype=torch.bfloat16, device=q.codes.device)
+    _need(out, torch.bfloat16, "out", (q.rows, q.cols))
+    L = _lib.load()
+    need = int(L.qlora_merge_workspace_bytes(q.rows, q.cols, r))
+    if need == ctypes.c_size_t(-1).value:
+        raise QLoRAError(2, "qlora_merge")
+    ws = _workspace(need, workspace, out.device)
+    st = q.struct()
+    _check(L.qlora_merge(ctypes.byref(st), _ptr(A), _ptr(B), r, float(alpha), _ptr(out), _ptr(ws),
+                         ws.numel() * ws.element_size(), _stream(stream)), "qlora_merge")
+    return out
 
 
 def check_device_error(stream=None) -> None:

@@ -17,6 +17,7 @@ QLORA_STATUS = {
 EXPORTS = (
     "qlora_nf4_storage_bytes", "qlora_quantize_workspace_bytes", "qlora_fwd_workspace_bytes",
     "qlora_bwd_workspace_bytes", "nf4_quantize", "nf4_dequantize", "qlora_linear_fwd", "qlora_linear_bwd",
+    "qlora_merge_workspace_bytes", "qlora_merge",
     "qlora_check_device_error", "qlora_status_string", "qlora_launch_count", "qlora_nf4_levels",
     "qlora_set_kernel_timer", "qlora_kernel_timer_count", "nf4_quantize_noalloc",
 )
@@ -45,6 +46,8 @@ def load():
         "qlora_quantize_workspace_bytes": (SZ, [I64, I64]),
         "qlora_fwd_workspace_bytes": (SZ, [I64, I64, I64, I32]),
         "qlora_bwd_workspace_bytes": (SZ, [I64, I64, I64, I32]),
+        "qlora_merge_workspace_bytes": (SZ, [I64, I64, I32]),
+        "qlora_merge": (ctypes.c_int, [ST, P, P, I32, ctypes.c_float, P, P, SZ, P]),
         "nf4_quantize": (ctypes.c_int, [P, ST, P, SZ, P]),
         "nf4_dequantize": (ctypes.c_int, [ST, P, P]),
         "nf4_quantize_noalloc": (ctypes.c_int, [P, ST, P]),

@@ -286,6 +286,43 @@ size_t qlora_bwd_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t r) {
     return layer_ws(M, N, K, r, true, num_sms_current()).total;
 }
 
+size_t qlora_merge_workspace_bytes(int64_t N, int64_t K, int32_t r) {
+    if (N < 1 || K < 64 || K % 64 != 0 || r < 1 || r > 256) return (size_t)-1;
+    return (r % 8 == 0) ? 0 : align256((size_t)N * (size_t)(((r + 7) / 8) * 8) * 2);
+}
+
+qlora_status qlora_merge(const qlora_nf4_tensor *W, const uint16_t *A, const uint16_t *B, int32_t r, float alpha,
+                         uint16_t *W_out, void *ws, size_t ws_bytes, void *stream) {
+    qlora_status s = check_tensor(W);
+    if (s != QLORA_OK) return s;
+    if (!A || !B || !W_out) return QLORA_ERR_INVALID_ARG;
+    if (r < 1 || r > 256 || !std::isfinite(alpha)) return QLORA_ERR_INVALID_ARG;
+    const bool r_vec = (r % 8) == 0;
+    if (!aligned16(A) || !aligned16(W_out) || (r_vec && !aligned16(B))) return QLORA_ERR_MISALIGNED;
+    const int64_t N = W->rows, K = W->cols;
+    const size_t need = qlora_merge_workspace_bytes(N, K, r);
+    if (need == (size_t)-1) return QLORA_ERR_UNSUPPORTED_SHAPE;
+    if (need > 0 && (!ws || ws_bytes < need || !aligned16(ws))) return QLORA_ERR_WORKSPACE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int sms = num_sms_current();
+    const int r8 = ((r + 7) / 8) * 8;
+    const uint16_t *Bq = B;
+    cudaError_t e;
+    if (!r_vec) {
+        uint16_t *Bpad = static_cast<uint16_t *>(ws);
+        if ((e = launch_pad_2d(B, N, r, Bpad, N, r8, sms, st)) != cudaSuccess) return from_cuda(e);
+        Bq = Bpad;
+    }
+    CUtensorMap mCodes, mB, mA, mOut;
+    if (!make_map(&mCodes, W->codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)K / 2, (uint64_t)N, (uint64_t)K / 2,
+                  128u, 128u, false) ||
+        !map_bf16(&mB, Bq, r_vec ? r : r8, N, 64, 128) || !map_bf16(&mA, A, K, r, 64, 64) ||
+        !map_bf16(&mOut, W_out, K, N, 64, 128))
+        return QLORA_ERR_CUDA;
+    return from_cuda(launch_merge(mCodes, mB, mA, mOut, W->scale_codes, W->scale_scales, W->scale_offset, N, K, r,
+                                  alpha / (float)r, tables(), sms, st));
+}
+
 qlora_status nf4_quantize(const float *W, const qlora_nf4_tensor *out, void *ws, size_t ws_bytes, void *stream) {
     if (!W) return QLORA_ERR_INVALID_ARG;
     qlora_status s = check_tensor(out);

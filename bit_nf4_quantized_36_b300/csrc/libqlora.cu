@@ -4,5 +4,6 @@
 #include "gemm.cu"
 #include "gemm_small.cu"
 #include "gemv.cu"
+#include "merge.cu"
 #include "api.cu"
 #include "noalloc.cu"

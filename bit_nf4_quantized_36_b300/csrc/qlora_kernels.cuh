@@ -112,6 +112,15 @@ cudaError_t launch_gemv(const uint8_t *codes, const int8_t *scale_q, const float
                         const uint16_t *X, int M, int64_t N, int64_t K, float *partial, const uint16_t *U, int ldu,
                         const uint16_t *B, int r, uint16_t *Y, const NF4Tables &tab, int num_sms, cudaStream_t st);
 
+// ---- adapter merge (merge.cu): W_m = bf16(W^ + s B A) -----------------------------------
+// map_codes: codes {K/2, N} u8, box {128, 128}; map_b: B [N, rb] bf16, box {64, 128}, 128-byte
+// swizzle; map_a: A [r, K] bf16, box {64, 64}, 128-byte swizzle; map_out: W_m [N, K] bf16, box
+// {64, 128}, 128-byte swizzle.
+cudaError_t launch_merge(const CUtensorMap &map_codes, const CUtensorMap &map_b, const CUtensorMap &map_a,
+                         const CUtensorMap &map_out, const int8_t *scale_q, const float *scale_c2,
+                         const float *scale_mu, int64_t N, int64_t K, int r, float s, const NF4Tables &tab,
+                         int num_sms, cudaStream_t st);
+
 // dst[rows_dst, cols_dst] = src[rows_src, cols_src] where both indices are in range, else 0
 cudaError_t launch_pad_2d(const uint16_t *src, int64_t rows_src, int64_t cols_src, uint16_t *dst, int64_t rows_dst,
                           int64_t cols_dst, int num_sms, cudaStream_t st);

@@ -77,6 +77,7 @@ size_t qlora_nf4_storage_bytes(int64_t rows, int64_t cols);
 size_t qlora_quantize_workspace_bytes(int64_t rows, int64_t cols);
 size_t qlora_fwd_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t r);
 size_t qlora_bwd_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t r);
+size_t qlora_merge_workspace_bytes(int64_t N, int64_t K, int32_t r);
 
 /* NF4-quantize an fp32 matrix W [rows, cols] into `out` (its four arrays must be allocated
  * with the sizes above; out->rows/cols give the shape).
@@ -111,6 +112,17 @@ qlora_status nf4_quantize_noalloc(const float *W, const qlora_nf4_tensor *out, v
 /* Dequantize to bf16: W_out[rows, cols] = bf16_rne(NF4[c] * s'_b) ("Cuantiles": w^ = NF4[c] *
  * absmax; glossary: dequantized to bfloat16 before the matmul).  No workspace. */
 qlora_status nf4_dequantize(const qlora_nf4_tensor *q, uint16_t *W_out, void *stream);
+
+/* Merge the adapters into the base weight ("QLoRA" glossary, "Compromissos": to merge the
+ * adapters the base weight is first dequantized to 16 bits; "QLoRA e metodos relacionados": the
+ * fine-tuned model is merged into 16-bit weights):
+ *   W_out [N, K] (bf16) = bf16_rne(fl32(W^ + s (B A))),  s = fl32(alpha / r),
+ * with W^ the nf4_dequantize values, A [r, K] and B [N, r] bf16, B A accumulated in fp32 and
+ * the sum formed by one fp32 fused multiply-add (s * (B A) + W^) before the rounding.
+ * Workspace: qlora_merge_workspace_bytes (B padded to a multiple of 8 columns when r % 8 != 0,
+ * else none).  W_out, A and (r % 8 == 0) B must be 16-byte aligned; 1 <= r <= 256. */
+qlora_status qlora_merge(const qlora_nf4_tensor *W, const uint16_t *A, const uint16_t *B, int32_t r, float alpha,
+                         uint16_t *W_out, void *ws, size_t ws_bytes, void *stream);
 
 /* Forward of the layer ("Parte 4 - LoRA encima", h = W^ x + (alpha/r) B A x):
  *   Y [M, N] (bf16) = X W^T + U B^T,   U = bf16((alpha/r) X A^T)  [M, r]

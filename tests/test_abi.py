@@ -61,6 +61,10 @@ def test_workspace_queries(L):
         scales = (K // 64) * N * 4 if M > 32 else 0
         assert f >= scales + M * r8 * 2
         assert b >= scales + 2 * M * r8 * 2
+    assert L.qlora_merge_workspace_bytes(4096, 4096, 16) == 0     # B used in place
+    assert L.qlora_merge_workspace_bytes(4096, 4096, 5) >= 4096 * 8 * 2
+    assert L.qlora_merge_workspace_bytes(4096, 100, 16) == bad
+    assert L.qlora_merge_workspace_bytes(4096, 4096, 0) == bad
     assert L.qlora_fwd_workspace_bytes(16, 256, 100, 8) == bad    # K % 64
     assert L.qlora_fwd_workspace_bytes(16, 250, 512, 8) == bad    # N % 8
     assert L.qlora_fwd_workspace_bytes(16, 256, 512, 0) == bad    # r
@@ -103,6 +107,17 @@ def test_argument_errors_before_any_launch(L):
                               P(0x7000), ws, 1 << 30, None) == 1
     assert L.qlora_linear_bwd(ctypes.byref(t), X, 16, A, B, 8, 16.0, P(0x8008), None, P(0x5000), P(0x6000),
                               P(0x7000), ws, 1 << 30, None) == 3
+    # merge: rank, alpha, NULLs, alignment, workspace (needed only when r % 8 != 0)
+    Wo = P(0x9000)
+    assert L.qlora_merge(ctypes.byref(t), A, B, 0, 16.0, Wo, None, 0, None) == 1
+    assert L.qlora_merge(ctypes.byref(t), A, B, 257, 16.0, Wo, None, 0, None) == 1
+    assert L.qlora_merge(ctypes.byref(t), A, B, 8, float("inf"), Wo, None, 0, None) == 1
+    assert L.qlora_merge(ctypes.byref(t), None, B, 8, 16.0, Wo, None, 0, None) == 1
+    assert L.qlora_merge(ctypes.byref(t), A, B, 8, 16.0, None, None, 0, None) == 1
+    assert L.qlora_merge(ctypes.byref(t), A, B, 8, 16.0, P(0x9002), None, 0, None) == 3
+    assert L.qlora_merge(ctypes.byref(t), A, P(0x3002), 8, 16.0, Wo, None, 0, None) == 3
+    assert L.qlora_merge(ctypes.byref(t), A, B, 5, 16.0, Wo, None, 0, None) == 4
+    assert L.qlora_merge(ctypes.byref(t), A, B, 5, 16.0, Wo, ws, 64, None) == 4
     assert L.qlora_launch_count() == 0  # nothing above reached a kernel launch
 
 
