@@ -382,6 +382,12 @@ def run_ours(args):
         except Exception as e:  # the headline line must still print
             extras = {"error": repr(e)}
 
+    if rank == 0 and not args.no_extras:
+        try:
+            extras["concat_qkv"] = concat_extras(q, dev, flush)
+        except Exception as e:
+            extras["concat_qkv"] = {"error": repr(e)}
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
@@ -406,6 +412,54 @@ def run_ours(args):
     if dist is not None:
         dist.destroy_process_group()
     return 0
+
+
+def concat_extras(q, dev, flush, reps=10):
+    """Llama-3-8B attention q/k/v (4096, 1024 and 1024 rows, K = 4096, 4096 tokens, r = 16 each):
+    fwd + bwd of the three modules as three separate layer calls against one concatenated call
+    (qlora_linear_fwd_cat / _bwd_cat)."""
+    import torch
+    from bit_nf4_quantized_36_b300 import synth
+    M, K, r, alpha = 4096, 4096, 16, 32.0
+    specs = [("q", 4096), ("k", 1024), ("v", 1024)]
+    X = torch.randn((M, K), device=dev).to(torch.bfloat16)
+    mods = []
+    for i, (_, N) in enumerate(specs):
+        W = synth.sweep_weight_gpu(0, i, N, K)
+        A = (torch.randn((r, K), device=dev) / K ** 0.5).to(torch.bfloat16)
+        B = (torch.randn((N, r), device=dev) * 0.01).to(torch.bfloat16)
+        mods.append((q.nf4_quantize(W), A, B, alpha))
+    Ncat = sum(N for _, N in specs)
+    dY = torch.randn((M, Ncat), device=dev).to(torch.bfloat16)
+    dYs = [dY[:, o:o + N].contiguous() for o, N in zip((0, 4096, 5120), (4096, 1024, 1024))]
+
+    def separate():
+        for (qw, A, B, a), g in zip(mods, dYs):
+            _, U = q.qlora_linear_fwd(qw, X, A, B, a)
+            q.qlora_linear_bwd(qw, X, A, B, a, g, U)
+
+    def concatenated():
+        _, U = q.qlora_linear_fwd_cat(mods, X)
+        q.qlora_linear_bwd_cat(mods, X, dY, U)
+
+    def timed(fn):
+        fn()
+        ts = []
+        for _ in range(reps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        return statistics.median(ts)
+
+    t_sep, t_cat = timed(separate), timed(concatenated)
+    fl = sum(4.0 * M * N * K + 6.0 * M * r * (N + K) for _, N in specs)
+    return {"modules": "q 4096x4096, k 1024x4096, v 1024x4096; M=4096, r=16", "separate_ms": t_sep,
+            "concatenated_ms": t_cat, "TFLOP/s_separate": fl / t_sep / 1e9, "TFLOP/s_concatenated": fl / t_cat / 1e9,
+            "speedup": t_sep / t_cat}
 
 
 def hbm_extras(q, _lib, L, dev, peaks, flush):

@@ -19,7 +19,7 @@ import torch
 from . import _lib
 
 __all__ = ["NF4Weight", "QLoRAError", "nf4_quantize", "nf4_quantize_noalloc", "nf4_dequantize", "qlora_linear_fwd", "qlora_linear_bwd",
-           "qlora_merge", "nf4_storage_bytes", "quantize_workspace_bytes", "fwd_workspace_bytes", "bwd_workspace_bytes",
+           "qlora_merge", "qlora_linear_fwd_cat", "qlora_linear_bwd_cat", "nf4_storage_bytes", "quantize_workspace_bytes", "fwd_workspace_bytes", "bwd_workspace_bytes",
            "merge_workspace_bytes",
            "check_device_error", "launch_count", "nf4_levels", "empty_nf4"]
 
@@ -237,6 +237,86 @@ def qlora_merge(q: NF4Weight, A: torch.Tensor, B: torch.Tensor, alpha: float, ou
     _check(L.qlora_merge(ctypes.byref(st), _ptr(A), _ptr(B), r, float(alpha), _ptr(out), _ptr(ws),
                          ws.numel() * ws.element_size(), _stream(stream)), "qlora_merge")
     return out
+
+
+class _CatModules:
+    """ctypes view of a module list [(NF4Weight, A, B, alpha), ...] for the concatenated calls."""
+
+    def __init__(self, modules):
+        if not 1 <= len(modules) <= 4:
+            raise ValueError("1 to 4 modules")
+        self.structs = [m[0].struct() for m in modules]  # kept alive for the call
+        arr = (_lib.CatModuleStruct * len(modules))()
+        for i, (qw, A, B, alpha) in enumerate(modules):
+            r = A.shape[0]
+            _need(A, torch.bfloat16, f"A[{i}]", (r, qw.cols))
+            _need(B, torch.bfloat16, f"B[{i}]", (qw.rows, r))
+            arr[i].W = ctypes.pointer(self.structs[i])
+            arr[i].A = A.data_ptr()
+            arr[i].B = B.data_ptr()
+            arr[i].r = r
+            arr[i].alpha = float(alpha)
+        self.arr = arr
+        self.G = len(modules)
+        self.N = (ctypes.c_int64 * self.G)(*[m[0].rows for m in modules])
+        self.r = (ctypes.c_int32 * self.G)(*[m[1].shape[0] for m in modules])
+        self.Ncat = sum(m[0].rows for m in modules)
+        self.R8 = sum((m[1].shape[0] + 7) // 8 * 8 for m in modules)
+        self.K = modules[0][0].cols
+
+
+def qlora_linear_fwd_cat(modules, X: torch.Tensor, Y: torch.Tensor | None = None, U_save: torch.Tensor | None = None,
+                         save_u: bool = True, workspace: torch.Tensor | None = None, stream=None):
+    """Modules [(NF4Weight, A, B, alpha), ...] sharing X, as one N-concatenated layer.
+    Returns (Y [M, sum N_i], U [M, R8] or None); Y[:, o_i:o_i + N_i] is module i's output."""
+    cm = _CatModules(modules)
+    M = X.shape[0]
+    _need(X, torch.bfloat16, "X", (M, cm.K))
+    dev = X.device
+    if Y is None:
+        Y = torch.empty((M, cm.Ncat), dtype=torch.bfloat16, device=dev)
+    _need(Y, torch.bfloat16, "Y", (M, cm.Ncat))
+    if U_save is None and save_u:
+        U_save = torch.empty((M, cm.R8), dtype=torch.bfloat16, device=dev)
+    if U_save is not None:
+        _need(U_save, torch.bfloat16, "U_save", (M, cm.R8))
+    L = _lib.load()
+    need = int(L.qlora_cat_fwd_workspace_bytes(ctypes.cast(cm.N, ctypes.c_void_p), ctypes.cast(cm.r, ctypes.c_void_p),
+                                               cm.G, M, cm.K))
+    if need == ctypes.c_size_t(-1).value:
+        raise QLoRAError(2, "qlora_linear_fwd_cat")
+    ws = _workspace(need, workspace, dev)
+    _check(L.qlora_linear_fwd_cat(ctypes.cast(cm.arr, ctypes.c_void_p), cm.G, _ptr(X), M, _ptr(Y), _ptr(U_save),
+                                  _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)), "qlora_linear_fwd_cat")
+    return Y, U_save
+
+
+def qlora_linear_bwd_cat(modules, X: torch.Tensor, dY: torch.Tensor, U_saved: torch.Tensor | None = None,
+                         dX: torch.Tensor | None = None, workspace: torch.Tensor | None = None, stream=None):
+    """Returns (dX bf16 [M, K], [dA_i fp32 [r_i, K]], [dB_i fp32 [N_i, r_i]])."""
+    cm = _CatModules(modules)
+    M = X.shape[0]
+    _need(X, torch.bfloat16, "X", (M, cm.K))
+    _need(dY, torch.bfloat16, "dY", (M, cm.Ncat))
+    if U_saved is not None:
+        _need(U_saved, torch.bfloat16, "U_saved", (M, cm.R8))
+    dev = X.device
+    dX = torch.empty((M, cm.K), dtype=torch.bfloat16, device=dev) if dX is None else dX
+    _need(dX, torch.bfloat16, "dX", (M, cm.K))
+    dA = [torch.empty((m[1].shape[0], cm.K), dtype=torch.float32, device=dev) for m in modules]
+    dB = [torch.empty((m[0].rows, m[1].shape[0]), dtype=torch.float32, device=dev) for m in modules]
+    pa = (ctypes.c_void_p * cm.G)(*[t.data_ptr() for t in dA])
+    pb = (ctypes.c_void_p * cm.G)(*[t.data_ptr() for t in dB])
+    L = _lib.load()
+    need = int(L.qlora_cat_bwd_workspace_bytes(ctypes.cast(cm.N, ctypes.c_void_p), ctypes.cast(cm.r, ctypes.c_void_p),
+                                               cm.G, M, cm.K))
+    if need == ctypes.c_size_t(-1).value:
+        raise QLoRAError(2, "qlora_linear_bwd_cat")
+    ws = _workspace(need, workspace, dev)
+    _check(L.qlora_linear_bwd_cat(ctypes.cast(cm.arr, ctypes.c_void_p), cm.G, _ptr(X), M, _ptr(dY), _ptr(U_saved),
+                                  _ptr(dX), ctypes.cast(pa, ctypes.c_void_p), ctypes.cast(pb, ctypes.c_void_p),
+                                  _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)), "qlora_linear_bwd_cat")
+    return dX, dA, dB
 
 
 def check_device_error(stream=None) -> None:

@@ -18,6 +18,7 @@ EXPORTS = (
     "qlora_nf4_storage_bytes", "qlora_quantize_workspace_bytes", "qlora_fwd_workspace_bytes",
     "qlora_bwd_workspace_bytes", "nf4_quantize", "nf4_dequantize", "qlora_linear_fwd", "qlora_linear_bwd",
     "qlora_merge_workspace_bytes", "qlora_merge",
+    "qlora_cat_fwd_workspace_bytes", "qlora_cat_bwd_workspace_bytes", "qlora_linear_fwd_cat", "qlora_linear_bwd_cat",
     "qlora_check_device_error", "qlora_status_string", "qlora_launch_count", "qlora_nf4_levels",
     "qlora_set_kernel_timer", "qlora_kernel_timer_count", "nf4_quantize_noalloc",
 )
@@ -27,6 +28,11 @@ class NF4TensorStruct(ctypes.Structure):
     _fields_ = [("rows", ctypes.c_int64), ("cols", ctypes.c_int64), ("codes", ctypes.c_void_p),
                 ("scale_codes", ctypes.c_void_p), ("scale_scales", ctypes.c_void_p),
                 ("scale_offset", ctypes.c_void_p)]
+
+
+class CatModuleStruct(ctypes.Structure):
+    _fields_ = [("W", ctypes.POINTER(NF4TensorStruct)), ("A", ctypes.c_void_p), ("B", ctypes.c_void_p),
+                ("r", ctypes.c_int32), ("alpha", ctypes.c_float)]
 
 
 _lib = None
@@ -48,6 +54,10 @@ def load():
         "qlora_bwd_workspace_bytes": (SZ, [I64, I64, I64, I32]),
         "qlora_merge_workspace_bytes": (SZ, [I64, I64, I32]),
         "qlora_merge": (ctypes.c_int, [ST, P, P, I32, ctypes.c_float, P, P, SZ, P]),
+        "qlora_cat_fwd_workspace_bytes": (SZ, [P, P, I32, I64, I64]),
+        "qlora_cat_bwd_workspace_bytes": (SZ, [P, P, I32, I64, I64]),
+        "qlora_linear_fwd_cat": (ctypes.c_int, [P, I32, P, I64, P, P, P, SZ, P]),
+        "qlora_linear_bwd_cat": (ctypes.c_int, [P, I32, P, I64, P, P, P, P, P, P, SZ, P]),
         "nf4_quantize": (ctypes.c_int, [P, ST, P, SZ, P]),
         "nf4_dequantize": (ctypes.c_int, [ST, P, P]),
         "nf4_quantize_noalloc": (ctypes.c_int, [P, ST, P]),

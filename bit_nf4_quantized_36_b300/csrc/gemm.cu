@@ -554,7 +554,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFusedThreads, 1)
 __device__ __forceinline__ void proj_store(const ProjArgs &a, int64_t i, int j, float v) {
     if (a.mode == 0) {
         if (j < a.ld_h) {
-            __nv_bfloat16 h = __float2bfloat16_rn(__fmul_rn(v, a.scale));
+            __nv_bfloat16 h = __float2bfloat16_rn(__fmul_rn(v, a.col_scale ? a.col_scale[j] : a.scale));
             const uint16_t hb = *reinterpret_cast<uint16_t *>(&h);
             a.out_h[i * a.ld_h + j] = hb;
             if (a.out_h2 && j < a.r) a.out_h2[i * a.r + j] = hb;
@@ -726,7 +726,7 @@ __global__ void __launch_bounds__(128, 1)
 // ---------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) dq_scales_t_kernel(const int8_t *__restrict__ q, const float *__restrict__ c2,
                                                           const float *__restrict__ mu_p, int64_t N, int KB,
-                                                          float *__restrict__ out) {
+                                                          float *__restrict__ out, int64_t ld) {
     __shared__ float tile[32][33];
     const float mu = *mu_p;
     const int64_t n0 = (int64_t)blockIdx.x * 32;
@@ -746,7 +746,7 @@ __global__ void __launch_bounds__(256) dq_scales_t_kernel(const int8_t *__restri
     for (int i = ty; i < 32; i += 8) {
         const int kb = kb0 + i;
         const int64_t n = n0 + tx;
-        if (n < N && kb < KB) out[(int64_t)kb * N + n] = tile[tx][i];
+        if (n < N && kb < KB) out[(int64_t)kb * ld + n] = tile[tx][i];
     }
 }
 
@@ -957,9 +957,9 @@ cudaError_t launch_proj(bool p_mn, bool q_mn, const CUtensorMap &map_p, const CU
 }
 
 cudaError_t launch_dq_scales_t(const int8_t *q, const float *c2, const float *mu, int64_t N, int KB, float *out,
-                               cudaStream_t st) {
+                               cudaStream_t st, int64_t ld) {
     dim3 grid((unsigned)((N + 31) / 32), (unsigned)((KB + 31) / 32));
-    dq_scales_t_kernel<<<grid, 256, 0, st>>>(q, c2, mu, N, KB, out);
+    dq_scales_t_kernel<<<grid, 256, 0, st>>>(q, c2, mu, N, KB, out, ld > 0 ? ld : N);
     count_launch();
     return cudaGetLastError();
 }

@@ -6,4 +6,5 @@
 #include "gemv.cu"
 #include "merge.cu"
 #include "api.cu"
+#include "cat.cu"
 #include "noalloc.cu"

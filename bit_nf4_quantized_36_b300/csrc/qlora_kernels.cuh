@@ -74,9 +74,9 @@ cudaError_t launch_fused(bool dx, const CUtensorMap &map_codes, const CUtensorMa
                          const FusedArgs &args, const FusedPlan &plan, cudaStream_t st);
 cudaError_t launch_splitk_reduce(const float *partial, int splits, int64_t rows, int64_t cols, uint16_t *out,
                                  int num_sms, cudaStream_t st);
-// out[kb, n] = fmaf(q[n*KB + kb], fl32(c2 / 127), mu)
+// out[kb * ld + n] = fmaf(q[n*KB + kb], fl32(c2 / 127), mu)   (ld = N when 0)
 cudaError_t launch_dq_scales_t(const int8_t *q, const float *c2, const float *mu, int64_t N, int KB, float *out,
-                               cudaStream_t st);
+                               cudaStream_t st, int64_t ld = 0);
 
 // ---- skinny LoRA products D[i, j] = sum_c P[i, c] Q[j, c], j < r64 (gemm.cu) -------------
 // P: K-major ([Mp, Kc] row-major, map dims {Kc, Mp}, box {64, 128}) or
@@ -85,13 +85,15 @@ cudaError_t launch_dq_scales_t(const int8_t *q, const float *c2, const float *mu
 //    MN-major ([Kc, r], map dims {r, Kc}, box {64, 64}); rows/columns >= r read as zero.
 // Split over the contraction across the CTAs of one cluster, whose fp32 partial tiles are summed
 // in split order through distributed shared memory, and stored:
-//   mode 0: out_h[i, j] = bf16(scale * D) for j < ld_h; out_h2[i, j] (nullable) for j < r
+//   mode 0: out_h[i, j] = bf16(scale_j * D) for j < ld_h (scale_j = col_scale[j], or scale when
+//           col_scale is NULL); out_h2[i, j] (nullable) for j < r
 //   mode 1: out_f[j, i] = D for j < r  (transposed fp32)
 //   mode 2: out_f[i, j] = D for j < r  (fp32)
 struct ProjArgs {
     int Mp, r64, r, tiles, splits, ktiles;
     int mode;
     float scale;
+    const float *col_scale;  // [ld_h] per-column scales (nullable)
     uint16_t *out_h;
     int ld_h;
     uint16_t *out_h2;

@@ -113,6 +113,40 @@ qlora_status nf4_quantize_noalloc(const float *W, const qlora_nf4_tensor *out, v
  * absmax; glossary: dequantized to bfloat16 before the matmul).  No workspace. */
 qlora_status nf4_dequantize(const qlora_nf4_tensor *q, uint16_t *W_out, void *stream);
 
+/* ---- Concatenated projections sharing one input ----------------------------------------
+ * Several modules applied to the same X (q/k/v, or gate/up, with "all-linear" adapters: coddykit
+ * "Módulos objetivo" and the config's target_modules) computed as one N-concatenated layer, so
+ * that X is streamed once and all modules' tiles fill the GPU's waves together.
+ * Module i: W_i [N_i, K] (N_i a multiple of 128, the same K for all modules), A_i [r_i, K] and
+ * B_i [N_i, r_i] bf16 (16-byte aligned), 1 <= r_i <= 256, alpha_i finite.  1 <= G <= 4 modules,
+ * and R8 = sum_i ceil8(r_i) <= 256.  Column offsets: o_i = N_0 + ... + N_{i-1} (outputs),
+ * c_i = ceil8(r_0) + ... + ceil8(r_{i-1}) (the concatenated rank). */
+typedef struct {
+    const qlora_nf4_tensor *W;
+    const uint16_t *A;
+    const uint16_t *B;
+    int32_t r;
+    float alpha;
+} qlora_cat_module;
+
+/* Workspace sizes of the two calls below for modules with rows N[i] and ranks r[i]; (size_t)-1
+ * for unsupported shapes. */
+size_t qlora_cat_fwd_workspace_bytes(const int64_t *N, const int32_t *r, int32_t G, int64_t M, int64_t K);
+size_t qlora_cat_bwd_workspace_bytes(const int64_t *N, const int32_t *r, int32_t G, int64_t M, int64_t K);
+
+/* Y [M, sum N_i] bf16: columns o_i .. o_i + N_i - 1 hold module i's qlora_linear_fwd output.
+ * U_save (nullable) [M, R8] bf16: columns c_i .. c_i + r_i - 1 hold bf16(s_i X A_i^T), the other
+ * columns 0 (pass it to qlora_linear_bwd_cat). */
+qlora_status qlora_linear_fwd_cat(const qlora_cat_module *mods, int32_t G, const uint16_t *X, int64_t M,
+                                  uint16_t *Y, uint16_t *U_save, void *ws, size_t ws_bytes, void *stream);
+
+/* dY [M, sum N_i] bf16 (columns as in Y); U_saved [M, R8] (nullable: recomputed).
+ * dX [M, K] = sum_i (dY_i W^_i + s_i (dY_i B_i) A_i), one fp32 accumulation, bf16 out;
+ * dA[i] [r_i, K] and dB[i] [N_i, r_i] fp32 as qlora_linear_bwd gives for module i. */
+qlora_status qlora_linear_bwd_cat(const qlora_cat_module *mods, int32_t G, const uint16_t *X, int64_t M,
+                                  const uint16_t *dY, const uint16_t *U_saved, uint16_t *dX, float *const *dA,
+                                  float *const *dB, void *ws, size_t ws_bytes, void *stream);
+
 /* Merge the adapters into the base weight ("QLoRA" glossary, "Compromissos": to merge the
  * adapters the base weight is first dequantized to 16 bits; "QLoRA e metodos relacionados": the
  * fine-tuned model is merged into 16-bit weights):
