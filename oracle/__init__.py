@@ -77,6 +77,11 @@ def _declare(L):
     L.orc_bf16_round_d.argtypes = [_D]
     L.orc_bf16_round_d.restype = ctypes.c_uint16
     L.orc_merge.argtypes = [_P, _P, _P, _I64, _I64, _I64, _D, _P]
+    L.orc_philox4x32_10.argtypes = [_P, _P, _P]
+    L.orc_dropout_scale.argtypes = [ctypes.c_uint64, ctypes.c_uint64, _D, _I64, _P]
+    L.orc_layer_fwd_rows_drop.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _I64, _D, _P, _P, _I64, _P, _P]
+    L.orc_layer_dx_rows_drop.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _I64, _D, _P, _P, _I64, _P]
+    L.orc_layer_adapter_grads_drop.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _I64, _D, _P, _P, _P]
 
 
 def _c(a: np.ndarray, dtype) -> np.ndarray:
@@ -281,3 +286,59 @@ def merge(What, A, B, alpha: float) -> np.ndarray:
     out = np.zeros((N, K), dtype=np.uint16)
     lib().orc_merge(_ptr(What), _ptr(A), _ptr(B), N, K, r, float(alpha), _ptr(out))
     return out
+
+
+def philox4x32_10(ctr, key) -> np.ndarray:
+    """Philox4x32-10 block: four uint32 counter words and two uint32 key words -> four words."""
+    c = _c(np.asarray(ctr, dtype=np.uint64).astype(np.uint32), np.uint32)
+    k = _c(np.asarray(key, dtype=np.uint64).astype(np.uint32), np.uint32)
+    out = np.zeros(4, dtype=np.uint32)
+    lib().orc_philox4x32_10(_ptr(c), _ptr(k), _ptr(out))
+    return out
+
+
+def dropout_scale(seed: int, offset: int, p: float, M: int, K: int) -> np.ndarray:
+    """fp64 [M, K]: 1 / (1 - p) where the element of the adapter input is kept, else 0."""
+    D = np.zeros(M * K, dtype=np.float64)
+    lib().orc_dropout_scale(ctypes.c_uint64(seed), ctypes.c_uint64(offset), float(p), M * K, _ptr(D))
+    return D.reshape(M, K)
+
+
+def layer_fwd_rows_drop(What, X, A, B, alpha: float, D, rows=None):
+    What, X, A, B = (_c(t, np.uint16) for t in (What, X, A, B))
+    D = _c(D, np.float64)
+    N, K = What.shape
+    M = X.shape[0]
+    r = A.shape[0]
+    sel = np.arange(M, dtype=np.int64) if rows is None else _c(rows, np.int64)
+    Y = np.zeros((sel.size, N), dtype=np.float64)
+    U = np.zeros((sel.size, r), dtype=np.float64)
+    lib().orc_layer_fwd_rows_drop(_ptr(What), _ptr(X), _ptr(A), _ptr(B), M, N, K, r, float(alpha), _ptr(D),
+                                  _ptr(sel), sel.size, _ptr(Y), _ptr(U))
+    return Y, U
+
+
+def layer_dx_rows_drop(What, A, B, G, alpha: float, D, rows=None):
+    What, A, B, G = (_c(t, np.uint16) for t in (What, A, B, G))
+    D = _c(D, np.float64)
+    N, K = What.shape
+    M = G.shape[0]
+    r = A.shape[0]
+    sel = np.arange(M, dtype=np.int64) if rows is None else _c(rows, np.int64)
+    dX = np.zeros((sel.size, K), dtype=np.float64)
+    lib().orc_layer_dx_rows_drop(_ptr(What), _ptr(A), _ptr(B), _ptr(G), M, N, K, r, float(alpha), _ptr(D),
+                                 _ptr(sel), sel.size, _ptr(dX))
+    return dX
+
+
+def layer_adapter_grads_drop(X, A, B, G, alpha: float, D):
+    X, A, B, G = (_c(t, np.uint16) for t in (X, A, B, G))
+    D = _c(D, np.float64)
+    M, K = X.shape
+    N = G.shape[1]
+    r = A.shape[0]
+    dA = np.zeros((r, K), dtype=np.float64)
+    dB = np.zeros((N, r), dtype=np.float64)
+    lib().orc_layer_adapter_grads_drop(_ptr(X), _ptr(A), _ptr(B), _ptr(G), M, N, K, r, float(alpha), _ptr(D),
+                                       _ptr(dA), _ptr(dB))
+    return dA, dB

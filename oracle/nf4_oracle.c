@@ -541,3 +541,147 @@ void orc_merge(const uint16_t *What, const uint16_t *A, const uint16_t *B, int64
         }
     }
 }
+
+/* ------------------------------------------------------------------------------------ */
+/* LoRA dropout on the adapter input ([coddykit], LoraConfig: lora_dropout=0.05): the       */
+/* adapter branch sees x_d = x * mask / (1 - p) with mask ~ Bernoulli(1 - p) per element:    */
+/*   h = W^ x + s B A x_d,   dX = G W^ + mask/(1-p) * (s (G B) A),                           */
+/*   dA = s (G B)^T x_d,     dB = s G^T (x_d A^T).                                         */
+/* READING (the pages give only p): the mask comes from the counter-based generator          */
+/* Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as 1, 2, 3",  */
+/* SC'11): element e of the row-major [M, K] input uses word e % 4 of the block with counter */
+/* (e / 4 as two 32-bit halves, offset as two 32-bit halves) and key (seed as two halves);  */
+/* it is kept when word >= floor(p 2^32).                                                  */
+/* ------------------------------------------------------------------------------------ */
+static uint32_t mulhilo32(uint32_t a, uint32_t b, uint32_t *hi)
+{
+    uint64_t prod = (uint64_t)a * (uint64_t)b;
+    *hi = (uint32_t)(prod >> 32);
+    return (uint32_t)prod;
+}
+
+/* Philox4x32 with 10 rounds: each round multiplies counter words 0 and 2 by the round
+ * multipliers, mixes the high halves with words 1, 3 and the key, and the key is bumped by
+ * the Weyl constants between rounds. */
+void orc_philox4x32_10(const uint32_t ctr_in[4], const uint32_t key_in[2], uint32_t out[4])
+{
+    uint32_t c0 = ctr_in[0], c1 = ctr_in[1], c2 = ctr_in[2], c3 = ctr_in[3];
+    uint32_t k0 = key_in[0], k1 = key_in[1];
+    for (int round = 0; round < 10; ++round) {
+        uint32_t hi0, hi1;
+        uint32_t lo0 = mulhilo32(0xD2511F53u, c0, &hi0);
+        uint32_t lo1 = mulhilo32(0xCD9E8D57u, c2, &hi1);
+        uint32_t n0 = hi1 ^ c1 ^ k0, n1 = lo1, n2 = hi0 ^ c3 ^ k1, n3 = lo0;
+        c0 = n0; c1 = n1; c2 = n2; c3 = n3;
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
+}
+
+/* D[e] = 1 / (1 - p) where element e is kept, 0 where it is dropped (fp64), for e < n. */
+void orc_dropout_scale(uint64_t seed, uint64_t offset, double p, int64_t n, double *D)
+{
+    uint32_t thr = (uint32_t)floor(p * 4294967296.0);
+    double keep_scale = 1.0 / (1.0 - p);
+    uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+    for (int64_t e = 0; e < n; ++e) {
+        uint64_t blk = (uint64_t)e / 4;
+        uint32_t ctr[4] = {(uint32_t)blk, (uint32_t)(blk >> 32), (uint32_t)offset, (uint32_t)(offset >> 32)};
+        uint32_t w[4];
+        orc_philox4x32_10(ctr, key, w);
+        D[e] = (w[e % 4] >= thr) ? keep_scale : 0.0;
+    }
+}
+
+/* As orc_layer_fwd_rows, with the adapter input x * D (D [M, K] from orc_dropout_scale). */
+void orc_layer_fwd_rows_drop(const uint16_t *What, const uint16_t *X, const uint16_t *A, const uint16_t *B,
+                             int64_t M, int64_t N, int64_t K, int64_t r, double alpha, const double *D,
+                             const int64_t *sel, int64_t nsel, double *Y_out, double *U_out)
+{
+    (void)M;
+    double s = alpha / (double)r;
+    double *u = (double *)malloc(sizeof(double) * (size_t)(r > 0 ? r : 1));
+    for (int64_t ii = 0; ii < nsel; ++ii) {
+        int64_t m = sel[ii];
+        for (int64_t j = 0; j < r; ++j) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; ++k)
+                acc += orc_bf16_to_double(X[m * K + k]) * D[m * K + k] * orc_bf16_to_double(A[j * K + k]);
+            u[j] = acc;
+            if (U_out) U_out[ii * r + j] = acc;
+        }
+        for (int64_t n = 0; n < N; ++n) {
+            double base = 0.0;
+            for (int64_t k = 0; k < K; ++k) base += orc_bf16_to_double(X[m * K + k]) * orc_bf16_to_double(What[n * K + k]);
+            double lora = 0.0;
+            for (int64_t j = 0; j < r; ++j) lora += u[j] * orc_bf16_to_double(B[n * r + j]);
+            Y_out[ii * N + n] = base + s * lora;
+        }
+    }
+    free(u);
+}
+
+/* As orc_layer_dx_rows, with the adapter branch's input gradient multiplied by D. */
+void orc_layer_dx_rows_drop(const uint16_t *What, const uint16_t *A, const uint16_t *B, const uint16_t *G,
+                            int64_t M, int64_t N, int64_t K, int64_t r, double alpha, const double *D,
+                            const int64_t *sel, int64_t nsel, double *dX_out)
+{
+    (void)M;
+    double s = alpha / (double)r;
+    double *v = (double *)malloc(sizeof(double) * (size_t)(r > 0 ? r : 1));
+    double *row = (double *)malloc(sizeof(double) * (size_t)K);
+    for (int64_t ii = 0; ii < nsel; ++ii) {
+        int64_t m = sel[ii];
+        for (int64_t j = 0; j < r; ++j) {
+            double acc = 0.0;
+            for (int64_t n = 0; n < N; ++n) acc += orc_bf16_to_double(G[m * N + n]) * orc_bf16_to_double(B[n * r + j]);
+            v[j] = acc;
+        }
+        for (int64_t k = 0; k < K; ++k) row[k] = 0.0;
+        for (int64_t n = 0; n < N; ++n) {
+            double g = orc_bf16_to_double(G[m * N + n]);
+            for (int64_t k = 0; k < K; ++k) row[k] += g * orc_bf16_to_double(What[n * K + k]);
+        }
+        for (int64_t k = 0; k < K; ++k) {
+            double lora = 0.0;
+            for (int64_t j = 0; j < r; ++j) lora += v[j] * orc_bf16_to_double(A[j * K + k]);
+            dX_out[ii * K + k] = row[k] + D[m * K + k] * s * lora;
+        }
+    }
+    free(v);
+    free(row);
+}
+
+/* As orc_layer_adapter_grads, with the adapter input x * D. */
+void orc_layer_adapter_grads_drop(const uint16_t *X, const uint16_t *A, const uint16_t *B, const uint16_t *G,
+                                  int64_t M, int64_t N, int64_t K, int64_t r, double alpha, const double *D,
+                                  double *dA_out, double *dB_out)
+{
+    double s = alpha / (double)r;
+    double *U = (double *)calloc((size_t)(M * r), sizeof(double));
+    double *V = (double *)calloc((size_t)(M * r), sizeof(double));
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t j = 0; j < r; ++j) {
+            double au = 0.0, av = 0.0;
+            for (int64_t k = 0; k < K; ++k)
+                au += orc_bf16_to_double(X[m * K + k]) * D[m * K + k] * orc_bf16_to_double(A[j * K + k]);
+            for (int64_t n = 0; n < N; ++n) av += orc_bf16_to_double(G[m * N + n]) * orc_bf16_to_double(B[n * r + j]);
+            U[m * r + j] = au;
+            V[m * r + j] = av;
+        }
+    for (int64_t j = 0; j < r; ++j)
+        for (int64_t k = 0; k < K; ++k) {
+            double acc = 0.0;
+            for (int64_t m = 0; m < M; ++m) acc += V[m * r + j] * orc_bf16_to_double(X[m * K + k]) * D[m * K + k];
+            dA_out[j * K + k] = s * acc;
+        }
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t j = 0; j < r; ++j) {
+            double acc = 0.0;
+            for (int64_t m = 0; m < M; ++m) acc += orc_bf16_to_double(G[m * N + n]) * U[m * r + j];
+            dB_out[n * r + j] = s * acc;
+        }
+    free(U);
+    free(V);
+}

@@ -483,3 +483,79 @@ def test_merge_ties_round_to_even(orc):
     assert np.all(orc.merge(What, A, B1, 1.0) == 0x3F80)
     B3 = np.array([[orc.bf16_round(3 * 2.0 ** -8)]], dtype=np.uint16)     # 1 + 3 2^-8: a tie
     assert np.all(orc.merge(What, A, B3, 1.0) == 0x3F82)
+
+
+# ---------------------------------------------------------------------------------------
+# LoRA dropout on the adapter input ("LoRA y QLoRA ...", coddykit, LoraConfig lora_dropout=0.05).
+# The mask generator is Philox4x32-10 (Salmon et al., "Parallel random numbers: as easy as 1, 2,
+# 3", SC'11); its published known-answer vectors pin the oracle's implementation.
+# ---------------------------------------------------------------------------------------
+
+def test_philox_known_answer_vectors(orc):
+    assert list(orc.philox4x32_10([0, 0, 0, 0], [0, 0])) == [0x6627E8D5, 0xE169C58D, 0xBC57AC4C, 0x9B00DBD8]
+    assert list(orc.philox4x32_10([0xFFFFFFFF] * 4, [0xFFFFFFFF] * 2)) == [0x408F276D, 0x41C83B0E, 0xA20BC7C6, 0x6D5451FD]
+    assert list(orc.philox4x32_10([0x243F6A88, 0x85A308D3, 0x13198A2E, 0x03707344], [0xA4093822, 0x299F31D0])) == \
+        [0xD16CFE09, 0x94FDCCEB, 0x5001E420, 0x24126EA1]
+
+
+def test_dropout_mask_rate_and_layout(orc):
+    p = 0.05
+    D = orc.dropout_scale(1234, 0, p, 400, 512)
+    keep = D != 0
+    n = keep.size
+    assert np.all(D[keep] == 1.0 / (1.0 - p))
+    frac = keep.mean()
+    assert abs(frac - (1 - p)) < 5 * np.sqrt(p * (1 - p) / n)
+    # element e uses word e % 4 of block e // 4: the kept flags follow the generator directly
+    thr = int(np.floor(p * 2.0 ** 32))
+    for e in (0, 1, 2, 3, 4, 77, n - 1):
+        w = orc.philox4x32_10([e // 4, 0, 0, 0], [1234, 0])[e % 4]
+        assert keep.flat[e] == (int(w) >= thr)
+    # a different offset gives a different mask; p = 0.5: neighbouring flags look independent
+    assert not np.array_equal(keep, orc.dropout_scale(1234, 1, p, 400, 512) != 0)
+    k2 = orc.dropout_scale(99, 7, 0.5, 400, 512) != 0
+    both = (k2.flat[:-1] & k2.flat[1:]).mean()
+    assert abs(both - 0.25) < 5 * np.sqrt(0.25 * 0.75 / (k2.size - 1))
+
+
+def test_dropout_p0_is_the_plain_layer(orc):
+    What, X, A, B, G = _small_layer(24, M=5, N=6, K=64, r=3)
+    alpha = 6.0
+    D = orc.dropout_scale(5, 0, 0.0, 5, 64)
+    assert np.all(D == 1.0)
+    Y0, U0 = orc.layer_fwd_rows(What, X, A, B, alpha)
+    Y1, U1 = orc.layer_fwd_rows_drop(What, X, A, B, alpha, D)
+    assert np.array_equal(Y0, Y1) and np.array_equal(U0, U1)
+    assert np.array_equal(orc.layer_dx_rows(What, A, B, G, alpha), orc.layer_dx_rows_drop(What, A, B, G, alpha, D))
+    for a, b in zip(orc.layer_adapter_grads(X, A, B, G, alpha), orc.layer_adapter_grads_drop(X, A, B, G, alpha, D)):
+        assert np.array_equal(a, b)
+
+
+def test_dropout_grads_finite_differences(orc):
+    What, X, A, B, G = _small_layer(25, M=4, N=5, K=64, r=2)
+    alpha = 4.0
+    f = orc.bf16_to_f64
+    s = alpha / A.shape[0]
+    D = orc.dropout_scale(77, 3, 0.3, 4, 64)
+    assert (D == 0).any() and (D != 0).any()
+
+    def loss(Xf, Af, Bf):
+        return float(np.sum(f(G) * (Xf @ f(What).T + s * ((Xf * D) @ Af.T) @ Bf.T)))
+
+    dA, dB = orc.layer_adapter_grads_drop(X, A, B, G, alpha, D)
+    dX = orc.layer_dx_rows_drop(What, A, B, G, alpha, D)
+    Xf, Af, Bf = f(X), f(A), f(B)
+    h = 1e-3
+    for (j, k) in [(0, 0), (1, 17), (0, 63)]:
+        E = np.zeros_like(Af)
+        E[j, k] = h
+        assert dA[j, k] == pytest.approx((loss(Xf, Af + E, Bf) - loss(Xf, Af - E, Bf)) / (2 * h), rel=1e-7, abs=1e-9)
+    for (n, j) in [(0, 0), (4, 1), (2, 1)]:
+        E = np.zeros_like(Bf)
+        E[n, j] = h
+        assert dB[n, j] == pytest.approx((loss(Xf, Af, Bf + E) - loss(Xf, Af, Bf - E)) / (2 * h), rel=1e-7, abs=1e-9)
+    dropped = np.argwhere(D == 0)[0]
+    for (m, k) in [(0, 0), (3, 40), tuple(dropped)]:
+        E = np.zeros_like(Xf)
+        E[m, k] = h
+        assert dX[m, k] == pytest.approx((loss(Xf + E, Af, Bf) - loss(Xf - E, Af, Bf)) / (2 * h), rel=1e-7, abs=1e-9)
