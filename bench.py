@@ -387,6 +387,10 @@ def run_ours(args):
             extras["concat_qkv"] = concat_extras(q, dev, flush)
         except Exception as e:
             extras["concat_qkv"] = {"error": repr(e)}
+        try:
+            extras["dropout_attn"] = dropout_extras(q, dev, flush, inp)
+        except Exception as e:
+            extras["dropout_attn"] = {"error": repr(e)}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -412,6 +416,40 @@ def run_ours(args):
     if dist is not None:
         dist.destroy_process_group()
     return 0
+
+
+def dropout_extras(q, dev, flush, inp, reps=10):
+    """The bench layer (Llama-3-8B attention projection, M = 4096) fwd + bwd with LoRA dropout
+    p = 0.05 on the adapter input, against the same call without dropout."""
+    import torch
+    W = torch.from_numpy(inp.W).to(dev)
+    qw = q.nf4_quantize(W)
+    X, A, B, G = (torch.from_numpy(np.ascontiguousarray(t).view(np.int16)).to(dev).view(torch.bfloat16)
+                  for t in (inp.X, inp.A, inp.B, inp.G))
+
+    def plain():
+        _, U = q.qlora_linear_fwd(qw, X, A, B, inp.alpha)
+        q.qlora_linear_bwd(qw, X, A, B, inp.alpha, G, U)
+
+    def drop():
+        _, U = q.qlora_linear_fwd_dropout(qw, X, A, B, inp.alpha, 0.05, 1234)
+        q.qlora_linear_bwd_dropout(qw, X, A, B, inp.alpha, 0.05, 1234, G, U)
+
+    def timed(fn):
+        fn()
+        ts = []
+        for _ in range(reps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        return statistics.median(ts)
+
+    t0, t1 = timed(plain), timed(drop)
+    return {"p": 0.05, "plain_fwd_bwd_ms": t0, "dropout_fwd_bwd_ms": t1, "overhead": t1 / t0 - 1.0}
 
 
 def concat_extras(q, dev, flush, reps=10):

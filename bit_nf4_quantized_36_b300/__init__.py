@@ -19,7 +19,8 @@ import torch
 from . import _lib
 
 __all__ = ["NF4Weight", "QLoRAError", "nf4_quantize", "nf4_quantize_noalloc", "nf4_dequantize", "qlora_linear_fwd", "qlora_linear_bwd",
-           "qlora_merge", "qlora_linear_fwd_cat", "qlora_linear_bwd_cat", "nf4_storage_bytes", "quantize_workspace_bytes", "fwd_workspace_bytes", "bwd_workspace_bytes",
+           "qlora_merge", "qlora_linear_fwd_cat", "qlora_linear_bwd_cat", "qlora_linear_fwd_dropout",
+           "qlora_linear_bwd_dropout", "nf4_storage_bytes", "quantize_workspace_bytes", "fwd_workspace_bytes", "bwd_workspace_bytes",
            "merge_workspace_bytes",
            "check_device_error", "launch_count", "nf4_levels", "empty_nf4"]
 
@@ -237,6 +238,64 @@ def qlora_merge(q: NF4Weight, A: torch.Tensor, B: torch.Tensor, alpha: float, ou
     _check(L.qlora_merge(ctypes.byref(st), _ptr(A), _ptr(B), r, float(alpha), _ptr(out), _ptr(ws),
                          ws.numel() * ws.element_size(), _stream(stream)), "qlora_merge")
     return out
+
+
+def qlora_linear_fwd_dropout(q: NF4Weight, X: torch.Tensor, A: torch.Tensor, B: torch.Tensor, alpha: float, p: float,
+                             seed: int, offset: int = 0, Y: torch.Tensor | None = None,
+                             U_save: torch.Tensor | None = None, save_u: bool = True,
+                             workspace: torch.Tensor | None = None, stream=None):
+    """qlora_linear_fwd with LoRA dropout (probability p) on the adapter input; the mask is
+    Philox4x32-10 of (seed, offset, element index).  Returns (Y, U)."""
+    M = X.shape[0]
+    r = A.shape[0]
+    _need(X, torch.bfloat16, "X", (M, q.cols))
+    _need(A, torch.bfloat16, "A", (r, q.cols))
+    _need(B, torch.bfloat16, "B", (q.rows, r))
+    dev = X.device
+    if Y is None:
+        Y = torch.empty((M, q.rows), dtype=torch.bfloat16, device=dev)
+    _need(Y, torch.bfloat16, "Y", (M, q.rows))
+    if U_save is None and save_u:
+        U_save = torch.empty((M, r), dtype=torch.bfloat16, device=dev)
+    L = _lib.load()
+    need = int(L.qlora_fwd_dropout_workspace_bytes(M, q.rows, q.cols, r))
+    if need == ctypes.c_size_t(-1).value:
+        raise QLoRAError(2, "qlora_linear_fwd_dropout")
+    ws = _workspace(need, workspace, dev)
+    d = _lib.DropoutStruct(float(p), int(seed), int(offset))
+    st = q.struct()
+    _check(L.qlora_linear_fwd_dropout(ctypes.byref(st), _ptr(X), M, _ptr(A), _ptr(B), r, float(alpha), ctypes.byref(d),
+                                      _ptr(Y), _ptr(U_save), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
+           "qlora_linear_fwd_dropout")
+    return Y, U_save
+
+
+def qlora_linear_bwd_dropout(q: NF4Weight, X: torch.Tensor, A: torch.Tensor, B: torch.Tensor, alpha: float, p: float,
+                             seed: int, dY: torch.Tensor, U_saved: torch.Tensor | None = None, offset: int = 0,
+                             workspace: torch.Tensor | None = None, stream=None):
+    """qlora_linear_bwd under the forward's dropout (same p, seed, offset).  Returns (dX, dA, dB)."""
+    M = X.shape[0]
+    r = A.shape[0]
+    N, K = q.rows, q.cols
+    _need(X, torch.bfloat16, "X", (M, K))
+    _need(dY, torch.bfloat16, "dY", (M, N))
+    if U_saved is not None:
+        _need(U_saved, torch.bfloat16, "U_saved", (M, r))
+    dev = X.device
+    dX = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+    dA = torch.empty((r, K), dtype=torch.float32, device=dev)
+    dB = torch.empty((N, r), dtype=torch.float32, device=dev)
+    L = _lib.load()
+    need = int(L.qlora_bwd_dropout_workspace_bytes(M, N, K, r))
+    if need == ctypes.c_size_t(-1).value:
+        raise QLoRAError(2, "qlora_linear_bwd_dropout")
+    ws = _workspace(need, workspace, dev)
+    d = _lib.DropoutStruct(float(p), int(seed), int(offset))
+    st = q.struct()
+    _check(L.qlora_linear_bwd_dropout(ctypes.byref(st), _ptr(X), M, _ptr(A), _ptr(B), r, float(alpha), ctypes.byref(d),
+                                      _ptr(dY), _ptr(U_saved), _ptr(dX), _ptr(dA), _ptr(dB), _ptr(ws),
+                                      ws.numel() * ws.element_size(), _stream(stream)), "qlora_linear_bwd_dropout")
+    return dX, dA, dB
 
 
 class _CatModules:

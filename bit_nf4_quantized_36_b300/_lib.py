@@ -19,6 +19,8 @@ EXPORTS = (
     "qlora_bwd_workspace_bytes", "nf4_quantize", "nf4_dequantize", "qlora_linear_fwd", "qlora_linear_bwd",
     "qlora_merge_workspace_bytes", "qlora_merge",
     "qlora_cat_fwd_workspace_bytes", "qlora_cat_bwd_workspace_bytes", "qlora_linear_fwd_cat", "qlora_linear_bwd_cat",
+    "qlora_fwd_dropout_workspace_bytes", "qlora_bwd_dropout_workspace_bytes", "qlora_linear_fwd_dropout",
+    "qlora_linear_bwd_dropout",
     "qlora_check_device_error", "qlora_status_string", "qlora_launch_count", "qlora_nf4_levels",
     "qlora_set_kernel_timer", "qlora_kernel_timer_count", "nf4_quantize_noalloc",
 )
@@ -28,6 +30,10 @@ class NF4TensorStruct(ctypes.Structure):
     _fields_ = [("rows", ctypes.c_int64), ("cols", ctypes.c_int64), ("codes", ctypes.c_void_p),
                 ("scale_codes", ctypes.c_void_p), ("scale_scales", ctypes.c_void_p),
                 ("scale_offset", ctypes.c_void_p)]
+
+
+class DropoutStruct(ctypes.Structure):
+    _fields_ = [("p", ctypes.c_float), ("seed", ctypes.c_uint64), ("offset", ctypes.c_uint64)]
 
 
 class CatModuleStruct(ctypes.Structure):
@@ -58,6 +64,11 @@ def load():
         "qlora_cat_bwd_workspace_bytes": (SZ, [P, P, I32, I64, I64]),
         "qlora_linear_fwd_cat": (ctypes.c_int, [P, I32, P, I64, P, P, P, SZ, P]),
         "qlora_linear_bwd_cat": (ctypes.c_int, [P, I32, P, I64, P, P, P, P, P, P, SZ, P]),
+        "qlora_fwd_dropout_workspace_bytes": (SZ, [I64, I64, I64, I32]),
+        "qlora_bwd_dropout_workspace_bytes": (SZ, [I64, I64, I64, I32]),
+        "qlora_linear_fwd_dropout": (ctypes.c_int, [ST, P, I64, P, P, I32, ctypes.c_float, P, P, P, P, SZ, P]),
+        "qlora_linear_bwd_dropout": (ctypes.c_int, [ST, P, I64, P, P, I32, ctypes.c_float, P, P, P, P, P, P, P, SZ,
+                                                    P]),
         "nf4_quantize": (ctypes.c_int, [P, ST, P, SZ, P]),
         "nf4_dequantize": (ctypes.c_int, [ST, P, P]),
         "nf4_quantize_noalloc": (ctypes.c_int, [P, ST, P]),

@@ -181,9 +181,9 @@ struct LayerWs {
     bool gemv;  // forward with M <= 2: the CUDA-core GEMV instead of the fused kernel
     FusedPlan fp;
     ProjPlan pu, pv, pda, pdb;
-    size_t off_scales, off_u, off_v, off_bpad, off_main, total;
+    size_t off_scales, off_u, off_v, off_bpad, off_main, off_xd, off_mask, total;
 };
-static LayerWs layer_ws(int64_t M, int64_t N, int64_t K, int r, bool bwd, int num_sms) {
+static LayerWs layer_ws(int64_t M, int64_t N, int64_t K, int r, bool bwd, int num_sms, bool drop = false) {
     LayerWs w{};
     w.r8 = ((r + 7) / 8) * 8;
     w.r64 = ((r + 63) / 64) * 64;
@@ -209,6 +209,11 @@ static LayerWs layer_ws(int64_t M, int64_t N, int64_t K, int r, bool bwd, int nu
     if (bwd && r % 8 != 0) off += align256((size_t)N * w.r8 * 2);
     w.off_main = off;
     off += align256(w.gemv ? (size_t)gemv_slices(K) * M * N * 4 : w.fp.partial_bytes);
+    // LoRA dropout: the masked adapter input, and (backward) its kept-element bits
+    w.off_xd = off;
+    if (drop) off += align256((size_t)M * K * 2);
+    w.off_mask = off;
+    if (drop && bwd) off += align256((size_t)M * K / 8);
     w.total = off;
     return w;
 }
@@ -385,16 +390,23 @@ static FusedArgs fused_args(const qlora_nf4_tensor *W, int64_t M, const LayerWs 
     return fa;
 }
 
-qlora_status qlora_linear_fwd(const qlora_nf4_tensor *W, const uint16_t *X, int64_t M, const uint16_t *A,
-                              const uint16_t *B, int32_t r, float alpha, uint16_t *Y, uint16_t *U_save, void *ws,
-                              size_t ws_bytes, void *stream) {
+}  // extern "C"
+
+namespace qlora {
+
+static bool dropout_ok(const qlora_dropout *d) { return d && std::isfinite(d->p) && d->p >= 0.0f && d->p < 1.0f; }
+
+// qlora_linear_fwd, with LoRA dropout on the adapter input when `d` is given
+static qlora_status layer_fwd(const qlora_nf4_tensor *W, const uint16_t *X, int64_t M, const uint16_t *A,
+                              const uint16_t *B, int32_t r, float alpha, const qlora_dropout *d, uint16_t *Y,
+                              uint16_t *U_save, void *ws, size_t ws_bytes, void *stream) {
     qlora_status s = check_layer_args(W, X, M, A, B, r, alpha);
     if (s != QLORA_OK) return s;
     if (!Y) return QLORA_ERR_INVALID_ARG;
     if (!aligned16(Y) || (U_save && !aligned16(U_save))) return QLORA_ERR_MISALIGNED;
     const int64_t N = W->rows, K = W->cols, KB = K / 64;
     const int sms = num_sms_current();
-    const LayerWs w = layer_ws(M, N, K, r, false, sms);
+    const LayerWs w = layer_ws(M, N, K, r, false, sms, d != nullptr);
     if (!ws || ws_bytes < w.total || !aligned16(ws)) return QLORA_ERR_WORKSPACE;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     uint8_t *base = static_cast<uint8_t *>(ws);
@@ -402,10 +414,12 @@ qlora_status qlora_linear_fwd(const qlora_nf4_tensor *W, const uint16_t *X, int6
     uint16_t *U = reinterpret_cast<uint16_t *>(base + w.off_u);
     float *mainp = reinterpret_cast<float *>(base + w.off_main);
     const float scale = alpha / (float)r;
+    // the adapter branch's input: X, or X with the dropout mask applied
+    const uint16_t *Xl = d ? reinterpret_cast<const uint16_t *>(base + w.off_xd) : X;
 
     CUtensorMap mX_k, mA_k, mCodes, mScales, mX_act, mU_act, mY;
     std::memset(&mScales, 0, sizeof(mScales));
-    if (!map_bf16(&mX_k, X, K, M, 64, 128) || !map_bf16(&mA_k, A, K, r, 64, w.r64) ||
+    if (!map_bf16(&mX_k, Xl, K, M, 64, 128) || !map_bf16(&mA_k, A, K, r, 64, w.r64) ||
         !map_codes(&mCodes, W->codes, N, K, false) ||
         (!w.fp.small && !map_scales(&mScales, scalesT, N, KB, false)) ||
         !map_bf16(&mX_act, X, K, M, 64, w.fp.act_rows) || !map_bf16(&mU_act, U, w.r8, M, 64, w.fp.act_rows) ||
@@ -413,10 +427,13 @@ qlora_status qlora_linear_fwd(const qlora_nf4_tensor *W, const uint16_t *X, int6
         return QLORA_ERR_CUDA;
 
     cudaError_t e;
+    if (d && (e = launch_dropout_x(X, M * K, d->seed, d->offset, d->p, const_cast<uint16_t *>(Xl), nullptr, sms, st)) !=
+                 cudaSuccess)
+        return from_cuda(e);
     if (!w.fp.small && (e = launch_dq_scales_t(W->scale_codes, W->scale_scales, W->scale_offset, N, (int)KB, scalesT,
                                                st)) != cudaSuccess)
         return from_cuda(e);
-    // U = bf16(s * X A^T)  [M, r8] (+ U_save [M, r])
+    // U = bf16(s * X A^T)  [M, r8] (+ U_save [M, r]), X masked under dropout
     ProjArgs pu = proj_args(w.pu, M, w, r, 0, scale);
     pu.out_h = U;
     pu.ld_h = w.r8;
@@ -436,9 +453,13 @@ qlora_status qlora_linear_fwd(const qlora_nf4_tensor *W, const uint16_t *X, int6
     return QLORA_OK;
 }
 
-qlora_status qlora_linear_bwd(const qlora_nf4_tensor *W, const uint16_t *X, int64_t M, const uint16_t *A,
-                              const uint16_t *B, int32_t r, float alpha, const uint16_t *dY, const uint16_t *U_saved,
-                              uint16_t *dX, float *dA, float *dB, void *ws, size_t ws_bytes, void *stream) {
+// qlora_linear_bwd, with LoRA dropout on the adapter input when `d` is given: the mask is
+// regenerated from (seed, offset); dX's base term comes from the fused kernel without the adapter
+// k-steps, and the masked adapter term is added by a rank-r update.
+static qlora_status layer_bwd(const qlora_nf4_tensor *W, const uint16_t *X, int64_t M, const uint16_t *A,
+                              const uint16_t *B, int32_t r, float alpha, const qlora_dropout *d, const uint16_t *dY,
+                              const uint16_t *U_saved, uint16_t *dX, float *dA, float *dB, void *ws, size_t ws_bytes,
+                              void *stream) {
     qlora_status s = check_layer_args(W, X, M, A, B, r, alpha);
     if (s != QLORA_OK) return s;
     if (!dY || !dX || !dA || !dB) return QLORA_ERR_INVALID_ARG;
@@ -446,13 +467,16 @@ qlora_status qlora_linear_bwd(const qlora_nf4_tensor *W, const uint16_t *X, int6
         return QLORA_ERR_MISALIGNED;
     const int64_t N = W->rows, K = W->cols, KB = K / 64;
     const int sms = num_sms_current();
-    const LayerWs w = layer_ws(M, N, K, r, true, sms);
+    const LayerWs w = layer_ws(M, N, K, r, true, sms, d != nullptr);
     if (!ws || ws_bytes < w.total || !aligned16(ws)) return QLORA_ERR_WORKSPACE;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     uint8_t *base = static_cast<uint8_t *>(ws);
     float *scalesT = reinterpret_cast<float *>(base + w.off_scales);
     uint16_t *U = reinterpret_cast<uint16_t *>(base + w.off_u);
     uint16_t *V = reinterpret_cast<uint16_t *>(base + w.off_v);
+    uint16_t *Xd = reinterpret_cast<uint16_t *>(base + w.off_xd);
+    uint32_t *mask = reinterpret_cast<uint32_t *>(base + w.off_mask);
+    const uint16_t *Xl = d ? Xd : X;  // the adapter branch's input
     uint16_t *Bpad = reinterpret_cast<uint16_t *>(base + w.off_bpad);
     float *mainp = reinterpret_cast<float *>(base + w.off_main);
     const float scale = alpha / (float)r;
@@ -464,17 +488,23 @@ qlora_status qlora_linear_bwd(const qlora_nf4_tensor *W, const uint16_t *X, int6
     const int64_t rb = r_vec ? r : w.r8;
 
     CUtensorMap mX_k, mA_k, mG_k, mB_mn, mX_mn, mV_mn, mG_mn, mU_mn, mCodes, mScales, mG_act, mV_act, mDX;
+    CUtensorMap mV_k, mA_mn, mDX_sw;
     std::memset(&mScales, 0, sizeof(mScales));
-    if (!map_bf16(&mX_k, X, K, M, 64, 128) || !map_bf16(&mA_k, A, K, r, 64, w.r64) ||
+    if (!map_bf16(&mX_k, Xl, K, M, 64, 128) || !map_bf16(&mA_k, A, K, r, 64, w.r64) ||
         !map_bf16(&mG_k, dY, N, M, 64, 128) || !map_bf16(&mB_mn, Bq, rb, N, 64, 64) ||
-        !map_bf16(&mX_mn, X, K, M, 64, 64) || !map_bf16(&mV_mn, V, w.r8, M, 64, 64) ||
+        !map_bf16(&mX_mn, Xl, K, M, 64, 64) || !map_bf16(&mV_mn, V, w.r8, M, 64, 64) ||
         !map_bf16(&mG_mn, dY, N, M, 64, 64) || !map_bf16(&mU_mn, Uq, ru, M, 64, 64) ||
         !map_codes(&mCodes, W->codes, N, K, true) || (!w.fp.small && !map_scales(&mScales, scalesT, N, KB, true)) ||
         !map_bf16(&mG_act, dY, N, M, 64, w.fp.act_rows) || !map_bf16(&mV_act, V, w.r8, M, 64, w.fp.act_rows) ||
         !map_out(&mDX, dX, M, K))
         return QLORA_ERR_CUDA;
+    if (d && (!map_bf16(&mV_k, V, w.r8, M, 64, 128) || !map_bf16(&mA_mn, A, K, r, 64, 64) ||
+              !map_bf16(&mDX_sw, dX, K, M, 64, 128)))
+        return QLORA_ERR_CUDA;
 
     cudaError_t e;
+    if (d && (e = launch_dropout_x(X, M * K, d->seed, d->offset, d->p, Xd, mask, sms, st)) != cudaSuccess)
+        return from_cuda(e);
     if (!w.fp.small && (e = launch_dq_scales_t(W->scale_codes, W->scale_scales, W->scale_offset, N, (int)KB, scalesT,
                                                st)) != cudaSuccess)
         return from_cuda(e);
@@ -493,9 +523,12 @@ qlora_status qlora_linear_bwd(const qlora_nf4_tensor *W, const uint16_t *X, int6
     pv.out_h = V;
     pv.ld_h = w.r8;
     if ((e = launch_proj(false, true, mG_k, mB_mn, pv, st)) != cudaSuccess) return from_cuda(e);
-    // dX = G W^ + V A
-    const FusedArgs fa = fused_args(W, M, w, r, A, K, dX, mainp, K);
+    // dX = G W^ + V A  (under dropout: G W^, then += mask / (1 - p) * (V A))
+    FusedArgs fa = fused_args(W, M, w, r, A, K, dX, mainp, K);
+    if (d) fa.kt_lora = 0;
     if ((e = timed_fused(true, mCodes, mScales, mG_act, mV_act, mDX, fa, w.fp, sms, st)) != cudaSuccess)
+        return from_cuda(e);
+    if (d && (e = launch_dropout_dx(mV_k, mA_mn, mDX_sw, dX, mask, d->p, M, K, w.r8, sms, st)) != cudaSuccess)
         return from_cuda(e);
     // dA = V^T X  (D[k, j] = sum_m X[m, k] V[m, j], stored transposed)
     ProjArgs pa = proj_args(w.pda, K, w, r, 1, 1.0f);
@@ -506,6 +539,47 @@ qlora_status qlora_linear_bwd(const qlora_nf4_tensor *W, const uint16_t *X, int6
     pb.out_f = dB;
     if ((e = launch_proj(true, true, mG_mn, mU_mn, pb, st)) != cudaSuccess) return from_cuda(e);
     return QLORA_OK;
+}
+
+}  // namespace qlora
+
+extern "C" {
+
+qlora_status qlora_linear_fwd(const qlora_nf4_tensor *W, const uint16_t *X, int64_t M, const uint16_t *A,
+                              const uint16_t *B, int32_t r, float alpha, uint16_t *Y, uint16_t *U_save, void *ws,
+                              size_t ws_bytes, void *stream) {
+    return layer_fwd(W, X, M, A, B, r, alpha, nullptr, Y, U_save, ws, ws_bytes, stream);
+}
+
+qlora_status qlora_linear_bwd(const qlora_nf4_tensor *W, const uint16_t *X, int64_t M, const uint16_t *A,
+                              const uint16_t *B, int32_t r, float alpha, const uint16_t *dY, const uint16_t *U_saved,
+                              uint16_t *dX, float *dA, float *dB, void *ws, size_t ws_bytes, void *stream) {
+    return layer_bwd(W, X, M, A, B, r, alpha, nullptr, dY, U_saved, dX, dA, dB, ws, ws_bytes, stream);
+}
+
+size_t qlora_fwd_dropout_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t r) {
+    if (M < 1 || N < 1 || N % 8 != 0 || K < 64 || K % 64 != 0 || r < 1 || r > 256) return (size_t)-1;
+    return layer_ws(M, N, K, r, false, num_sms_current(), true).total;
+}
+
+size_t qlora_bwd_dropout_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t r) {
+    if (M < 1 || N < 1 || N % 8 != 0 || K < 64 || K % 64 != 0 || r < 1 || r > 256) return (size_t)-1;
+    return layer_ws(M, N, K, r, true, num_sms_current(), true).total;
+}
+
+qlora_status qlora_linear_fwd_dropout(const qlora_nf4_tensor *W, const uint16_t *X, int64_t M, const uint16_t *A,
+                                      const uint16_t *B, int32_t r, float alpha, const qlora_dropout *dropout,
+                                      uint16_t *Y, uint16_t *U_save, void *ws, size_t ws_bytes, void *stream) {
+    if (!dropout_ok(dropout)) return QLORA_ERR_INVALID_ARG;
+    return layer_fwd(W, X, M, A, B, r, alpha, dropout, Y, U_save, ws, ws_bytes, stream);
+}
+
+qlora_status qlora_linear_bwd_dropout(const qlora_nf4_tensor *W, const uint16_t *X, int64_t M, const uint16_t *A,
+                                      const uint16_t *B, int32_t r, float alpha, const qlora_dropout *dropout,
+                                      const uint16_t *dY, const uint16_t *U_saved, uint16_t *dX, float *dA, float *dB,
+                                      void *ws, size_t ws_bytes, void *stream) {
+    if (!dropout_ok(dropout)) return QLORA_ERR_INVALID_ARG;
+    return layer_bwd(W, X, M, A, B, r, alpha, dropout, dY, U_saved, dX, dA, dB, ws, ws_bytes, stream);
 }
 
 qlora_status qlora_set_kernel_timer(void **events, int32_t capacity) {

@@ -168,7 +168,10 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
                     umma_commit(&empty_c[sc]);
                 }
                 if (!ok) break;
-                umma_commit(&acc_full[a]);  // units have at least kSmallIssuers k-steps
+                // an issuer without a step in this unit still waits for the buffer's previous
+                // use to be drained, so that its arrival lands in this unit's phase
+                if (first && !mbar_wait(&acc_empty[a], ((lt >> 1) & 1) ^ 1u, s_abort)) { ok = false; break; }
+                umma_commit(&acc_full[a]);  // also without a step of its own in the unit (the epilogue knows)
             }
             if (!ok && any) {
                 umma_commit(&drain[me]);
@@ -180,9 +183,12 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
     } else if (warp < kSmallDecodeWarp0) {
         // ------------------------------ epilogue -----------------------------------------
         const int quarter = warp & 3;
-        int lt = 0;
+        int lt = 0, g0 = 0;
         for (int u = blockIdx.x; u < total_units; u += gridDim.x, ++lt) {
             const UnitInfo ui = unit_info(p, u);
+            // a unit of one k-step leaves the other issuer's accumulator unwritten
+            const bool has0 = ui.nk >= 2 || (g0 & 1) == 0, has1 = ui.nk >= 2 || (g0 & 1) == 1;
+            g0 += ui.nk;
             const int a = lt & 1;
             if (!warp_wait(&acc_full[a], (lt >> 1) & 1, s_abort)) break;
             tc_fence_after();
@@ -197,7 +203,8 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
                 tmem_ld_32x32b_x16(taddr + (uint32_t)(kBN + c * 16), r1);
                 tmem_ld_wait();
 #pragma unroll
-                for (int jj = 0; jj < 16; ++jj) acc[c * 16 + jj] = __fadd_rn(__uint_as_float(r0[jj]), __uint_as_float(r1[jj]));
+                for (int jj = 0; jj < 16; ++jj)
+                    acc[c * 16 + jj] = __fadd_rn(has0 ? __uint_as_float(r0[jj]) : 0.0f, has1 ? __uint_as_float(r1[jj]) : 0.0f);
             }
             tc_fence_before();
             __syncwarp();

@@ -4,6 +4,7 @@
 #include "gemm.cu"
 #include "gemm_small.cu"
 #include "gemv.cu"
+#include "dropout.cu"
 #include "merge.cu"
 #include "api.cu"
 #include "cat.cu"

@@ -1,4 +1,7 @@
-// merge.cu -- the adapter merged into the dequantized base weight:
+// merge.cu -- rank-r updates of a [rows, K] bf16 matrix on the tensor cores:
+//   mode 0 (the adapter merge) and mode 1 (the LoRA branch of dX under dropout, below).
+//
+// Mode 0, the adapter merged into the dequantized base weight:
 //   W_m[n, k] = bf16(W^[n, k] + s (B A)[n, k]),   s = alpha / r,
 // with W^ the bf16 dequantized NF4 weight (the nf4_dequantize values) and B A accumulated in fp32.
 // Source: "QLoRA" glossary (ultralytics), "Compromissos" and "QLoRA e metodos relacionados": to
@@ -14,6 +17,12 @@
 //     accumulator, decode the tile's codes with the per-block table (exact bf16 W^), form
 //     fma(s, acc, W^) in fp32, round to bf16, and store [128 rows][64 cols] tiles through
 //     128-byte-swizzled shared memory and TMA.
+//
+// Mode 1, the dropout backward (dropout.cu): dX[m, k] = bf16(dX0[m, k] + D[m, k] (V A)[m, k]) in
+// place, with dX0 the fused kernel's base term (dY W^), V = bf16(s dY B), and D = 1 / (1 - p) where
+// the adapter input element was kept, 0 where dropped (a bit mask from the forward's generator).
+// The same pipeline with V as the K-major operand; the epilogue reads dX0 from global memory and
+// the mask bits instead of decoding codes.
 #include "qlora_common.cuh"
 #include "qlora_kernels.cuh"
 
@@ -29,7 +38,7 @@ static constexpr uint32_t kMrgOutBytes = 128u * 128u;      // 128 rows x 64 bf16
 static constexpr uint32_t kMrgSmem = 2 * kMrgOpBytes + 2 * kMrgCodesBytes + 4 * kMrgOutBytes + 256;
 
 struct MergeArgs {
-    int64_t N, K;
+    int64_t N, K;               // rows (weight rows, or tokens in mode 1), columns
     int32_t KB;                 // K / 64
     int32_t n_tiles, k_tiles;   // 128-row and 256-column tiles
     int32_t rc;                 // 64-wide chunks of the rank
@@ -38,8 +47,18 @@ struct MergeArgs {
     const float *scale_c2;
     const float *scale_mu;
     NF4Tables tab;
+    const uint32_t *mask_bits;  // mode 1: [N * K / 32] kept-element bits
+    float inv;                  // mode 1: 1 / (1 - p)
+    const uint16_t *base;       // mode 1: dX0 [N, K] bf16 (the output, updated in place)
 };
 
+__device__ __forceinline__ uint4 ld_global_v4(const uint4 *ptr) {
+    uint4 v;
+    asm volatile("ld.global.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(ptr));
+    return v;
+}
+
+template <int kMode>
 __global__ void __launch_bounds__(kMrgThreads, 1)
     nf4_merge_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant__ CUtensorMap map_b,
                      const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_out,
@@ -102,11 +121,13 @@ __global__ void __launch_bounds__(kMrgThreads, 1)
             for (int u = blockIdx.x; u < total && ok; u += gridDim.x, ++lt) {
                 const int n0 = (u / p.k_tiles) * 128, k0 = (u % p.k_tiles) * 256;
                 const int cb = lt & 1;
-                if (!mbar_wait(&codes_empty[cb], ((lt >> 1) & 1) ^ 1u, s_abort)) { ok = false; break; }
-                mbar_arrive_expect_tx(&codes_full[cb], kMrgCodesBytes);
-                tma_load_2d(sCodes + cb * kMrgCodesBytes, &map_codes, &codes_full[cb], k0 / 2, n0);
-                codes_issued[cb] = true;
-                codes_par[cb] = (lt >> 1) & 1;
+                if (kMode == 0) {
+                    if (!mbar_wait(&codes_empty[cb], ((lt >> 1) & 1) ^ 1u, s_abort)) { ok = false; break; }
+                    mbar_arrive_expect_tx(&codes_full[cb], kMrgCodesBytes);
+                    tma_load_2d(sCodes + cb * kMrgCodesBytes, &map_codes, &codes_full[cb], k0 / 2, n0);
+                    codes_issued[cb] = true;
+                    codes_par[cb] = (lt >> 1) & 1;
+                }
                 for (int c = 0; c < p.rc; ++c, ++gc) {
                     const int sl = gc & 1;
                     if (!mbar_wait(&op_empty[sl], ((gc >> 1) & 1) ^ 1u, s_abort)) { ok = false; break; }
@@ -187,15 +208,32 @@ __global__ void __launch_bounds__(kMrgThreads, 1)
 #pragma unroll
             for (int g = 0; g < 2; ++g) {
                 const int64_t kb = (k0 + half * 128 + g * 64) / 64;
-                if (n < p.N && kb < p.KB) {
+                if (kMode == 0 && n < p.N && kb < p.KB) {
                     const int64_t b = n * p.KB + kb;
                     sc[g] = __fmaf_rn((float)__ldg(p.scale_q + b), __fdiv_rn(__ldg(p.scale_c2 + (b >> 8)), 127.0f), mu);
                 }
             }
             // one outcome per half: its four warps meet at named barriers below
+            // mode 1: this thread's base values and mask words, requested before the waits
+            uint4 bv[2][2][4];
+            uint32_t mw[2][2];
+            if (kMode == 1) {
+#pragma unroll
+                for (int g = 0; g < 2; ++g)
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        const int64_t kk = (int64_t)k0 + half * 128 + g * 64 + c * 32;
+                        const bool in = n < p.N && kk < p.K;
+                        const uint4 *src = reinterpret_cast<const uint4 *>(p.base + n * p.K + kk);
+                        // a plain (coherent) load: this kernel rewrites these elements afterwards
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) bv[g][c][i] = in ? ld_global_v4(src + i) : make_uint4(0, 0, 0, 0);
+                        mw[g][c] = in ? __ldg(p.mask_bits + (n * p.K + kk) / 32) : 0u;
+                    }
+            }
             if (et == 0)
                 s_ok[half] = (mbar_wait(&acc_full[a], (lt >> 1) & 1, s_abort) &&
-                              mbar_wait(&codes_full[a], (lt >> 1) & 1, s_abort)) ? 1u : 0u;
+                              (kMode == 1 || mbar_wait(&codes_full[a], (lt >> 1) & 1, s_abort))) ? 1u : 0u;
             named_barrier_sync(3 + half, 128);
             const uint32_t okw = s_ok[half];
             named_barrier_sync(3 + half, 128);
@@ -204,7 +242,7 @@ __global__ void __launch_bounds__(kMrgThreads, 1)
             const uint8_t *crow = sCodes + a * kMrgCodesBytes + row * 128 + half * 64;
             for (int g = 0; g < 2; ++g, ++store_n) {
                 uint32_t lo[4], hi[4];
-                build_table(sc[g], p.tab, lo, hi);
+                if (kMode == 0) build_table(sc[g], p.tab, lo, hi);
                 uint8_t *buf = sOut + (half * 2 + (store_n & 1)) * kMrgOutBytes;
                 if (et == 0) bulk_wait_group_read<1>();  // the store two groups back has read buf
                 named_barrier_sync(1 + half, 128);
@@ -215,18 +253,28 @@ __global__ void __launch_bounds__(kMrgThreads, 1)
                                            (uint32_t)(half * 128 + g * 64 + c * 32),
                                        r);
                     tmem_ld_wait();
-                    const uint4 cw = *reinterpret_cast<const uint4 *>(crow + g * 32 + c * 16);  // 32 codes
-                    const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+                    uint32_t words[4];
+                    if (kMode == 0) {
+                        const uint4 cw = *reinterpret_cast<const uint4 *>(crow + g * 32 + c * 16);  // 32 codes
+                        words[0] = cw.x; words[1] = cw.y; words[2] = cw.z; words[3] = cw.w;
+                    }
 #pragma unroll
                     for (int w = 0; w < 4; ++w) {
-                        const uint4 d = decode8(words[w], lo, hi);  // 8 bf16 of W^ as pairs
+                        // 8 bf16 base values as pairs: W^ decoded (mode 0) or dX0 (mode 1)
+                        const uint4 d = kMode == 0 ? decode8(words[w], lo, hi) : bv[g][c][w];
                         const uint32_t dw[4] = {d.x, d.y, d.z, d.w};
                         uint32_t o[4];
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const float w0 = __uint_as_float(dw[e] << 16), w1 = __uint_as_float(dw[e] & 0xffff0000u);
-                            const float t0 = __fmaf_rn(p.s, __uint_as_float(r[8 * w + 2 * e]), w0);
-                            const float t1 = __fmaf_rn(p.s, __uint_as_float(r[8 * w + 2 * e + 1]), w1);
+                            float f0 = p.s, f1 = p.s;
+                            if (kMode == 1) {
+                                const int bit = 8 * w + 2 * e;  // element within the 32-column chunk
+                                f0 = (mw[g][c] >> bit) & 1u ? p.inv : 0.0f;
+                                f1 = (mw[g][c] >> (bit + 1)) & 1u ? p.inv : 0.0f;
+                            }
+                            const float t0 = __fmaf_rn(f0, __uint_as_float(r[8 * w + 2 * e]), w0);
+                            const float t1 = __fmaf_rn(f1, __uint_as_float(r[8 * w + 2 * e + 1]), w1);
                             o[e] = bf16x2(t0, t1);
                         }
                         // 16-byte chunk (4 c + w) of this row's 128 bytes, 128-byte swizzle
@@ -246,7 +294,7 @@ __global__ void __launch_bounds__(kMrgThreads, 1)
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(&acc_empty[a]);
-                mbar_arrive(&codes_empty[a]);
+                if (kMode == 0) mbar_arrive(&codes_empty[a]);
             }
         }
         if (et == 0) bulk_wait_group_all();
@@ -260,29 +308,47 @@ __global__ void __launch_bounds__(kMrgThreads, 1)
     }
 }
 
-cudaError_t launch_merge(const CUtensorMap &map_codes, const CUtensorMap &map_b, const CUtensorMap &map_a,
-                         const CUtensorMap &map_out, const int8_t *scale_q, const float *scale_c2,
-                         const float *scale_mu, int64_t N, int64_t K, int r, float s, const NF4Tables &tab,
-                         int num_sms, cudaStream_t st) {
-    MergeArgs p{};
+template <int kMode>
+static cudaError_t launch_rank_update(const CUtensorMap &map_codes, const CUtensorMap &map_b, const CUtensorMap &map_a,
+                                      const CUtensorMap &map_out, MergeArgs p, int64_t N, int64_t K, int r, int num_sms,
+                                      cudaStream_t st) {
     p.N = N;
     p.K = K;
     p.KB = (int32_t)(K / 64);
     p.n_tiles = (int32_t)((N + 127) / 128);
     p.k_tiles = (int32_t)((K + 255) / 256);
     p.rc = (r + 63) / 64;
+    cudaError_t e = cudaFuncSetAttribute(nf4_merge_kernel<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kMrgSmem);
+    if (e != cudaSuccess) return e;
+    const int64_t units = (int64_t)p.n_tiles * p.k_tiles;
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(units, num_sms));
+    nf4_merge_kernel<kMode><<<grid, kMrgThreads, kMrgSmem, st>>>(map_codes, map_b, map_a, map_out, p);
+    count_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t launch_merge(const CUtensorMap &map_codes, const CUtensorMap &map_b, const CUtensorMap &map_a,
+                         const CUtensorMap &map_out, const int8_t *scale_q, const float *scale_c2,
+                         const float *scale_mu, int64_t N, int64_t K, int r, float s, const NF4Tables &tab,
+                         int num_sms, cudaStream_t st) {
+    MergeArgs p{};
     p.s = s;
     p.scale_q = scale_q;
     p.scale_c2 = scale_c2;
     p.scale_mu = scale_mu;
     p.tab = tab;
-    cudaError_t e = cudaFuncSetAttribute(nf4_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMrgSmem);
-    if (e != cudaSuccess) return e;
-    const int64_t units = (int64_t)p.n_tiles * p.k_tiles;
-    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(units, num_sms));
-    nf4_merge_kernel<<<grid, kMrgThreads, kMrgSmem, st>>>(map_codes, map_b, map_a, map_out, p);
-    count_launch();
-    return cudaGetLastError();
+    return launch_rank_update<0>(map_codes, map_b, map_a, map_out, p, N, K, r, num_sms, st);
+}
+
+cudaError_t launch_dropout_dx(const CUtensorMap &map_v, const CUtensorMap &map_a, const CUtensorMap &map_dx,
+                              const uint16_t *dx0, const uint32_t *mask_bits, float p_drop, int64_t M, int64_t K,
+                              int r, int num_sms, cudaStream_t st) {
+    MergeArgs p{};
+    p.inv = 1.0f / (1.0f - p_drop);
+    p.mask_bits = mask_bits;
+    p.base = dx0;
+    return launch_rank_update<1>(map_v /* unused codes map */, map_v, map_a, map_dx, p, M, K, r, num_sms, st);
 }
 
 }  // namespace qlora

@@ -123,6 +123,18 @@ cudaError_t launch_merge(const CUtensorMap &map_codes, const CUtensorMap &map_b,
                          const float *scale_mu, int64_t N, int64_t K, int r, float s, const NF4Tables &tab,
                          int num_sms, cudaStream_t st);
 
+// ---- LoRA dropout on the adapter input (dropout.cu, merge.cu) ----------------------------
+// Xd[e] = bf16(X[e] / (1 - p)) where kept, else 0 (Philox4x32-10 of (seed, offset, e)), for
+// e < n (n % 64 == 0); mask_bits (nullable) [n / 32]: bit e % 32 of word e / 32 = kept.
+cudaError_t launch_dropout_x(const uint16_t *X, int64_t n, uint64_t seed, uint64_t offset, float p, uint16_t *Xd,
+                             uint32_t *mask_bits, int num_sms, cudaStream_t st);
+// dX[m, k] = bf16(dX0[m, k] + kept(m, k) / (1 - p) * (V A)[m, k]) in place (dx0 = the dX buffer);
+// map_v: V [M, rv] bf16, box {64, 128}, 128-byte swizzle; map_a: A [r, K] bf16, box {64, 64},
+// 128-byte swizzle; map_dx: dX [M, K] bf16, box {64, 128}, 128-byte swizzle; r = rv.
+cudaError_t launch_dropout_dx(const CUtensorMap &map_v, const CUtensorMap &map_a, const CUtensorMap &map_dx,
+                              const uint16_t *dx0, const uint32_t *mask_bits, float p_drop, int64_t M, int64_t K,
+                              int r, int num_sms, cudaStream_t st);
+
 // dst[rows_dst, cols_dst] = src[rows_src, cols_src] where both indices are in range, else 0
 cudaError_t launch_pad_2d(const uint16_t *src, int64_t rows_src, int64_t cols_src, uint16_t *dst, int64_t rows_dst,
                           int64_t cols_dst, int num_sms, cudaStream_t st);

@@ -113,6 +113,33 @@ qlora_status nf4_quantize_noalloc(const float *W, const qlora_nf4_tensor *out, v
  * absmax; glossary: dequantized to bfloat16 before the matmul).  No workspace. */
 qlora_status nf4_dequantize(const qlora_nf4_tensor *q, uint16_t *W_out, void *stream);
 
+/* ---- LoRA dropout on the adapter input ----------------------------------------------------
+ * ("LoRA y QLoRA para un ajuste eficiente en costes", coddykit: LoraConfig lora_dropout=0.05.)
+ * The adapter branch sees x_d = x * mask / (1 - p), mask ~ Bernoulli(1 - p) per element of X:
+ *   Y = X W^T + s (X_d A^T) B^T;  dX = dY W^ + mask/(1-p) * (V A), V = bf16(s dY B);
+ *   dA = V^T X_d;  dB = dY^T U,  U = bf16(s X_d A^T).
+ * The mask is drawn from Philox4x32-10 (Salmon et al., SC'11): element e of the row-major [M, K]
+ * X takes word e % 4 of the block with counter (e / 4 as two 32-bit words, offset as two 32-bit
+ * words) and key (seed as two 32-bit words), and is kept when the word is >= floor(p 2^32).  The
+ * backward call with the same (p, seed, offset) regenerates the forward's mask.  X_d is rounded
+ * to bf16 (bf16(x * fl32(1 / (1 - p)))) before the adapter products.  0 <= p < 1; p = 0 keeps
+ * every element (the plain layer, through the dropout code path). */
+typedef struct {
+    float p;
+    uint64_t seed;
+    uint64_t offset;
+} qlora_dropout;
+
+size_t qlora_fwd_dropout_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t r);
+size_t qlora_bwd_dropout_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t r);
+qlora_status qlora_linear_fwd_dropout(const qlora_nf4_tensor *W, const uint16_t *X, int64_t M, const uint16_t *A,
+                                      const uint16_t *B, int32_t r, float alpha, const qlora_dropout *dropout,
+                                      uint16_t *Y, uint16_t *U_save, void *ws, size_t ws_bytes, void *stream);
+qlora_status qlora_linear_bwd_dropout(const qlora_nf4_tensor *W, const uint16_t *X, int64_t M, const uint16_t *A,
+                                      const uint16_t *B, int32_t r, float alpha, const qlora_dropout *dropout,
+                                      const uint16_t *dY, const uint16_t *U_saved, uint16_t *dX, float *dA, float *dB,
+                                      void *ws, size_t ws_bytes, void *stream);
+
 /* ---- Concatenated projections sharing one input ----------------------------------------
  * Several modules applied to the same X (q/k/v, or gate/up, with "all-linear" adapters: coddykit
  * "Módulos objetivo" and the config's target_modules) computed as one N-concatenated layer, so

@@ -61,6 +61,9 @@ def test_workspace_queries(L):
         scales = (K // 64) * N * 4 if M > 32 else 0
         assert f >= scales + M * r8 * 2
         assert b >= scales + 2 * M * r8 * 2
+    # dropout: the masked input (and, backward, its bits) on top of the plain layer's workspace
+    assert L.qlora_fwd_dropout_workspace_bytes(64, 256, 512, 8) >= L.qlora_fwd_workspace_bytes(64, 256, 512, 8) + 64 * 512 * 2
+    assert L.qlora_bwd_dropout_workspace_bytes(64, 256, 512, 8) >= L.qlora_bwd_workspace_bytes(64, 256, 512, 8) + 64 * 512 * 2
     assert L.qlora_merge_workspace_bytes(4096, 4096, 16) == 0     # B used in place
     assert L.qlora_merge_workspace_bytes(4096, 4096, 5) >= 4096 * 8 * 2
     assert L.qlora_merge_workspace_bytes(4096, 100, 16) == bad
@@ -118,6 +121,14 @@ def test_argument_errors_before_any_launch(L):
     assert L.qlora_merge(ctypes.byref(t), A, P(0x3002), 8, 16.0, Wo, None, 0, None) == 3
     assert L.qlora_merge(ctypes.byref(t), A, B, 5, 16.0, Wo, None, 0, None) == 4
     assert L.qlora_merge(ctypes.byref(t), A, B, 5, 16.0, Wo, ws, 64, None) == 4
+    # dropout: probability outside [0, 1), missing options
+    d_bad = _lib.DropoutStruct(1.0, 1, 0)
+    assert L.qlora_linear_fwd_dropout(ctypes.byref(t), X, 16, A, B, 8, 16.0, ctypes.byref(d_bad), Y, None, ws,
+                                      1 << 30, None) == 1
+    assert L.qlora_linear_fwd_dropout(ctypes.byref(t), X, 16, A, B, 8, 16.0, None, Y, None, ws, 1 << 30, None) == 1
+    d_nan = _lib.DropoutStruct(float("nan"), 1, 0)
+    assert L.qlora_linear_bwd_dropout(ctypes.byref(t), X, 16, A, B, 8, 16.0, ctypes.byref(d_nan), P(0x8000), None,
+                                      P(0x5000), P(0x6000), P(0x7000), ws, 1 << 30, None) == 1
     assert L.qlora_launch_count() == 0  # nothing above reached a kernel launch
 
 
