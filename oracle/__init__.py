@@ -78,6 +78,7 @@ def _declare(L):
     L.orc_bf16_round_d.restype = ctypes.c_uint16
     L.orc_merge.argtypes = [_P, _P, _P, _I64, _I64, _I64, _D, _P]
     L.orc_philox4x32_10.argtypes = [_P, _P, _P]
+    L.orc_adamw_step.argtypes = [_P, _P, _P, _P, _I64, _D, _D, _D, _D, _D, _I64]
     L.orc_dropout_scale.argtypes = [ctypes.c_uint64, ctypes.c_uint64, _D, _I64, _P]
     L.orc_layer_fwd_rows_drop.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _I64, _D, _P, _P, _I64, _P, _P]
     L.orc_layer_dx_rows_drop.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _I64, _D, _P, _P, _I64, _P]
@@ -342,3 +343,11 @@ def layer_adapter_grads_drop(X, A, B, G, alpha: float, D):
     lib().orc_layer_adapter_grads_drop(_ptr(X), _ptr(A), _ptr(B), _ptr(G), M, N, K, r, float(alpha), _ptr(D),
                                        _ptr(dA), _ptr(dB))
     return dA, dB
+
+
+def adamw_step(p, g, m, v, lr: float, b1: float, b2: float, eps: float, wd: float, t: int):
+    """One AdamW step in fp64: returns new (p, m, v)."""
+    p, g, m, v = (np.array(a, dtype=np.float64).ravel().copy() for a in (p, g, m, v))
+    lib().orc_adamw_step(_ptr(p), _ptr(g), _ptr(m), _ptr(v), p.size, float(lr), float(b1), float(b2), float(eps),
+                         float(wd), int(t))
+    return p, m, v

@@ -685,3 +685,26 @@ void orc_layer_adapter_grads_drop(const uint16_t *X, const uint16_t *A, const ui
     free(U);
     free(V);
 }
+
+/* ------------------------------------------------------------------------------------ */
+/* The adapters' optimizer step.  Only the two LoRA matrices are updated [QLoRA-ultralytics,   */
+/* "Como funciona a QLoRA"]; their optimizer states are paged: kept in NVIDIA unified memory  */
+/* and moved to CPU RAM under memory pressure [QLoRA-ultralytics, "Otimizadores paginados"    */
+/* bullet; QLoRA-skillverse, "Componentes clave", "Optimizadores paginados"].  READING: the    */
+/* pages name no update rule; the optimizer is AdamW (decoupled weight decay, Loshchilov and  */
+/* Hutter, ICLR 2019), step t >= 1:                                                           */
+/*   p <- p (1 - lr wd);  m <- b1 m + (1 - b1) g;  v <- b2 v + (1 - b2) g^2;                   */
+/*   p <- p - lr (m / (1 - b1^t)) / (sqrt(v / (1 - b2^t)) + eps).                            */
+/* In fp64 on fp32 inputs; the caller rounds.                                              */
+/* ------------------------------------------------------------------------------------ */
+void orc_adamw_step(double *p, const double *g, double *m, double *v, int64_t n, double lr, double b1, double b2,
+                    double eps, double wd, int64_t t)
+{
+    double bc1 = 1.0 - pow(b1, (double)t), bc2 = 1.0 - pow(b2, (double)t);
+    for (int64_t i = 0; i < n; ++i) {
+        p[i] *= 1.0 - lr * wd;
+        m[i] = b1 * m[i] + (1.0 - b1) * g[i];
+        v[i] = b2 * v[i] + (1.0 - b2) * g[i] * g[i];
+        p[i] -= lr * (m[i] / bc1) / (sqrt(v[i] / bc2) + eps);
+    }
+}

@@ -559,3 +559,35 @@ def test_dropout_grads_finite_differences(orc):
         E = np.zeros_like(Xf)
         E[m, k] = h
         assert dX[m, k] == pytest.approx((loss(Xf + E, Af, Bf) - loss(Xf - E, Af, Bf)) / (2 * h), rel=1e-7, abs=1e-9)
+
+
+# ---------------------------------------------------------------------------------------
+# The adapters' optimizer step (AdamW; paged optimizer states, "Otimizadores paginados").
+# ---------------------------------------------------------------------------------------
+
+def test_adamw_matches_torch_adamw(orc):
+    """torch.optim.AdamW (an independent implementation), in fp64, over 5 steps."""
+    rng = np.random.default_rng(31)
+    n = 257
+    p0 = rng.standard_normal(n)
+    grads = [rng.standard_normal(n) * 0.1 for _ in range(5)]
+    hp = dict(lr=2e-4, b1=0.9, b2=0.999, eps=1e-8, wd=0.01)
+    tp = torch.nn.Parameter(torch.tensor(p0, dtype=torch.float64))
+    opt = torch.optim.AdamW([tp], lr=hp["lr"], betas=(hp["b1"], hp["b2"]), eps=hp["eps"], weight_decay=hp["wd"])
+    p, m, v = p0.copy(), np.zeros(n), np.zeros(n)
+    for t, g in enumerate(grads, start=1):
+        tp.grad = torch.tensor(g, dtype=torch.float64)
+        opt.step()
+        p, m, v = orc.adamw_step(p, g, m, v, hp["lr"], hp["b1"], hp["b2"], hp["eps"], hp["wd"], t)
+        np.testing.assert_allclose(p, tp.detach().numpy(), rtol=1e-14, atol=1e-16)
+
+
+def test_adamw_first_step_is_a_sign_step(orc):
+    """t = 1 from zero moments: m^ = g, v^ = g^2, so the step is lr g / (|g| + eps)."""
+    g = np.array([0.5, -2.0, 1e-3, -7.0])
+    p0 = np.array([1.0, -1.0, 0.25, 3.0])
+    lr, wd, eps = 1e-2, 0.1, 1e-8
+    p, m, v = orc.adamw_step(p0, g, np.zeros(4), np.zeros(4), lr, 0.9, 0.999, eps, wd, 1)
+    np.testing.assert_allclose(p, p0 * (1 - lr * wd) - lr * g / (np.abs(g) + eps), rtol=1e-12)
+    np.testing.assert_allclose(m, 0.1 * g, rtol=1e-15)
+    np.testing.assert_allclose(v, 0.001 * g * g, rtol=1e-12)
