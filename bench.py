@@ -391,6 +391,10 @@ def run_ours(args):
             extras["dropout_attn"] = dropout_extras(q, dev, flush, inp)
         except Exception as e:
             extras["dropout_attn"] = {"error": repr(e)}
+        try:
+            extras["paged_adamw"] = optim_extras(q, dev, peaks, flush)
+        except Exception as e:
+            extras["paged_adamw"] = {"error": repr(e)}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -450,6 +454,56 @@ def dropout_extras(q, dev, flush, inp, reps=10):
 
     t0, t1 = timed(plain), timed(drop)
     return {"p": 0.05, "plain_fwd_bwd_ms": t0, "dropout_fwd_bwd_ms": t1, "overhead": t1 / t0 - 1.0}
+
+
+def optim_extras(q, dev, peaks, flush, reps=10):
+    """The adapters' AdamW step with paged optimizer states, over every adapter of Llama-3-8B
+    (rank 16 on all seven linear layers of 32 blocks: 41.9 M weights) in one launch: the step
+    with the pages resident (reads p, g, m, v and writes p, m, v and the bf16 copy: 30 bytes per
+    weight), paging the two fp32 moment buffers out to host memory and back in, and a step that
+    finds its moments on the host and faults them in."""
+    import torch
+    from bit_nf4_quantized_36_b300 import synth
+    n = synth.adapter_param_count()
+    p, g, m0, v0 = synth.adamw_inputs_gpu(synth.LLAMA8B_ADAPTERS["id"], n, dev)
+    opt = q.PagedAdamW(n)
+    opt.m.tensor(torch.float32, n).copy_(m0)
+    opt.v.tensor(torch.float32, n).copy_(v0)
+    del m0, v0
+    pb = torch.empty(n, dtype=torch.bfloat16, device=dev)
+    opt.page_in()
+    opt.step(p, g, pb)
+    torch.cuda.synchronize()
+
+    def ev(fn):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b)
+
+    res = []
+    for _ in range(reps):
+        flush.zero_()
+        res.append(ev(lambda: opt.step(p, g, pb)))
+    t_res = statistics.median(res)
+    t_out, t_in, t_fault = [], [], []
+    for _ in range(3):
+        t_out.append(ev(opt.page_out))
+        t_fault.append(ev(lambda: opt.step(p, g, pb)))     # moments on the host: migrated on demand
+        opt.page_out()
+        torch.cuda.synchronize()
+        t_in.append(ev(opt.page_in))
+    q.check_device_error()
+    byt = 30 * n
+    state = 8 * n
+    return {"workload": synth.LLAMA8B_ADAPTERS["name"], "n": n, "kernel": "adamw_kernel",
+            "step_ms_resident": t_res, "GB/s": byt / t_res / 1e6, "frac_hbm": byt / t_res / 1e6 / peaks["hbm_gbs"],
+            "algorithmic_bytes": byt, "moment_bytes": state,
+            "page_out_ms": statistics.median(t_out), "page_in_ms": statistics.median(t_in),
+            "page_in_GB/s": state / statistics.median(t_in) / 1e6,
+            "step_ms_faulting": statistics.median(t_fault)}
 
 
 def concat_extras(q, dev, flush, reps=10):
@@ -576,13 +630,24 @@ def hbm_extras(q, _lib, L, dev, peaks, flush):
 
 def run_ncu_target(args):
     """A short, untimed run for profiler captures: three forward+backward passes of the layer on the
-    bench workload (--ncu-target fused) or three small-M forwards on a 70B MLP matrix
-    (--ncu-target decode)."""
+    bench workload (--ncu-target fused), three small-M forwards on a 70B MLP matrix
+    (--ncu-target decode), or three AdamW steps over the Llama-3-8B adapter set with the moments
+    in plain device memory (--ncu-target adamw; the same kernel as with paged moments)."""
     import torch
 
     import bit_nf4_quantized_36_b300 as q
     from bit_nf4_quantized_36_b300 import synth
     dev = torch.device("cuda")
+    if args.ncu_target == "adamw":
+        n = synth.adapter_param_count()
+        p, g, m, v = synth.adamw_inputs_gpu(synth.LLAMA8B_ADAPTERS["id"], n, dev)
+        pb = torch.empty(n, dtype=torch.bfloat16, device=dev)
+        for t in range(1, 4):
+            q.adamw_step(p, g, m, v, t, 2e-4, p_bf16=pb)
+        torch.cuda.synchronize()
+        q.check_device_error()
+        print(json.dumps({"ncu_target": "adamw", "n": n, "ok": True}))
+        return 0
     if args.ncu_target == "fused":
         c = synth.LLAMA8B_ATTN
         M, N, K, r, alpha = c["M"], c["N"], c["K"], c["r"], c["alpha"]
@@ -614,7 +679,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true")
-    ap.add_argument("--ncu-target", choices=["fused", "decode"], default=None,
+    ap.add_argument("--ncu-target", choices=["fused", "decode", "adamw"], default=None,
                     help="untimed short run of one kernel family, for profiler captures")
     ap.add_argument("--decode-m", type=int, default=1)
     args = ap.parse_args()

@@ -21,7 +21,7 @@ from . import _lib
 __all__ = ["NF4Weight", "QLoRAError", "nf4_quantize", "nf4_quantize_noalloc", "nf4_dequantize", "qlora_linear_fwd", "qlora_linear_bwd",
            "qlora_merge", "qlora_linear_fwd_cat", "qlora_linear_bwd_cat", "qlora_linear_fwd_dropout",
            "qlora_linear_bwd_dropout", "nf4_storage_bytes", "quantize_workspace_bytes", "fwd_workspace_bytes", "bwd_workspace_bytes",
-           "merge_workspace_bytes",
+           "merge_workspace_bytes", "PagedBuffer", "PagedAdamW", "adamw_step",
            "check_device_error", "launch_count", "nf4_levels", "empty_nf4"]
 
 
@@ -376,6 +376,128 @@ def qlora_linear_bwd_cat(modules, X: torch.Tensor, dY: torch.Tensor, U_saved: to
                                   _ptr(dX), ctypes.cast(pa, ctypes.c_void_p), ctypes.cast(pb, ctypes.c_void_p),
                                   _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)), "qlora_linear_bwd_cat")
     return dX, dA, dB
+
+
+class PagedBuffer:
+    """Unified (managed) memory from qlora_paged_alloc, for optimizer states that page to host RAM
+    when GPU memory runs short.  Freed when the object and every tensor view of it are gone."""
+
+    def __init__(self, nbytes: int):
+        out = ctypes.c_void_p()
+        _check(_lib.load().qlora_paged_alloc(int(nbytes), ctypes.byref(out)), "qlora_paged_alloc")
+        self.ptr = int(out.value)
+        self.nbytes = int(nbytes)
+
+    def free(self) -> None:
+        if self.ptr:
+            _check(_lib.load().qlora_paged_free(ctypes.c_void_p(self.ptr)), "qlora_paged_free")
+            self.ptr = 0
+
+    def __del__(self):
+        try:
+            self.free()
+        except Exception:
+            pass
+
+    def prefetch(self, where="cuda", offset: int = 0, nbytes: int | None = None, stream=None) -> None:
+        """Move the pages of [offset, offset + nbytes) to a device ("cuda", "cuda:i", an ordinal or a
+        torch.device) or to host memory ("cpu"), asynchronously on `stream`."""
+        nbytes = self.nbytes - offset if nbytes is None else nbytes
+        if offset < 0 or nbytes < 0 or offset + nbytes > self.nbytes:
+            raise ValueError("prefetch range outside the buffer")
+        if where == "cpu":
+            dev = _lib.QLORA_PAGE_HOST
+        elif isinstance(where, int):
+            dev = where
+        else:
+            d = torch.device(where)
+            dev = d.index if d.index is not None else torch.cuda.current_device()
+        _check(_lib.load().qlora_paged_prefetch(ctypes.c_void_p(self.ptr + offset), nbytes, dev, _stream(stream)),
+               "qlora_paged_prefetch")
+
+    def zero_(self) -> "PagedBuffer":
+        """Zero-fill from the host (places untouched pages in host memory)."""
+        ctypes.memset(self.ptr, 0, self.nbytes)
+        return self
+
+    def host_view(self, count: int | None = None, offset: int = 0, ctype=ctypes.c_float):
+        """A host ctypes array over the buffer; valid to read only with no kernel in flight on it."""
+        count = (self.nbytes - offset) // ctypes.sizeof(ctype) if count is None else count
+        return (ctype * count).from_address(self.ptr + offset)
+
+    def tensor(self, dtype=torch.float32, count: int | None = None, offset: int = 0) -> torch.Tensor:
+        """A zero-copy 1-D CUDA tensor over the buffer (keeps the buffer alive)."""
+        es = torch.empty((), dtype=dtype).element_size()
+        count = (self.nbytes - offset) // es if count is None else count
+        if offset < 0 or offset % es or offset + count * es > self.nbytes:
+            raise ValueError("view outside the buffer")
+        # bf16 has no array-interface type string: view 16-bit integers as bf16
+        typestr = {torch.float32: "<f4", torch.bfloat16: "<i2", torch.int32: "<i4", torch.uint8: "|u1"}[dtype]
+        buf = self
+
+        class _View:
+            __cuda_array_interface__ = {"shape": (count,), "typestr": typestr, "data": (self.ptr + offset, False),
+                                        "version": 3, "strides": None}
+            owner = buf
+
+        t = torch.as_tensor(_View(), device=f"cuda:{torch.cuda.current_device()}")
+        return t.view(torch.bfloat16) if dtype == torch.bfloat16 else t
+
+
+def _f32_addr(x, n: int | None, name: str) -> tuple[int, int]:
+    """(address, elements) of an fp32 array given as a CUDA tensor or a PagedBuffer."""
+    if isinstance(x, PagedBuffer):
+        cnt = x.nbytes // 4
+        if n is not None and cnt < n:
+            raise ValueError(f"{name}: paged buffer holds {cnt} fp32 elements, need {n}")
+        return x.ptr, cnt if n is None else n
+    _need(x, torch.float32, name)
+    if n is not None and x.numel() != n:
+        raise ValueError(f"{name} has {x.numel()} elements, expected {n}")
+    return x.data_ptr(), x.numel()
+
+
+def adamw_step(p, g, m, v, t: int, lr: float, betas=(0.9, 0.999), eps: float = 1e-8, weight_decay: float = 0.0,
+               p_bf16: torch.Tensor | None = None, stream=None) -> None:
+    """One AdamW step (qlora_adamw_step) on flat fp32 arrays: p, m, v updated in place, g read;
+    p_bf16 (optional bf16 tensor) receives bf16(p).  Each array is a CUDA tensor or a PagedBuffer."""
+    pa, n = _f32_addr(p, None, "p")
+    ga, _ = _f32_addr(g, n, "g")
+    ma, _ = _f32_addr(m, n, "m")
+    va, _ = _f32_addr(v, n, "v")
+    if p_bf16 is not None:
+        _need(p_bf16, torch.bfloat16, "p_bf16")
+        if p_bf16.numel() != n:
+            raise ValueError(f"p_bf16 has {p_bf16.numel()} elements, expected {n}")
+    hp = _lib.AdamWStruct(lr, betas[0], betas[1], eps, weight_decay)
+    _check(_lib.load().qlora_adamw_step(ctypes.byref(hp), int(t), n, ctypes.c_void_p(pa), ctypes.c_void_p(ga),
+                                        ctypes.c_void_p(ma), ctypes.c_void_p(va), _ptr(p_bf16), _stream(stream)),
+           "qlora_adamw_step")
+
+
+class PagedAdamW:
+    """AdamW for the adapters with paged optimizer states: m and v (fp32, n each) live in unified
+    memory.  page_out() moves them to host RAM before a memory spike, page_in() brings them back
+    before the next step; step() is correct wherever the pages are."""
+
+    def __init__(self, n: int, lr: float = 2e-4, betas=(0.9, 0.999), eps: float = 1e-8,
+                 weight_decay: float = 0.0):
+        self.n, self.lr, self.betas, self.eps, self.weight_decay = int(n), lr, betas, eps, weight_decay
+        self.m = PagedBuffer(4 * self.n).zero_()
+        self.v = PagedBuffer(4 * self.n).zero_()
+        self.t = 0
+
+    def page_out(self, stream=None) -> None:
+        self.m.prefetch("cpu", stream=stream)
+        self.v.prefetch("cpu", stream=stream)
+
+    def page_in(self, device="cuda", stream=None) -> None:
+        self.m.prefetch(device, stream=stream)
+        self.v.prefetch(device, stream=stream)
+
+    def step(self, p, g, p_bf16: torch.Tensor | None = None, stream=None) -> None:
+        self.t += 1
+        adamw_step(p, g, self.m, self.v, self.t, self.lr, self.betas, self.eps, self.weight_decay, p_bf16, stream)
 
 
 def check_device_error(stream=None) -> None:

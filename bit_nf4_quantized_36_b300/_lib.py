@@ -23,7 +23,10 @@ EXPORTS = (
     "qlora_linear_bwd_dropout",
     "qlora_check_device_error", "qlora_status_string", "qlora_launch_count", "qlora_nf4_levels",
     "qlora_set_kernel_timer", "qlora_kernel_timer_count", "nf4_quantize_noalloc",
+    "qlora_paged_alloc", "qlora_paged_free", "qlora_paged_prefetch", "qlora_adamw_step",
 )
+
+QLORA_PAGE_HOST = -1
 
 
 class NF4TensorStruct(ctypes.Structure):
@@ -34,6 +37,11 @@ class NF4TensorStruct(ctypes.Structure):
 
 class DropoutStruct(ctypes.Structure):
     _fields_ = [("p", ctypes.c_float), ("seed", ctypes.c_uint64), ("offset", ctypes.c_uint64)]
+
+
+class AdamWStruct(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_float), ("beta1", ctypes.c_float), ("beta2", ctypes.c_float),
+                ("eps", ctypes.c_float), ("weight_decay", ctypes.c_float)]
 
 
 class CatModuleStruct(ctypes.Structure):
@@ -80,6 +88,10 @@ def load():
         "qlora_nf4_levels": (None, [P]),
         "qlora_set_kernel_timer": (ctypes.c_int, [P, I32]),
         "qlora_kernel_timer_count": (I32, []),
+        "qlora_paged_alloc": (ctypes.c_int, [SZ, ctypes.POINTER(ctypes.c_void_p)]),
+        "qlora_paged_free": (ctypes.c_int, [P]),
+        "qlora_paged_prefetch": (ctypes.c_int, [P, SZ, I32, P]),
+        "qlora_adamw_step": (ctypes.c_int, [ctypes.POINTER(AdamWStruct), I64, I64, P, P, P, P, P, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)

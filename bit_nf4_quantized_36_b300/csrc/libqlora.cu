@@ -9,3 +9,4 @@
 #include "api.cu"
 #include "cat.cu"
 #include "noalloc.cu"
+#include "optim.cu"

@@ -101,6 +101,15 @@ LLAMA70B_DECODE = dict(name="llama70b-mlp-decode-8192<->28672-m{1,8,32}-r16", id
 LLAMA70B_SWEEP = dict(name="llama70b-80-layer-quantize-dequantize-sweep", id=4, layers=80, w_std=0.02,
                       mats=[("q", 8192, 8192), ("k", 1024, 8192), ("v", 1024, 8192), ("o", 8192, 8192),
                             ("gate", 28672, 8192), ("up", 28672, 8192), ("down", 8192, 28672)])
+# Every adapter of Llama-3-8B with rank 16 on all seven linear layers of its 32 blocks (A [r, K]
+# and B [N, r] per matrix): the parameters one optimizer step updates.
+LLAMA8B_ADAPTERS = dict(name="llama3-8b-all-linear-adapters-r16-adamw", id=5, layers=32, r=16,
+                        mats=[("q", 4096, 4096), ("k", 1024, 4096), ("v", 1024, 4096), ("o", 4096, 4096),
+                              ("gate", 14336, 4096), ("up", 14336, 4096), ("down", 4096, 14336)])
+
+
+def adapter_param_count(c=LLAMA8B_ADAPTERS) -> int:
+    return c["layers"] * sum(c["r"] * (N + K) for _, N, K in c["mats"])
 
 
 def tiny_inputs() -> LayerInputs:
@@ -123,3 +132,53 @@ def sweep_weight_gpu(layer: int, mat_index: int, rows: int, cols: int, device="c
         chi = torch.randn((cnt, 3), generator=gen, device=device).pow_(2).sum(1)
         w[mask] = std * z / torch.sqrt(chi / 3.0)
     return w
+
+
+# ---------------------------------------------------------------------------------------
+# Optimizer-step inputs (flat fp32 arrays of adapter weights, gradients and AdamW moments).
+# ---------------------------------------------------------------------------------------
+S_P, S_GRAD, S_M, S_V = 16, 17, 18, 19
+
+
+@dataclass
+class OptimInputs:
+    p: np.ndarray   # fp32 [n] weights
+    g: np.ndarray   # fp32 [n] gradients
+    m: np.ndarray   # fp32 [n] first moments
+    v: np.ndarray   # fp32 [n] second moments (>= 0)
+
+
+def adamw_inputs(workload_id: int, n: int, sub: int = 0) -> OptimInputs:
+    """Weights: the first half A-like U(-1/64, 1/64), the rest B-like N(0, 0.01).  Gradients:
+    N(0, 1e-3) times a log-normal(0, 1) per-element scale (a heavy tail), 1% exact zeros.  First
+    moments N(0, 1e-4); second moments the square of N(0, 1e-3), 1% exact zeros (entries not yet
+    updated)."""
+    h = n // 2
+    gp = rng(workload_id, S_P, sub)
+    p = np.concatenate([gp.uniform(-1 / 64, 1 / 64, h), gp.standard_normal(n - h) * 0.01]).astype(np.float32)
+    gg = rng(workload_id, S_GRAD, sub)
+    g = (gg.standard_normal(n) * 1e-3 * np.exp(gg.standard_normal(n))).astype(np.float32)
+    g[gg.random(n) < 0.01] = 0.0
+    m = (rng(workload_id, S_M, sub).standard_normal(n) * 1e-4).astype(np.float32)
+    gv = rng(workload_id, S_V, sub)
+    v = np.square(gv.standard_normal(n) * 1e-3).astype(np.float32)
+    v[gv.random(n) < 0.01] = 0.0
+    return OptimInputs(p, g, m, v)
+
+
+def adamw_inputs_gpu(workload_id: int, n: int, device="cuda"):
+    """The distributions of adamw_inputs, drawn on the GPU with torch's seeded device generator
+    (for sizes where host generation would dominate): returns (p, g, m, v) fp32 CUDA tensors."""
+    import torch
+    gen = torch.Generator(device=device)
+    gen.manual_seed(SEED_BASE + workload_id * 0x1000 + S_P)
+    h = n // 2
+    p = torch.empty(n, device=device, dtype=torch.float32)
+    p[:h].uniform_(-1 / 64, 1 / 64, generator=gen)
+    p[h:].normal_(0.0, 0.01, generator=gen)
+    g = torch.randn(n, generator=gen, device=device).mul_(1e-3).mul_(torch.randn(n, generator=gen, device=device).exp_())
+    g[torch.rand(n, generator=gen, device=device) < 0.01] = 0.0
+    m = torch.randn(n, generator=gen, device=device).mul_(1e-4)
+    v = torch.randn(n, generator=gen, device=device).mul_(1e-3).square_()
+    v[torch.rand(n, generator=gen, device=device) < 0.01] = 0.0
+    return p, g, m, v

@@ -207,6 +207,58 @@ qlora_status qlora_linear_bwd(const qlora_nf4_tensor *W, const uint16_t *X, int6
                               const uint16_t *dY, const uint16_t *U_saved, uint16_t *dX, float *dA,
                               float *dB, void *ws, size_t ws_bytes, void *stream);
 
+/* ---------------------------------------------------------------------------------------
+ * Paged optimizer states for the adapters ("QLoRA" glossary entry (ultralytics.com), "Como
+ * funciona a QLoRA", paged-optimizers bullet; "Capitulo 1: Que es QLoRA?"
+ * (docs.skillversehub.com), "Componentes clave", "Optimizadores paginados"): the states live in
+ * NVIDIA unified memory and move to CPU RAM during memory spikes, so that training does not
+ * fail for lack of GPU memory.
+ * --------------------------------------------------------------------------------------- */
+
+/* Location argument of qlora_paged_prefetch: host memory (any value >= 0 is a device ordinal). */
+#define QLORA_PAGE_HOST (-1)
+
+/* Allocates `bytes` of unified (managed) memory, accessible from the host and every device,
+ * migrated page by page by the driver; *out receives the pointer (NULL on error).  The pages
+ * are first placed on the processor that touches them first.  QLORA_ERR_INVALID_ARG for
+ * bytes == 0 or out == NULL; QLORA_ERR_CUDA when the current device has no managed memory or
+ * the allocation fails.  Free with qlora_paged_free. */
+qlora_status qlora_paged_alloc(size_t bytes, void **out);
+
+/* Frees memory from qlora_paged_alloc (synchronizes the device, as cudaFree does).  NULL is a
+ * no-op; a pointer that is not managed memory returns QLORA_ERR_INVALID_ARG. */
+qlora_status qlora_paged_free(void *ptr);
+
+/* Moves the pages of [ptr, ptr + bytes) (inside one paged allocation) to `device` (a device
+ * ordinal) or to host memory (QLORA_PAGE_HOST), asynchronously on `stream`: page the states out
+ * before a memory spike and back in before the next optimizer step.  A hint: the data stays
+ * valid wherever the pages are.  On a device without concurrent managed access it does nothing
+ * and returns QLORA_OK.  QLORA_ERR_INVALID_ARG for a NULL or non-managed pointer or an unknown
+ * device; bytes == 0 is a no-op. */
+qlora_status qlora_paged_prefetch(const void *ptr, size_t bytes, int32_t device, void *stream);
+
+/* Hyper-parameters of the adapters' AdamW step.  READING: the pages name no update rule; the
+ * optimizer is AdamW (Loshchilov and Hutter, decoupled weight decay). */
+typedef struct qlora_adamw {
+    float lr;            /* >= 0, finite                     */
+    float beta1, beta2;  /* in [0, 1)                         */
+    float eps;           /* > 0, finite                      */
+    float weight_decay;  /* >= 0, finite (decoupled)          */
+} qlora_adamw;
+
+/* One AdamW step, t >= 1 (the step count including this one), over n elements, in fp32:
+ *   p <- p (1 - lr wd);  m <- b1 m + (1 - b1) g;  v <- b2 v + (1 - b2) g^2;
+ *   p <- p - (lr / (1 - b1^t)) m / (sqrt(v) / sqrt(1 - b2^t) + eps)
+ * p, m, v [n] fp32 are updated in place; g [n] fp32 is read (the dA or dB of qlora_linear_bwd).
+ * Any of them may be paged memory (wherever its pages are) or device memory; all must be
+ * 16-byte aligned.  p_bf16 (nullable, 8-byte aligned) receives bf16(p) after the step: the
+ * adapter copy the layer calls read.  Concatenate every adapter of a model into one range to
+ * update them all in one launch.  n == 0 is a no-op.  Returns QLORA_ERR_INVALID_ARG for
+ * out-of-range hyper-parameters, t < 1, n < 0 or a NULL array, QLORA_ERR_MISALIGNED, or
+ * QLORA_ERR_CUDA. */
+qlora_status qlora_adamw_step(const qlora_adamw *hp, int64_t t, int64_t n, float *p, const float *g, float *m,
+                              float *v, uint16_t *p_bf16, void *stream);
+
 /* Synchronizes `stream`, then reads and clears the library's device error word on the current
  * device.  QLORA_OK, QLORA_ERR_TIMEOUT (a pipelined kernel gave up a bounded wait and exited
  * early; its outputs are undefined) or QLORA_ERR_CUDA. */

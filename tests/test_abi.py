@@ -129,6 +129,27 @@ def test_argument_errors_before_any_launch(L):
     d_nan = _lib.DropoutStruct(float("nan"), 1, 0)
     assert L.qlora_linear_bwd_dropout(ctypes.byref(t), X, 16, A, B, 8, 16.0, ctypes.byref(d_nan), P(0x8000), None,
                                       P(0x5000), P(0x6000), P(0x7000), ws, 1 << 30, None) == 1
+    # AdamW: hyper-parameters out of range, step count, NULL arrays, alignment
+    hp = _lib.AdamWStruct(2e-4, 0.9, 0.999, 1e-8, 0.01)
+    pa, ga, ma, va = P(0x1000), P(0x2000), P(0x3000), P(0x4000)
+    assert L.qlora_adamw_step(None, 1, 16, pa, ga, ma, va, None, None) == 1
+    assert L.qlora_adamw_step(ctypes.byref(hp), 0, 16, pa, ga, ma, va, None, None) == 1
+    assert L.qlora_adamw_step(ctypes.byref(hp), 1, -1, pa, ga, ma, va, None, None) == 1
+    assert L.qlora_adamw_step(ctypes.byref(hp), 1, 0, None, None, None, None, None, None) == 0   # empty: no-op
+    for bad in [_lib.AdamWStruct(-1.0, 0.9, 0.999, 1e-8, 0.0), _lib.AdamWStruct(1e-3, 1.0, 0.999, 1e-8, 0.0),
+                _lib.AdamWStruct(1e-3, 0.9, float("nan"), 1e-8, 0.0), _lib.AdamWStruct(1e-3, 0.9, 0.999, 0.0, 0.0),
+                _lib.AdamWStruct(1e-3, 0.9, 0.999, 1e-8, float("inf"))]:
+        assert L.qlora_adamw_step(ctypes.byref(bad), 1, 16, pa, ga, ma, va, None, None) == 1
+    assert L.qlora_adamw_step(ctypes.byref(hp), 1, 16, pa, None, ma, va, None, None) == 1
+    assert L.qlora_adamw_step(ctypes.byref(hp), 1, 16, P(0x1004), ga, ma, va, None, None) == 3
+    assert L.qlora_adamw_step(ctypes.byref(hp), 1, 16, pa, ga, ma, va, P(0x5002), None) == 3
+    # paged memory: empty or NULL requests
+    out = ctypes.c_void_p(0x1234)
+    assert L.qlora_paged_alloc(0, ctypes.byref(out)) == 1 and not out.value
+    assert L.qlora_paged_alloc(64, None) == 1
+    assert L.qlora_paged_free(None) == 0
+    assert L.qlora_paged_prefetch(None, 64, 0, None) == 1
+    assert L.qlora_paged_prefetch(P(0x1000), 64, -2, None) == 1
     assert L.qlora_launch_count() == 0  # nothing above reached a kernel launch
 
 
