@@ -631,13 +631,22 @@ def hbm_extras(q, _lib, L, dev, peaks, flush):
 def run_ncu_target(args):
     """A short, untimed run for profiler captures: three forward+backward passes of the layer on the
     bench workload (--ncu-target fused), three small-M forwards on a 70B MLP matrix
-    (--ncu-target decode), or three AdamW steps over the Llama-3-8B adapter set with the moments
-    in plain device memory (--ncu-target adamw; the same kernel as with paged moments)."""
+    (--ncu-target decode), three AdamW steps over the Llama-3-8B adapter set with the moments
+    in plain device memory (--ncu-target adamw; the same kernel as with paged moments), or three
+    quantizations of a 28672 x 8192 matrix (--ncu-target quantize)."""
     import torch
 
     import bit_nf4_quantized_36_b300 as q
     from bit_nf4_quantized_36_b300 import synth
     dev = torch.device("cuda")
+    if args.ncu_target == "quantize":
+        W = synth.sweep_weight_gpu(0, 4, 28672, 8192)
+        for _ in range(3):
+            qw = q.nf4_quantize(W)
+        torch.cuda.synchronize()
+        q.check_device_error()
+        print(json.dumps({"ncu_target": "quantize", "rows": 28672, "cols": 8192, "ok": True}))
+        return 0
     if args.ncu_target == "adamw":
         n = synth.adapter_param_count()
         p, g, m, v = synth.adamw_inputs_gpu(synth.LLAMA8B_ADAPTERS["id"], n, dev)
@@ -679,7 +688,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true")
-    ap.add_argument("--ncu-target", choices=["fused", "decode", "adamw"], default=None,
+    ap.add_argument("--ncu-target", choices=["fused", "decode", "adamw", "quantize"], default=None,
                     help="untimed short run of one kernel family, for profiler captures")
     ap.add_argument("--decode-m", type=int, default=1)
     args = ap.parse_args()

@@ -90,6 +90,15 @@ static const NF4Tables &tables() {
             t.thr[k] = f32_from_key(b);
         }
         t.thr[15] = INFINITY;
+        for (int j = 0; j < kNF4Buckets; ++j) {
+            const double start = -1.0 + (j - 1) / 16.0 - std::ldexp(1.0, -12);
+            int c = 0;
+            while (c < 15 && (double)t.thr[c] <= start) ++c;
+            const float tc = c < 15 ? t.thr[c] : 2.0f;
+            uint32_t bits;
+            std::memcpy(&bits, &tc, 4);
+            t.bucket[j] = (bits & ~15u) | (uint32_t)c;
+        }
     });
     return t;
 }

@@ -25,9 +25,16 @@ static constexpr int kGroup = 256;    // blocks per double-quantization group
 
 // Kernel-argument copy of the tables: levels, and the 15 exact decision thresholds of the
 // nearest-level rule (code = number of thresholds <= x; computed on the host).
+static constexpr int kNF4Buckets = 34;  // entries j = 0..33 for the 1/16-wide buckets j - 1 of [-1, 1]
+
 struct NF4Tables {
     float level[16];
-    float thr[16];   // thr[0..14] used
+    float thr[16];   // thr[0..14] used, thr[15] = +inf
+    // Entry j describes the bucket starting at b = -1 + (j - 1) / 16: c = the number of thresholds
+    // at or below b - 2^-12 and t = thr[c] (2.0 when c = 15), the one threshold that can fall in
+    // [b - 2^-12, b + 1/16] (consecutive thresholds are at least 0.0805 apart).  Stored as t's
+    // bit pattern with its low 4 mantissa bits replaced by c, which moves t by less than 2^-20.
+    uint32_t bucket[kNF4Buckets];
 };
 
 // ---------------------------------------------------------------------------------------

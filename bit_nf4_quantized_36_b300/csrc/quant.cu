@@ -13,14 +13,18 @@
 namespace qlora {
 
 // ---------------------------------------------------------------------------------------
-// K1: per 64-block absmax, NF4 code of every weight, two codes per byte.
-// 16 threads per block (float4 each); the absmax is a 16-lane shuffle reduction.
+// K1: per 64-block absmax, NF4 code of every weight, two codes per byte, and the fp64 sums of
+// the 256-block groups' scales folded into aligned subtrees of the mean's pairwise tree.
+// One CTA (256 threads) per run of `run` consecutive groups; 16 threads per 64-block (float4
+// each), four blocks' loads in flight per thread; the absmax is a 16-lane max reduction.
+//
 // Code rule: thr[0..14] are the exact fp32 decision thresholds of the nearest-level rule
 // (thr[k] = smallest x in (L_k, L_k+1] with fl(L_k+1 - x) < fl(x - L_k)), so the code is the
-// number of thresholds <= x; a 4-step binary search finds it.  Identical to the argmin with
-// fp32 distances and lower-index ties because no two non-adjacent levels can tie (levels
-// are >= 0.079 apart and |x| <= 1).
+// number of thresholds <= x = fl(w / s).  Identical to the argmin with fp32 distances and
+// lower-index ties because no two non-adjacent levels can tie (levels are >= 0.079 apart and
+// |x| <= 1).
 // ---------------------------------------------------------------------------------------
+// Exact: a 4-step binary search on x = fl(w / s).
 __device__ __forceinline__ uint32_t nf4_code(float w, float s, const float *thr) {
     if (s == 0.0f) return kZeroCode;
     const float x = __fdiv_rn(w, s);
@@ -31,97 +35,215 @@ __device__ __forceinline__ uint32_t nf4_code(float w, float s, const float *thr)
     return c;
 }
 
-__global__ void __launch_bounds__(256) nf4_quantize_blocks_kernel(const float4 *__restrict__ W, int64_t nb,
-                                                                  uint16_t *__restrict__ codes16,
-                                                                  float *__restrict__ absmax, NF4Tables tab) {
-    __shared__ float s_thr[16];
-    if (threadIdx.x < 16) s_thr[threadIdx.x] = tab.thr[threadIdx.x];
-    __syncthreads();
-    const uint32_t lane = threadIdx.x & 31u;
-    const uint32_t l16 = threadIdx.x & 15u;
-    const uint32_t gmask = 0xFFFFu << (lane & 16u);
-    const int64_t per_cta = blockDim.x / 16;
-    for (int64_t b = (int64_t)blockIdx.x * per_cta + threadIdx.x / 16; b < nb; b += (int64_t)gridDim.x * per_cta) {
-        const float4 v = __ldcs(W + b * 16 + l16);
-        float m = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
-        m = fmaxf(m, __shfl_xor_sync(gmask, m, 8));
-        m = fmaxf(m, __shfl_xor_sync(gmask, m, 4));
-        m = fmaxf(m, __shfl_xor_sync(gmask, m, 2));
-        m = fmaxf(m, __shfl_xor_sync(gmask, m, 1));
-        const uint32_t c0 = nf4_code(v.x, m, s_thr), c1 = nf4_code(v.y, m, s_thr);
-        const uint32_t c2 = nf4_code(v.z, m, s_thr), c3 = nf4_code(v.w, m, s_thr);
-        codes16[b * 16 + l16] = (uint16_t)(((c0 << 4) | c1) | (((c2 << 4) | c3) << 8));
-        if (l16 == 0) absmax[b] = m;
-    }
+// Without a division: x0 = fl(w * fl(1/s)) is within 2^-22 of x when s is normal (|w / s| <= 1:
+// two roundings of 2^-24 relative each, plus 2^-24 for x's own rounding).  j = floor(fl(16 x0 +
+// 17)) puts x0 in [b - 2^-23, b + 1/16 + 2^-23) for b = -1 + (j - 1) / 16, so every threshold at or
+// below b - 2^-12 is below x and the one after t = thr[c] is above x: the code is c + [t <= x].
+// With the table's t' (t moved by under 2^-20), the comparison on x0 gives [t <= x] whenever x0
+// is more than 2^-19 from t'; otherwise `unsure` asks for the exact rule.  NaN weights land on
+// j = 0 and are unsure.
+__device__ __forceinline__ uint32_t nf4_code_fast(float w, float rcp, const uint32_t *tab, bool &unsure) {
+    const float x0 = __fmul_rn(w, rcp);
+    const uint32_t e = tab[__float2int_rd(__fmaf_rn(x0, 16.0f, 17.0f))];  // in [0, 33] for |x0| <= 1 + 2^-22
+    const float d = __fsub_rn(x0, __uint_as_float(e));
+    unsure |= !(fabsf(d) > 0x1p-19f);
+    return (e & 15u) + (d >= 0.0f ? 1u : 0u);
 }
 
-// K2a: S_g = fp64 sum of the group's scales in index order; slots ng..p2-1 get +0.0.
-// One warp per group.  The scales are non-negative fp32 values; when the group's non-zero scales
-// span at most 2^21 in binary exponent, every partial sum is an integer multiple of the smallest
-// scale's ulp below 2^(24 + 21 + 8) of it, hence exact in fp64, so any summation order -- here a
-// warp tree -- gives the bit pattern of the sequential sum.  Other groups (rare: scales differing
-// by more than 2^21) take the sequential chain in index order.
-__global__ void __launch_bounds__(256) dq_group_sums_kernel(const float *__restrict__ absmax, int64_t nb, int64_t ng,
-                                                            int64_t p2, double *__restrict__ tree) {
-    const uint32_t lane = threadIdx.x & 31u;
-    const int64_t warps = (int64_t)gridDim.x * (blockDim.x / 32);
-    for (int64_t g = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32; g < p2; g += warps) {
-        if (g >= ng) {
-            if (lane == 0) tree[g] = 0.0;
-            continue;
-        }
-        float v[8];
-        int emin = 255, emax = 0;
+// S_g = fp64 sum of one group's scales s[0..255] (zeros past the last block) in index order, by
+// one warp.  The scales are non-negative fp32 values; when the group's non-zero scales span at
+// most 2^21 in binary exponent, every partial sum is an integer multiple of the smallest scale's
+// ulp below 2^(24 + 21 + 8) of it, hence exact in fp64, so any summation order -- here a warp
+// tree -- gives the bit pattern of the sequential sum.  Other groups (rare: scales differing by
+// more than 2^21) take the sequential chain in index order.
+__device__ __forceinline__ double group_sum(const float *s, uint32_t lane) {
+    float v[8];
+    int emin = 255, emax = 0;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int64_t b = g * kGroup + i * 32 + lane;
-            v[i] = (b < nb) ? absmax[b] : 0.0f;
-            const int e = (int)((__float_as_uint(v[i]) >> 23) & 0xFFu);
-            if (v[i] != 0.0f) {
-                emin = min(emin, e);
-                emax = max(emax, e);
+    for (int i = 0; i < 8; ++i) {
+        v[i] = s[i * 32 + lane];
+        const int e = (int)((__float_as_uint(v[i]) >> 23) & 0xFFu);
+        if (v[i] != 0.0f) {
+            emin = min(emin, e);
+            emax = max(emax, e);
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        emin = min(emin, __shfl_xor_sync(0xffffffffu, emin, o));
+        emax = max(emax, __shfl_xor_sync(0xffffffffu, emax, o));
+    }
+    double acc = 0.0;
+    if (emax - emin <= 21) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc = __dadd_rn(acc, (double)v[i]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc = __dadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, o));
+    } else if (lane == 0) {
+        for (int b = 0; b < kGroup; ++b) acc = __dadd_rn(acc, (double)s[b]);
+    }
+    return acc;
+}
+
+static constexpr int kQuantThreads = kGroup;  // one thread per block of the group in the epilogue
+static constexpr int kMeanLeaves = 1024;      // at most this many subtree sums reach the mean
+// 8 threads per 64-block, two float4 each: a pass of the CTA covers 32 blocks.  Each thread
+// stages its own two float4 of the next kQAhead passes in shared memory with cp.async (no
+// register held while the loads are in flight), so every SM keeps eight CTAs x 256 threads x
+// kQAhead x 32 B in flight at 32 registers a thread.
+static constexpr int kQAhead = 3;
+static constexpr int kQPassBlocks = kQuantThreads / 8;
+static constexpr int kQPasses = kGroup / kQPassBlocks;  // passes per group
+
+__device__ __forceinline__ int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
+
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ uint32_t pack4(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3) {
+    return ((c0 << 4) | c1) | (((c2 << 4) | c3) << 8);
+}
+
+__global__ void __launch_bounds__(kQuantThreads, 8) nf4_quantize_groups_kernel(
+    const float4 *__restrict__ W, int64_t nb, int64_t ng, int64_t run, uint16_t *__restrict__ codes16,
+    float *__restrict__ absmax, double *__restrict__ leaves, NF4Tables tab) {
+    __shared__ float4 s_in[kQAhead][2][kQuantThreads];
+    __shared__ float s_thr[16];
+    __shared__ float s_abs[2][kGroup];  // double-buffered over groups: one barrier per group
+    __shared__ uint32_t s_tab[kNF4Buckets];
+    if (threadIdx.x < 16) s_thr[threadIdx.x] = tab.thr[threadIdx.x];
+    if (threadIdx.x < kNF4Buckets) s_tab[threadIdx.x] = tab.bucket[threadIdx.x];
+    __syncthreads();
+
+    // this CTA's groups [g0, g0 + run) hold blocks [B0, B1): a contiguous range of W
+    const int64_t g0 = (int64_t)blockIdx.x * run;
+    const int64_t B0 = min64(nb, g0 * kGroup), B1 = min64(nb, (g0 + run) * kGroup);
+    const int64_t ngrp = (B1 - B0 + kGroup - 1) / kGroup;  // groups of W in the run
+    const int64_t npass = ngrp * kQPasses;
+    const uint32_t lane = threadIdx.x & 31u, l8 = threadIdx.x & 7u;
+    const uint32_t gmask = 0xFFu << (lane & 24u);
+    const int sub = (int)(threadIdx.x >> 3);  // block within a pass
+    auto stage = [&](int64_t p) {             // this thread's two float4 of pass p, or zeros past W
+        const int64_t b = B0 + p * kQPassBlocks + sub;
+        float4 *d = &s_in[p % kQAhead][0][threadIdx.x];
+        if (b < B1) {
+            cp_async_16(smem_u32(d), W + b * 16 + l8);
+            cp_async_16(smem_u32(d + kQuantThreads), W + b * 16 + 8 + l8);
+        } else {
+            d[0] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            d[kQuantThreads] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        }
+        cp_async_commit();  // one group per pass, empty or not, keeps the wait count fixed
+    };
+#pragma unroll
+    for (int p = 0; p < kQAhead - 1; ++p) stage(p);
+
+    double stack[48];  // thread 0: pairwise-tree stack over the run's groups
+    for (int64_t p = 0; p < npass; ++p) {
+        stage(p + kQAhead - 1);
+        cp_async_wait<kQAhead - 1>();  // pass p has landed (only this thread reads its slots)
+        const float4 v = s_in[p % kQAhead][0][threadIdx.x];
+        const float4 u = s_in[p % kQAhead][1][threadIdx.x];
+        const int blk = (int)(p % kQPasses) * kQPassBlocks + sub;  // block within the group
+        // |w| >= 0 orders like its bit pattern; fmaxf drops NaN (finite input is required)
+        float m = fmaxf(fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))),
+                        fmaxf(fmaxf(fabsf(u.x), fabsf(u.y)), fmaxf(fabsf(u.z), fabsf(u.w))));
+        m = __uint_as_float(__reduce_max_sync(gmask, __float_as_uint(fmaxf(m, 0.0f))));
+        uint32_t c[8] = {kZeroCode, kZeroCode, kZeroCode, kZeroCode, kZeroCode, kZeroCode, kZeroCode, kZeroCode};
+        bool unsure = !(m >= 0x1p-100f && m < INFINITY);  // else 1/m is normal and finite
+        if (!unsure) {
+            const float rcp = __frcp_rn(m);
+            c[0] = nf4_code_fast(v.x, rcp, s_tab, unsure);
+            c[1] = nf4_code_fast(v.y, rcp, s_tab, unsure);
+            c[2] = nf4_code_fast(v.z, rcp, s_tab, unsure);
+            c[3] = nf4_code_fast(v.w, rcp, s_tab, unsure);
+            c[4] = nf4_code_fast(u.x, rcp, s_tab, unsure);
+            c[5] = nf4_code_fast(u.y, rcp, s_tab, unsure);
+            c[6] = nf4_code_fast(u.z, rcp, s_tab, unsure);
+            c[7] = nf4_code_fast(u.w, rcp, s_tab, unsure);
+        }
+        if (unsure) {
+            c[0] = nf4_code(v.x, m, s_thr);
+            c[1] = nf4_code(v.y, m, s_thr);
+            c[2] = nf4_code(v.z, m, s_thr);
+            c[3] = nf4_code(v.w, m, s_thr);
+            c[4] = nf4_code(u.x, m, s_thr);
+            c[5] = nf4_code(u.y, m, s_thr);
+            c[6] = nf4_code(u.z, m, s_thr);
+            c[7] = nf4_code(u.w, m, s_thr);
+        }
+        const int64_t b = B0 + p * kQPassBlocks + sub;
+        if (b < B1) {
+            codes16[b * 16 + l8] = (uint16_t)pack4(c[0], c[1], c[2], c[3]);
+            codes16[b * 16 + 8 + l8] = (uint16_t)pack4(c[4], c[5], c[6], c[7]);
+        }
+        const int64_t gi = p / kQPasses;  // group within the run
+        float *sa = s_abs[gi & 1];
+        if (l8 == 0) sa[blk] = m;  // 0 past the last block
+        if (p % kQPasses == kQPasses - 1) {  // the pass closes a group (uniform over the CTA)
+            // one barrier: the buffer is written again two groups later, after the next group's
+            // barrier, which every reader of this one has passed
+            __syncthreads();
+            const int64_t gb0 = b - blk;
+            if (gb0 + (int64_t)threadIdx.x < B1) absmax[gb0 + threadIdx.x] = sa[threadIdx.x];
+            if (threadIdx.x < 32) {
+                double sum = group_sum(sa, lane);
+                if (lane == 0) {  // leaf gi of the run, paired as the tree's levels pair them
+                    int lvl = 0;
+                    for (int64_t j = gi; j & 1; j >>= 1) sum = __dadd_rn(stack[lvl++], sum);
+                    stack[lvl] = sum;
+                }
             }
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            emin = min(emin, __shfl_xor_sync(0xffffffffu, emin, o));
-            emax = max(emax, __shfl_xor_sync(0xffffffffu, emax, o));
+    }
+    cp_async_wait<0>();  // the look-ahead copies past the range are empty groups; nothing lands late
+    if (threadIdx.x == 0) {
+        // groups of the run past the last one of W are leaves of +0.0
+        for (int64_t j = ngrp; j < run; ++j) {
+            double sum = 0.0;
+            int lvl = 0;
+            for (int64_t k = j; k & 1; k >>= 1) sum = __dadd_rn(stack[lvl++], sum);
+            stack[lvl] = sum;
         }
-        double acc = 0.0;
-        if (emax - emin <= 21) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) acc = __dadd_rn(acc, (double)v[i]);
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) acc = __dadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, o));
-        } else if (lane == 0) {
-            const int64_t b1 = (g * kGroup + kGroup < nb) ? g * kGroup + kGroup : nb;
-            for (int64_t b = g * kGroup; b < b1; ++b) acc = __dadd_rn(acc, (double)absmax[b]);
-        }
-        if (lane == 0) tree[g] = acc;
+        leaves[blockIdx.x] = stack[__ffsll((long long)run) - 1];
     }
 }
 
-// K2b: pairwise tree over the p2 group sums (level by level: t'[i] = t[2i] + t[2i+1], ping-pong
-// buffers), then mu = fl32(total / nb) with an IEEE fp64 division.  One CTA.
-__global__ void __launch_bounds__(1024) dq_mean_kernel(double *__restrict__ tree, double *__restrict__ tree2,
-                                                       int64_t p2, int64_t nb, float *__restrict__ mu_out) {
-    double *src = tree, *dst = tree2;
-    for (int64_t len = p2; len > 1; len >>= 1) {
-        for (int64_t i = threadIdx.x; i < len / 2; i += blockDim.x) dst[i] = __dadd_rn(src[2 * i], src[2 * i + 1]);
+// K2: mu = fl32(T / nb) with an IEEE fp64 division, T the pairwise tree over the p2 group sums
+// (level by level, t'[i] = t[2i] + t[2i+1]); K1 left the nl <= 1024 sums of its aligned
+// subtrees, and every CTA pairs them level by level in shared memory.  Then per group (one
+// warp): c2_g = max |fl32(s_b - mu)|; q_b = rint(fl32(fl32(d / c2) * 127)).
+static constexpr int kEncodeThreads = kMeanLeaves;
+
+__global__ void __launch_bounds__(kEncodeThreads) dq_encode_kernel(const float *__restrict__ absmax, int64_t nb,
+                                                                   int64_t ng, const double *__restrict__ leaves,
+                                                                   int nl, int8_t *__restrict__ qcode,
+                                                                   float *__restrict__ c2_out,
+                                                                   float *__restrict__ mu_out) {
+    __shared__ double s_t[kEncodeThreads];
+    __shared__ float s_mu;
+    if ((int)threadIdx.x < nl) s_t[threadIdx.x] = leaves[threadIdx.x];
+    __syncthreads();
+    for (int len = nl; len > 1; len >>= 1) {
+        double v = 0.0;
+        if ((int)threadIdx.x < len / 2) v = __dadd_rn(s_t[2 * threadIdx.x], s_t[2 * threadIdx.x + 1]);
         __syncthreads();
-        double *t = src;
-        src = dst;
-        dst = t;
+        if ((int)threadIdx.x < len / 2) s_t[threadIdx.x] = v;
+        __syncthreads();
     }
-    if (threadIdx.x == 0) *mu_out = __double2float_rn(__ddiv_rn(src[0], (double)nb));
-}
-
-// K2c: per group (one warp): c2_g = max |fl32(s_b - mu)|; q_b = rint(fl32(fl32(d / c2) * 127)).
-__global__ void __launch_bounds__(256) dq_encode_kernel(const float *__restrict__ absmax, int64_t nb, int64_t ng,
-                                                        const float *__restrict__ mu_ptr, int8_t *__restrict__ qcode,
-                                                        float *__restrict__ c2_out) {
+    if (threadIdx.x == 0) {
+        s_mu = __double2float_rn(__ddiv_rn(s_t[0], (double)nb));
+        if (blockIdx.x == 0) *mu_out = s_mu;
+    }
+    __syncthreads();
+    const float mu = s_mu;
     const uint32_t lane = threadIdx.x & 31u;
-    const float mu = *mu_ptr;
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x / 32);
     for (int64_t g = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32; g < ng; g += warps) {
         float d[8];
@@ -195,14 +317,16 @@ cudaError_t launch_quantize(const float *W, int64_t n, uint8_t *codes, int8_t *q
                             float *ws_absmax, double *ws_tree, int64_t p2, const NF4Tables &tab, int num_sms,
                             cudaStream_t st) {
     const int64_t nb = n / kBlock, ng = (nb + kGroup - 1) / kGroup;
-    nf4_quantize_blocks_kernel<<<grid_for(nb, 16, num_sms, 8), 256, 0, st>>>(
-        reinterpret_cast<const float4 *>(W), nb, reinterpret_cast<uint16_t *>(codes), ws_absmax, tab);
+    // runs of `run` groups (a power of two) so that at most min(1024, 8 per SM) subtree sums remain
+    int64_t run = 1;
+    while (p2 / run > std::min<int64_t>(kMeanLeaves, (int64_t)num_sms * 8)) run <<= 1;
+    const int nl = (int)(p2 / run);
+    nf4_quantize_groups_kernel<<<nl, kQuantThreads, 0, st>>>(reinterpret_cast<const float4 *>(W), nb, ng, run,
+                                                             reinterpret_cast<uint16_t *>(codes), ws_absmax, ws_tree,
+                                                             tab);
     count_launch();
-    dq_group_sums_kernel<<<grid_for(p2, 8, num_sms, 16), 256, 0, st>>>(ws_absmax, nb, ng, p2, ws_tree);
-    count_launch();
-    dq_mean_kernel<<<1, 1024, 0, st>>>(ws_tree, ws_tree + p2, p2, nb, mu);
-    count_launch();
-    dq_encode_kernel<<<grid_for(ng, 8, num_sms, 8), 256, 0, st>>>(ws_absmax, nb, ng, mu, qcode, c2);
+    const int g2 = (int)std::max<int64_t>(1, std::min<int64_t>((ng + 31) / 32, (int64_t)num_sms));
+    dq_encode_kernel<<<g2, kEncodeThreads, 0, st>>>(ws_absmax, nb, ng, ws_tree, nl, qcode, c2, mu);
     count_launch();
     return cudaGetLastError();
 }
