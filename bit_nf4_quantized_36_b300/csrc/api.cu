@@ -103,6 +103,72 @@ static const NF4Tables &tables() {
     return t;
 }
 
+// ---------------------------------------------------------------------------------------
+// Side streams.  The skinny products and the scale rebuild of one layer call are latency-bound
+// (a few microseconds of set-up, pipeline fill and reduction each) and some do not depend on one
+// another; those run on two side streams of the current device, forked from and joined back to
+// the caller's stream with events, so that their latencies overlap.  A per-device mutex covers
+// the enqueue of a call (not its execution), so concurrent host threads never mix up the events.
+// If the streams cannot be created, everything runs on the caller's stream.
+// ---------------------------------------------------------------------------------------
+struct SideStreams {
+    std::mutex mu;
+    bool tried = false, ok = false;
+    cudaStream_t s[2] = {nullptr, nullptr};
+    cudaEvent_t fork = nullptr, join[2] = {nullptr, nullptr};
+};
+
+static SideStreams *side_streams() {
+    static SideStreams ss[16];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 16) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    SideStreams &x = ss[dev];
+    std::lock_guard<std::mutex> lock(x.mu);
+    if (!x.tried) {
+        x.tried = true;
+        x.ok = cudaStreamCreateWithFlags(&x.s[0], cudaStreamNonBlocking) == cudaSuccess &&
+               cudaStreamCreateWithFlags(&x.s[1], cudaStreamNonBlocking) == cudaSuccess &&
+               cudaEventCreateWithFlags(&x.fork, cudaEventDisableTiming) == cudaSuccess &&
+               cudaEventCreateWithFlags(&x.join[0], cudaEventDisableTiming) == cudaSuccess &&
+               cudaEventCreateWithFlags(&x.join[1], cudaEventDisableTiming) == cudaSuccess;
+        if (!x.ok) (void)cudaGetLastError();
+    }
+    return x.ok ? &x : nullptr;
+}
+
+// One layer call's use of the side streams: fork() makes both side streams wait for what the
+// caller's stream has enqueued so far; side(i) is the stream to launch independent work on (the
+// caller's own stream when side streams are unavailable); join(i) makes the caller's stream wait
+// for side stream i.  Holds the device's side-stream mutex for its lifetime.
+class Fork {
+  public:
+    explicit Fork(cudaStream_t caller) : st_(caller), ss_(side_streams()) {
+        if (ss_) lock_ = std::unique_lock<std::mutex>(ss_->mu);
+    }
+    cudaError_t fork() {
+        if (!ss_) return cudaSuccess;
+        cudaError_t e = cudaEventRecord(ss_->fork, st_);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(ss_->s[0], ss_->fork, 0);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(ss_->s[1], ss_->fork, 0);
+        return e;
+    }
+    cudaStream_t side(int i) const { return ss_ ? ss_->s[i] : st_; }
+    cudaError_t join(int i) {
+        if (!ss_) return cudaSuccess;
+        cudaError_t e = cudaEventRecord(ss_->join[i], ss_->s[i]);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(st_, ss_->join[i], 0);
+        return e;
+    }
+
+  private:
+    cudaStream_t st_;
+    SideStreams *ss_;
+    std::unique_lock<std::mutex> lock_;
+};
+
 static int num_sms_current() {
     int dev = 0, n = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return 148; }
@@ -436,11 +502,14 @@ static qlora_status layer_fwd(const qlora_nf4_tensor *W, const uint16_t *X, int6
         return QLORA_ERR_CUDA;
 
     cudaError_t e;
+    Fork fk(st);
+    if ((e = fk.fork()) != cudaSuccess) return from_cuda(e);
+    // the fused kernel's block scales, alongside the adapter product
+    if (!w.fp.small && (e = launch_dq_scales_t(W->scale_codes, W->scale_scales, W->scale_offset, N, (int)KB, scalesT,
+                                               fk.side(0))) != cudaSuccess)
+        return from_cuda(e);
     if (d && (e = launch_dropout_x(X, M * K, d->seed, d->offset, d->p, const_cast<uint16_t *>(Xl), nullptr, sms, st)) !=
                  cudaSuccess)
-        return from_cuda(e);
-    if (!w.fp.small && (e = launch_dq_scales_t(W->scale_codes, W->scale_scales, W->scale_offset, N, (int)KB, scalesT,
-                                               st)) != cudaSuccess)
         return from_cuda(e);
     // U = bf16(s * X A^T)  [M, r8] (+ U_save [M, r]), X masked under dropout
     ProjArgs pu = proj_args(w.pu, M, w, r, 0, scale);
@@ -448,6 +517,7 @@ static qlora_status layer_fwd(const qlora_nf4_tensor *W, const uint16_t *X, int6
     pu.ld_h = w.r8;
     pu.out_h2 = U_save;
     if ((e = launch_proj(false, false, mX_k, mA_k, pu, st)) != cudaSuccess) return from_cuda(e);
+    if ((e = fk.join(0)) != cudaSuccess) return from_cuda(e);
     if (w.gemv) {
         const int32_t ti = timer_open(st);
         e = launch_gemv(W->codes, W->scale_codes, W->scale_scales, W->scale_offset, X, (int)M, N, K, mainp, U, w.r8, B,
@@ -512,10 +582,8 @@ static qlora_status layer_bwd(const qlora_nf4_tensor *W, const uint16_t *X, int6
         return QLORA_ERR_CUDA;
 
     cudaError_t e;
+    Fork fk(st);
     if (d && (e = launch_dropout_x(X, M * K, d->seed, d->offset, d->p, Xd, mask, sms, st)) != cudaSuccess)
-        return from_cuda(e);
-    if (!w.fp.small && (e = launch_dq_scales_t(W->scale_codes, W->scale_scales, W->scale_offset, N, (int)KB, scalesT,
-                                               st)) != cudaSuccess)
         return from_cuda(e);
     if (!r_vec && (e = launch_pad_2d(B, N, r, Bpad, N, w.r8, sms, st)) != cudaSuccess) return from_cuda(e);
     // U: the forward's saved copy, or recomputed
@@ -527,11 +595,21 @@ static qlora_status layer_bwd(const qlora_nf4_tensor *W, const uint16_t *X, int6
         pu.ld_h = w.r8;
         if ((e = launch_proj(false, false, mX_k, mA_k, pu, st)) != cudaSuccess) return from_cuda(e);
     }
+    // from here three independent pieces: the block scales and dB on the side streams, V here
+    if ((e = fk.fork()) != cudaSuccess) return from_cuda(e);
+    if (!w.fp.small && (e = launch_dq_scales_t(W->scale_codes, W->scale_scales, W->scale_offset, N, (int)KB, scalesT,
+                                               fk.side(0))) != cudaSuccess)
+        return from_cuda(e);
+    // dB = G^T U  (D[n, j] = sum_m G[m, n] U[m, j])
+    ProjArgs pb = proj_args(w.pdb, N, w, r, 2, 1.0f);
+    pb.out_f = dB;
+    if ((e = launch_proj(true, true, mG_mn, mU_mn, pb, fk.side(1))) != cudaSuccess) return from_cuda(e);
     // V = bf16(s * G B)  [M, r8]
     ProjArgs pv = proj_args(w.pv, M, w, r, 0, scale);
     pv.out_h = V;
     pv.ld_h = w.r8;
     if ((e = launch_proj(false, true, mG_k, mB_mn, pv, st)) != cudaSuccess) return from_cuda(e);
+    if ((e = fk.join(0)) != cudaSuccess) return from_cuda(e);
     // dX = G W^ + V A  (under dropout: G W^, then += mask / (1 - p) * (V A))
     FusedArgs fa = fused_args(W, M, w, r, A, K, dX, mainp, K);
     if (d) fa.kt_lora = 0;
@@ -543,10 +621,7 @@ static qlora_status layer_bwd(const qlora_nf4_tensor *W, const uint16_t *X, int6
     ProjArgs pa = proj_args(w.pda, K, w, r, 1, 1.0f);
     pa.out_f = dA;
     if ((e = launch_proj(true, true, mX_mn, mV_mn, pa, st)) != cudaSuccess) return from_cuda(e);
-    // dB = G^T U  (D[n, j] = sum_m G[m, n] U[m, j])
-    ProjArgs pb = proj_args(w.pdb, N, w, r, 2, 1.0f);
-    pb.out_f = dB;
-    if ((e = launch_proj(true, true, mG_mn, mU_mn, pb, st)) != cudaSuccess) return from_cuda(e);
+    if ((e = fk.join(1)) != cudaSuccess) return from_cuda(e);
     return QLORA_OK;
 }
 

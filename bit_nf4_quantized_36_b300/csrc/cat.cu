@@ -145,14 +145,10 @@ static qlora_status cat_check(const qlora_cat_module *mods, int32_t G, const uin
     return cat_shape(N, r, G, M, K, cs) ? QLORA_OK : QLORA_ERR_UNSUPPORTED_SHAPE;
 }
 
-// The concatenated codes, rebuilt scales, A_cat, block-diagonal B_cat and column scales.
-static cudaError_t cat_assemble(const qlora_cat_module *mods, const CatShape &s, uint8_t *codes, float *scalesT,
-                                uint16_t *Acat, uint16_t *Bcat, float *cscale, cudaStream_t st) {
+// The concatenated codes and rebuilt scales (read only by the fused kernel).
+static cudaError_t cat_assemble_weights(const qlora_cat_module *mods, const CatShape &s, uint8_t *codes,
+                                        float *scalesT, cudaStream_t st) {
     cudaError_t e;
-    if ((e = cudaMemsetAsync(Acat, 0, (size_t)s.R8 * s.K * 2, st)) != cudaSuccess) return e;
-    if ((e = cudaMemsetAsync(Bcat, 0, (size_t)s.Ncat * s.R8 * 2, st)) != cudaSuccess) return e;
-    CatScales sc{};
-    sc.G = s.G;
     for (int i = 0; i < s.G; ++i) {
         const qlora_nf4_tensor *W = mods[i].W;
         if ((e = cudaMemcpyAsync(codes + s.o[i] * s.K / 2, W->codes, (size_t)s.N[i] * s.K / 2, cudaMemcpyDeviceToDevice,
@@ -161,6 +157,19 @@ static cudaError_t cat_assemble(const qlora_cat_module *mods, const CatShape &s,
         if ((e = launch_dq_scales_t(W->scale_codes, W->scale_scales, W->scale_offset, s.N[i], (int)s.KB,
                                     scalesT + s.o[i], st, s.Ncat)) != cudaSuccess)
             return e;
+    }
+    return cudaSuccess;
+}
+
+// A_cat, block-diagonal B_cat and the column scales.
+static cudaError_t cat_assemble_adapters(const qlora_cat_module *mods, const CatShape &s, uint16_t *Acat,
+                                         uint16_t *Bcat, float *cscale, cudaStream_t st) {
+    cudaError_t e;
+    if ((e = cudaMemsetAsync(Acat, 0, (size_t)s.R8 * s.K * 2, st)) != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(Bcat, 0, (size_t)s.Ncat * s.R8 * 2, st)) != cudaSuccess) return e;
+    CatScales sc{};
+    sc.G = s.G;
+    for (int i = 0; i < s.G; ++i) {
         if ((e = cudaMemcpyAsync(Acat + (int64_t)s.c[i] * s.K, mods[i].A, (size_t)s.r[i] * s.K * 2,
                                  cudaMemcpyDeviceToDevice, st)) != cudaSuccess)
             return e;
@@ -278,7 +287,11 @@ qlora_status qlora_linear_fwd_cat(const qlora_cat_module *mods, int32_t G, const
     uint16_t *U = reinterpret_cast<uint16_t *>(base + w.off_u);
     float *mainp = reinterpret_cast<float *>(base + w.off_main);
     const int r64 = ((s.R8 + 63) / 64) * 64;
-    if ((e = cat_assemble(mods, s, codes, scalesT, Acat, Bcat, cscale, st)) != cudaSuccess) return from_cuda(e);
+    // the concatenated weight on a side stream, alongside the adapter product
+    Fork fk(st);
+    if ((e = fk.fork()) != cudaSuccess) return from_cuda(e);
+    if ((e = cat_assemble_weights(mods, s, codes, scalesT, fk.side(0))) != cudaSuccess) return from_cuda(e);
+    if ((e = cat_assemble_adapters(mods, s, Acat, Bcat, cscale, st)) != cudaSuccess) return from_cuda(e);
 
     CUtensorMap mX_k, mA_k, mCodes, mScales, mX_act, mU_act, mY;
     if (!map_bf16(&mX_k, X, s.K, M, 64, 128) || !map_bf16(&mA_k, Acat, s.K, s.R8, 64, r64) ||
@@ -293,6 +306,7 @@ qlora_status qlora_linear_fwd_cat(const qlora_cat_module *mods, int32_t G, const
     pu.ld_h = s.R8;
     pu.out_h2 = U_save;
     if ((e = launch_proj(false, false, mX_k, mA_k, pu, st)) != cudaSuccess) return from_cuda(e);
+    if ((e = fk.join(0)) != cudaSuccess) return from_cuda(e);
     // Y_cat = X W^_cat^T + U_cat B_cat^T
     const FusedArgs fa = cat_fused_args(s, w.fp, s.Ncat, Bcat, s.R8, Y, mainp, s.Ncat);
     if ((e = timed_fused(false, mCodes, mScales, mX_act, mU_act, mY, fa, w.fp, sms, st)) != cudaSuccess)
@@ -351,7 +365,8 @@ qlora_status qlora_linear_bwd_cat(const qlora_cat_module *mods, int32_t G, const
     uint16_t *V = reinterpret_cast<uint16_t *>(base + w.off_v);
     float *mainp = reinterpret_cast<float *>(base + w.off_main);
     const int r64 = ((s.R8 + 63) / 64) * 64;
-    if ((e = cat_assemble(mods, s, codes, scalesT, Acat, Bcat, cscale, st)) != cudaSuccess) return from_cuda(e);
+    Fork fk(st);
+    if ((e = cat_assemble_adapters(mods, s, Acat, Bcat, cscale, st)) != cudaSuccess) return from_cuda(e);
     const uint16_t *Uq = U_saved ? U_saved : U;
 
     CUtensorMap mX_k, mA_k, mG_k, mB_mn, mX_mn, mCodes, mScales, mG_act, mV_act, mDX;
@@ -368,31 +383,40 @@ qlora_status qlora_linear_bwd_cat(const qlora_cat_module *mods, int32_t G, const
         pu.ld_h = s.R8;
         if ((e = launch_proj(false, false, mX_k, mA_k, pu, st)) != cudaSuccess) return from_cuda(e);
     }
+    // from here: the concatenated weight and the dB_i on the side streams, V_cat here
+    if ((e = fk.fork()) != cudaSuccess) return from_cuda(e);
+    if ((e = cat_assemble_weights(mods, s, codes, scalesT, fk.side(0))) != cudaSuccess) return from_cuda(e);
+    for (int i = 0; i < G; ++i) {  // dB_i = dY_i^T U_i (column slices)
+        const int ri64 = ((s.r[i] + 63) / 64) * 64;
+        CUtensorMap mG_i, mU_i;
+        if (!map_cols(&mG_i, dY, s.o[i], s.N[i], M, s.Ncat, 64, 64) ||
+            !map_cols(&mU_i, Uq, s.c[i], s.r[i], M, s.R8, 64, 64))
+            return QLORA_ERR_CUDA;
+        ProjArgs pb = cat_proj_args(plan_proj(s.N[i], M, ri64, sms), s.N[i], ri64, s.r[i], 2);
+        pb.out_f = dB[i];
+        if ((e = launch_proj(true, true, mG_i, mU_i, pb, fk.side(1))) != cudaSuccess) return from_cuda(e);
+    }
     // V_cat = bf16(s_col (dY_cat B_cat))  [M, R8]
     ProjArgs pv = cat_proj_args(w.pv, M, r64, s.R8, 0);
     pv.col_scale = cscale;
     pv.out_h = V;
     pv.ld_h = s.R8;
     if ((e = launch_proj(false, true, mG_k, mB_mn, pv, st)) != cudaSuccess) return from_cuda(e);
+    if ((e = fk.join(0)) != cudaSuccess) return from_cuda(e);
     // dX = dY_cat W^_cat + V_cat A_cat
     const FusedArgs fa = cat_fused_args(s, w.fp, s.Ncat, Acat, s.K, dX, mainp, s.K);
     if ((e = timed_fused(true, mCodes, mScales, mG_act, mV_act, mDX, fa, w.fp, sms, st)) != cudaSuccess)
         return from_cuda(e);
-    // per module: dA_i = V_i^T X, dB_i = dY_i^T U_i (column slices)
+    // per module: dA_i = V_i^T X (column slices of V_cat)
     for (int i = 0; i < G; ++i) {
         const int ri64 = ((s.r[i] + 63) / 64) * 64;
-        CUtensorMap mV_i, mG_i, mU_i;
-        if (!map_cols(&mV_i, V, s.c[i], s.r[i], M, s.R8, 64, 64) ||
-            !map_cols(&mG_i, dY, s.o[i], s.N[i], M, s.Ncat, 64, 64) ||
-            !map_cols(&mU_i, Uq, s.c[i], s.r[i], M, s.R8, 64, 64))
-            return QLORA_ERR_CUDA;
+        CUtensorMap mV_i;
+        if (!map_cols(&mV_i, V, s.c[i], s.r[i], M, s.R8, 64, 64)) return QLORA_ERR_CUDA;
         ProjArgs pa = cat_proj_args(plan_proj(s.K, M, ri64, sms), s.K, ri64, s.r[i], 1);
         pa.out_f = dA[i];
         if ((e = launch_proj(true, true, mX_mn, mV_i, pa, st)) != cudaSuccess) return from_cuda(e);
-        ProjArgs pb = cat_proj_args(plan_proj(s.N[i], M, ri64, sms), s.N[i], ri64, s.r[i], 2);
-        pb.out_f = dB[i];
-        if ((e = launch_proj(true, true, mG_i, mU_i, pb, st)) != cudaSuccess) return from_cuda(e);
     }
+    if ((e = fk.join(1)) != cudaSuccess) return from_cuda(e);
     return QLORA_OK;
 }
 

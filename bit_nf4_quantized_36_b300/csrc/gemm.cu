@@ -832,15 +832,61 @@ FusedPlan plan_fused(int64_t M, int64_t wdim, int64_t kt_main, int r64, int num_
     return pl;
 }
 
+// Clusters of `s` projection CTAs (shared memory for rank r64) resident at once on the current
+// device; cached per (device, s, r64).  A cluster's CTAs must share a GPC, so large clusters fit
+// fewer times than the SM count suggests.
+static int proj_max_clusters(int s, int r64, int fallback) {
+    static std::mutex mu;
+    static int cache[8][9][3];  // [device < 8][s][r64 = 64, 128, 256]; zero until queried
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 8 || s < 1 || s > 8) {
+        (void)cudaGetLastError();
+        return fallback;
+    }
+    const int ri = r64 <= 64 ? 0 : (r64 <= 128 ? 1 : 2);
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache[dev][s][ri] > 0) return cache[dev][s][ri];
+    const size_t smem = proj_smem_bytes(r64);
+    int n = 0;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)s, 1, 1);
+    cfg.blockDim = dim3(128, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)s;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaFuncSetAttribute(lora_proj_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess ||
+        cudaOccupancyMaxActiveClusters(&n, lora_proj_kernel<false, false>, &cfg) != cudaSuccess || n <= 0) {
+        (void)cudaGetLastError();
+        return fallback;
+    }
+    cache[dev][s][ri] = n;
+    return n;
+}
+
 ProjPlan plan_proj(int64_t Mp, int64_t Kc, int r64, int num_sms) {
     ProjPlan pl{};
     pl.tiles = (int)((Mp + 127) / 128);
     pl.ktiles = (int)((Kc + 63) / 64);
-    const int per_sm = r64 <= 64 ? 2 : 1;
-    // splits of a tile form one cluster (at most 8, the portable cluster size)
-    int64_t s = std::max<int64_t>(1, ((int64_t)per_sm * num_sms) / pl.tiles);
-    s = std::max<int64_t>(1, std::min<int64_t>(s, std::min<int64_t>(pl.ktiles, 8)));
-    pl.splits = (int)s;
+    // The splits of a tile form one cluster (at most 8, the portable size).  Cost of a choice:
+    // waves of resident clusters x (k-steps per CTA + ~2 steps of set-up and reduction).
+    int best = 1;
+    int64_t best_cost = INT64_MAX;
+    for (int s = 1; s <= std::min(8, pl.ktiles); ++s) {
+        const int fit = std::max(1, proj_max_clusters(s, r64, std::max(1, num_sms / (2 * s))));
+        const int64_t waves = (pl.tiles + fit - 1) / fit;
+        const int64_t cost = waves * ((pl.ktiles + s - 1) / s + 2);
+        if (cost < best_cost) {
+            best_cost = cost;
+            best = s;
+        }
+    }
+    pl.splits = best;
     return pl;
 }
 
