@@ -620,8 +620,8 @@ def hbm_extras(q, _lib, L, dev, peaks, flush):
         L.qlora_set_kernel_timer(None, 0)
         tk = statistics.median(kev[2 * i].elapsed_time(kev[2 * i + 1]) for i in range(10))
         byt = storage + 2 * r * (rows + cols) + 2 * M * (rows + cols)
-        dec[f"M={M}"] = {"call_ms": t, "kernel": "nf4_gemv_kernel + gemv_finish_kernel" if M <= 2
-                         else "nf4_lora_gemm_small_kernel", "kernel_ms": tk, "GB/s_kernel": byt / tk / 1e6,
+        dec[f"M={M}"] = {"call_ms": t, "kernel": ("nf4_gemv_fma_kernel" if M == 1 else "nf4_gemv_kernel") + " + gemv_finish_kernel"
+                         if M <= 8 else "nf4_lora_gemm_small_kernel", "kernel_ms": tk, "GB/s_kernel": byt / tk / 1e6,
                          "frac_hbm_kernel": byt / tk / 1e6 / peaks["hbm_gbs"], "GB/s_call": byt / t / 1e6}
     out["decode_forward_28672x8192_r16"] = dec
     out["hbm_peak_GB/s"] = f"{peaks['hbm_gbs']} ({peaks['source']})"

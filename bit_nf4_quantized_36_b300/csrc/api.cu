@@ -253,7 +253,7 @@ static QuantWs quant_ws(int64_t rows, int64_t cols) {
 
 struct LayerWs {
     int r8, r64;
-    bool gemv;  // forward with M <= 2: the CUDA-core GEMV instead of the fused kernel
+    bool gemv;  // forward with M <= 8: the register-resident GEMV instead of the fused kernel
     FusedPlan fp;
     ProjPlan pu, pv, pda, pdb;
     size_t off_scales, off_u, off_v, off_bpad, off_main, off_xd, off_mask, total;
@@ -271,7 +271,7 @@ static LayerWs layer_ws(int64_t M, int64_t N, int64_t K, int r, bool bwd, int nu
         w.fp = plan_fused(M, K, (N + 63) / 64, w.r64, num_sms);
     } else {
         w.fp = plan_fused(M, N, K / 64, w.r64, num_sms);
-        w.gemv = M <= 2;
+        w.gemv = M <= 8;
     }
     size_t off = 0;
     w.off_scales = off;  // rebuilt block scales, for the CTA-pair kernel only

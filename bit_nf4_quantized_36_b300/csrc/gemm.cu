@@ -19,7 +19,7 @@
 // 2. lora_proj_kernel<p_mn, q_mn>: skinny products with N = r64 <= 256 (U = X A^T, V = G B,
 //    dA = V^T X, dB = G^T U), split over the contraction across the CTAs of a cluster, whose
 //    fp32 partial tiles are summed in split order through distributed shared memory.
-// The small-M variant of 1. is in gemm_small.cu; M <= 2 forwards use the GEMV in gemv.cu.
+// The small-M variant of 1. is in gemm_small.cu; forwards of up to 8 tokens use the GEMV in gemv.cu.
 #include <algorithm>
 #include <mutex>
 

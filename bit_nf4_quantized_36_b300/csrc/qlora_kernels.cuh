@@ -106,8 +106,8 @@ ProjPlan plan_proj(int64_t Mp, int64_t Kc, int r64, int num_sms);
 cudaError_t launch_proj(bool p_mn, bool q_mn, const CUtensorMap &map_p, const CUtensorMap &map_q, const ProjArgs &args,
                         cudaStream_t st);
 
-// ---- forward for M <= 2 on the CUDA cores (gemv.cu) --------------------------------------
-// Y[m, n] = bf16(sum_k X[m, k] W^[n, k] + sum_j U[m, j] B[n, j]) for m < M (1 or 2), with W^ decoded
+// ---- forward for M <= 8, register-resident (gemv.cu) --------------------------------------
+// Y[m, n] = bf16(sum_k X[m, k] W^[n, k] + sum_j U[m, j] B[n, j]) for m < M (1..8), with W^ decoded
 // from the NF4 tensor's codes and int8 scale codes; partial: [gemv_slices(K), M, N] fp32.
 int gemv_slices(int64_t K);
 cudaError_t launch_gemv(const uint8_t *codes, const int8_t *scale_q, const float *scale_c2, const float *scale_mu,

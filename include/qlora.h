@@ -279,7 +279,7 @@ void qlora_nf4_levels(float out[16]);
  * before and events[2i+1] just after the i-th weight-streaming step of a layer call: the
  * launch of the fused NF4-dequant GEMM kernel (forward or backward dX, with the reduction of its
  * partials when the contraction is split), or, for a forward of
- * one or two tokens, the CUDA-core GEMV and its finishing kernel; on the launch stream, until
+ * up to eight tokens, the register-resident GEMV and its finishing kernel; on the launch stream, until
  * `capacity` steps are recorded.
  * events == NULL switches the recording off.  Process-wide; do not change it while calls are
  * in flight on other host threads.  Returns QLORA_ERR_INVALID_ARG for capacity < 0 or a NULL

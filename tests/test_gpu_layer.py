@@ -91,6 +91,10 @@ def test_tiny_workload(orc):
     (257, 520, 640, 16),   # token tile 256 + 1, weight tiles 4 + ragged
     (2, 264, 4160, 16),    # two tokens: contraction of 2 full 2048-slices and a 64-wide tail
     (1, 136, 2112, 3),     # one token, odd rank, ragged rows
+    (7, 264, 4160, 16),    # seven tokens: eight token columns of the GEMV, one unused
+    (8, 136, 2112, 3),     # eight tokens, ragged rows, a contraction tail inside a 256-step
+    (600, 520, 640, 16),   # two 256-token tiles per unit: token ranges that cross weight tiles
+    (1100, 776, 384, 8),   # the same with more pairs, ragged tokens and weight rows
 ])
 def test_shapes(orc, M, N, K, r):
     inp = synth.layer_inputs(100 + r, M, N, K, r, 2.0 * r, b_std=0.3)
