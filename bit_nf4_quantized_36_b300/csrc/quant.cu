@@ -217,29 +217,43 @@ __global__ void __launch_bounds__(kQuantThreads, 8) nf4_quantize_groups_kernel(
 
 // K2: mu = fl32(T / nb) with an IEEE fp64 division, T the pairwise tree over the p2 group sums
 // (level by level, t'[i] = t[2i] + t[2i+1]); K1 left the nl <= 1024 sums of its aligned
-// subtrees, and every CTA pairs them level by level in shared memory.  Then per group (one
-// warp): c2_g = max |fl32(s_b - mu)|; q_b = rint(fl32(fl32(d / c2) * 127)).
-static constexpr int kEncodeThreads = kMeanLeaves;
+// subtrees, and warp 0 of every CTA pairs them the same way: each lane pairs an aligned run of
+// nl / 32 of them level by level, then a butterfly of shuffles pairs the lanes' results (lane l
+// adds its partner's value, and fp64 addition is commutative, so both partners hold t[2i] +
+// t[2i+1]).  Then per group (one warp): c2_g = max |fl32(s_b - mu)|;
+// q_b = rint(fl32(fl32(d / c2) * 127)).
+static constexpr int kEncodeThreads = 1024;
 
 __global__ void __launch_bounds__(kEncodeThreads) dq_encode_kernel(const float *__restrict__ absmax, int64_t nb,
                                                                    int64_t ng, const double *__restrict__ leaves,
                                                                    int nl, int8_t *__restrict__ qcode,
                                                                    float *__restrict__ c2_out,
                                                                    float *__restrict__ mu_out) {
-    __shared__ double s_t[kEncodeThreads];
     __shared__ float s_mu;
-    if ((int)threadIdx.x < nl) s_t[threadIdx.x] = leaves[threadIdx.x];
-    __syncthreads();
-    for (int len = nl; len > 1; len >>= 1) {
-        double v = 0.0;
-        if ((int)threadIdx.x < len / 2) v = __dadd_rn(s_t[2 * threadIdx.x], s_t[2 * threadIdx.x + 1]);
-        __syncthreads();
-        if ((int)threadIdx.x < len / 2) s_t[threadIdx.x] = v;
-        __syncthreads();
-    }
-    if (threadIdx.x == 0) {
-        s_mu = __double2float_rn(__ddiv_rn(s_t[0], (double)nb));
-        if (blockIdx.x == 0) *mu_out = s_mu;
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        const int per = nl > 32 ? nl / 32 : 1;  // leaves per lane (a power of two, <= 32)
+        const int nlanes = nl / per;            // lanes holding a subtree (a power of two)
+        double t[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) t[i] = (i < per && lane < nlanes) ? leaves[lane * per + i] : 0.0;
+#pragma unroll
+        for (int len = 32; len > 1; len >>= 1) {
+            if (len <= per) {
+#pragma unroll
+                for (int i = 0; i < len / 2; ++i) t[i] = __dadd_rn(t[2 * i], t[2 * i + 1]);
+            }
+        }
+        double v = t[0];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const double w = __shfl_xor_sync(0xffffffffu, v, o);
+            if (o < nlanes) v = __dadd_rn(v, w);
+        }
+        if (lane == 0) {
+            s_mu = __double2float_rn(__ddiv_rn(v, (double)nb));
+            if (blockIdx.x == 0) *mu_out = s_mu;
+        }
     }
     __syncthreads();
     const float mu = s_mu;
