@@ -308,7 +308,10 @@ def run_ours(args):
 
     # ---- timed region: K steps, L2 flushed between steps (outside the step events) ------
     Ksteps = args.steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(Ksteps)]
+    use_graph = dist is None and not args.no_graph
+    # events recorded inside a captured graph must be external to time its replays
+    ev = [(torch.cuda.Event(enable_timing=True, external=use_graph), torch.cuda.Event(enable_timing=True, external=use_graph))
+          for _ in range(Ksteps)]
     kev = new_events(4 * Ksteps)  # 2 fused launches per step
     kev_arr = (ctypes.c_void_p * len(kev))(*[e.cuda_event for e in kev])
     sampler = ClockSampler(dev)
@@ -316,12 +319,31 @@ def run_ours(args):
     n0 = q.launch_count()
     if L.qlora_set_kernel_timer(ctypes.cast(kev_arr, ctypes.c_void_p), 2 * Ksteps) != 0:
         raise RuntimeError("qlora_set_kernel_timer rejected the events")
-    with sampler:
+
+    def timed_steps():
         for i in range(Ksteps):
             flush.zero_()
             ev[i][0].record()
             step()
             ev[i][1].record()
+
+    # One process on one GPU: the K timed steps (flushes and events included) are captured once
+    # into a CUDA graph and replayed, as a training loop would replay its step; every kernel of
+    # every step still runs.  Under torchrun the all-reduces stay outside a graph.
+    if use_graph:
+        cap = torch.cuda.Stream()
+        cap.wait_stream(torch.cuda.current_stream())
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(graph, stream=cap):
+                timed_steps()
+        torch.cuda.current_stream().wait_stream(cap)
+        barrier()
+    with sampler:
+        if use_graph:
+            graph.replay()
+        else:
+            timed_steps()
         barrier()
     launches = q.launch_count() - n0
     nk = L.qlora_kernel_timer_count()
@@ -412,6 +434,8 @@ def run_ours(args):
                 "config": {"workload": WORKLOAD, "M_per_gpu": M, "N": N, "K": K, "r": r, "alpha": alpha,
                            "step": "nf4_quantize + nf4_dequantize + qlora_linear_fwd + qlora_linear_bwd",
                            "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write, outside the step events)",
+                           "launch": ("the K timed steps captured in one CUDA graph, replayed once" if use_graph
+                                      else "stream launches"),
                            "parallelism": f"dp{world}"},
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
                 "gpu_launches_per_step": launches / Ksteps, "clocks": clocks,
@@ -688,6 +712,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="launch the timed steps on the stream, not as a graph")
     ap.add_argument("--ncu-target", choices=["fused", "decode", "adamw", "quantize"], default=None,
                     help="untimed short run of one kernel family, for profiler captures")
     ap.add_argument("--decode-m", type=int, default=1)

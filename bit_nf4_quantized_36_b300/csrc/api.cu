@@ -23,6 +23,15 @@ static void **g_timer_events = nullptr;
 static int32_t g_timer_cap = 0;
 static std::atomic<int32_t> g_timer_n{0};
 
+// Records a timer event on `st`.  Under stream capture the record becomes an event-record node
+// of the graph, so that the event times every replay.
+static cudaError_t timer_record(void *event, cudaStream_t st) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) return cudaGetLastError();
+    return cudaEventRecordWithFlags(static_cast<cudaEvent_t>(event), st,
+                                    cs == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : cudaEventRecordDefault);
+}
+
 // Records the opening event of a timed step; returns its slot, or -1 when not timing.  A failed
 // record (e.g. a NULL handle) must not be reported as the kernel's launch error.
 static int32_t timer_open(cudaStream_t st) {
@@ -30,7 +39,7 @@ static int32_t timer_open(cudaStream_t st) {
     if (!ev) return -1;
     int32_t i = g_timer_n.fetch_add(1);
     if (i >= g_timer_cap) return -1;
-    if (cudaEventRecord(static_cast<cudaEvent_t>(ev[2 * i]), st) != cudaSuccess) {
+    if (timer_record(ev[2 * i], st) != cudaSuccess) {
         cudaGetLastError();
         return -1;
     }
@@ -38,7 +47,7 @@ static int32_t timer_open(cudaStream_t st) {
 }
 static void timer_close(int32_t i, cudaStream_t st) {
     void **ev = g_timer_events;
-    if (i >= 0 && ev && cudaEventRecord(static_cast<cudaEvent_t>(ev[2 * i + 1]), st) != cudaSuccess) cudaGetLastError();
+    if (i >= 0 && ev && timer_record(ev[2 * i + 1], st) != cudaSuccess) cudaGetLastError();
 }
 
 // the fused GEMM and, when the contraction is split, the reduction of its partials

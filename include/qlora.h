@@ -281,6 +281,7 @@ void qlora_nf4_levels(float out[16]);
  * partials when the contraction is split), or, for a forward of
  * up to eight tokens, the register-resident GEMV and its finishing kernel; on the launch stream, until
  * `capacity` steps are recorded.
+ * Under stream capture the records become event-record nodes of the graph, timing each replay.
  * events == NULL switches the recording off.  Process-wide; do not change it while calls are
  * in flight on other host threads.  Returns QLORA_ERR_INVALID_ARG for capacity < 0 or a NULL
  * handle among the 2*capacity events. */
