@@ -124,7 +124,8 @@ struct SideStreams {
     std::mutex mu;
     bool tried = false, ok = false;
     cudaStream_t s[2] = {nullptr, nullptr};
-    cudaEvent_t fork = nullptr, join[2] = {nullptr, nullptr};
+    cudaStream_t hp = nullptr;  // the device's highest stream priority
+    cudaEvent_t ev = nullptr;   // reused: a wait takes the event's latest record at the time it is enqueued
 };
 
 static SideStreams *side_streams() {
@@ -138,39 +139,43 @@ static SideStreams *side_streams() {
     std::lock_guard<std::mutex> lock(x.mu);
     if (!x.tried) {
         x.tried = true;
-        x.ok = cudaStreamCreateWithFlags(&x.s[0], cudaStreamNonBlocking) == cudaSuccess &&
+        int least = 0, greatest = 0;
+        x.ok = cudaDeviceGetStreamPriorityRange(&least, &greatest) == cudaSuccess &&
+               cudaStreamCreateWithFlags(&x.s[0], cudaStreamNonBlocking) == cudaSuccess &&
                cudaStreamCreateWithFlags(&x.s[1], cudaStreamNonBlocking) == cudaSuccess &&
-               cudaEventCreateWithFlags(&x.fork, cudaEventDisableTiming) == cudaSuccess &&
-               cudaEventCreateWithFlags(&x.join[0], cudaEventDisableTiming) == cudaSuccess &&
-               cudaEventCreateWithFlags(&x.join[1], cudaEventDisableTiming) == cudaSuccess;
+               cudaStreamCreateWithPriority(&x.hp, cudaStreamNonBlocking, greatest) == cudaSuccess &&
+               cudaEventCreateWithFlags(&x.ev, cudaEventDisableTiming) == cudaSuccess;
         if (!x.ok) (void)cudaGetLastError();
     }
     return x.ok ? &x : nullptr;
 }
 
 // One layer call's use of the side streams: fork() makes both side streams wait for what the
-// caller's stream has enqueued so far; side(i) is the stream to launch independent work on (the
-// caller's own stream when side streams are unavailable); join(i) makes the caller's stream wait
-// for side stream i.  Holds the device's side-stream mutex for its lifetime.
+// caller's stream has enqueued so far; side(i) is the stream to launch independent work on and
+// priority() a stream whose kernels the block scheduler serves first (both are the caller's own
+// stream when side streams are unavailable); link(a, b) makes stream b wait for what stream a has
+// enqueued so far; join(i) = link(side(i), caller).  Holds the device's side-stream mutex for its
+// lifetime.
 class Fork {
   public:
     explicit Fork(cudaStream_t caller) : st_(caller), ss_(side_streams()) {
         if (ss_) lock_ = std::unique_lock<std::mutex>(ss_->mu);
     }
+    cudaError_t link(cudaStream_t from, cudaStream_t to) {
+        if (!ss_ || from == to) return cudaSuccess;
+        cudaError_t e = cudaEventRecord(ss_->ev, from);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(to, ss_->ev, 0);
+        return e;
+    }
     cudaError_t fork() {
-        if (!ss_) return cudaSuccess;
-        cudaError_t e = cudaEventRecord(ss_->fork, st_);
-        if (e == cudaSuccess) e = cudaStreamWaitEvent(ss_->s[0], ss_->fork, 0);
-        if (e == cudaSuccess) e = cudaStreamWaitEvent(ss_->s[1], ss_->fork, 0);
+        cudaError_t e = link(st_, side(0));
+        if (e == cudaSuccess) e = link(st_, side(1));
         return e;
     }
     cudaStream_t side(int i) const { return ss_ ? ss_->s[i] : st_; }
-    cudaError_t join(int i) {
-        if (!ss_) return cudaSuccess;
-        cudaError_t e = cudaEventRecord(ss_->join[i], ss_->s[i]);
-        if (e == cudaSuccess) e = cudaStreamWaitEvent(st_, ss_->join[i], 0);
-        return e;
-    }
+    cudaStream_t priority() const { return ss_ ? ss_->hp : st_; }
+    cudaStream_t caller() const { return st_; }
+    cudaError_t join(int i) { return link(side(i), st_); }
 
   private:
     cudaStream_t st_;
@@ -618,19 +623,22 @@ static qlora_status layer_bwd(const qlora_nf4_tensor *W, const uint16_t *X, int6
     pv.out_h = V;
     pv.ld_h = w.r8;
     if ((e = launch_proj(false, true, mG_k, mB_mn, pv, st)) != cudaSuccess) return from_cuda(e);
-    if ((e = fk.join(0)) != cudaSuccess) return from_cuda(e);
+    // dX on the high-priority stream once V and the scales are there; dA (which needs only V) here,
+    // at the caller's priority: its CTAs take the SMs that the fused kernel's last wave leaves idle
+    cudaStream_t hp = fk.priority();
+    if ((e = fk.link(st, hp)) != cudaSuccess || (e = fk.link(fk.side(0), hp)) != cudaSuccess) return from_cuda(e);
     // dX = G W^ + V A  (under dropout: G W^, then += mask / (1 - p) * (V A))
     FusedArgs fa = fused_args(W, M, w, r, A, K, dX, mainp, K);
     if (d) fa.kt_lora = 0;
-    if ((e = timed_fused(true, mCodes, mScales, mG_act, mV_act, mDX, fa, w.fp, sms, st)) != cudaSuccess)
+    if ((e = timed_fused(true, mCodes, mScales, mG_act, mV_act, mDX, fa, w.fp, sms, hp)) != cudaSuccess)
         return from_cuda(e);
-    if (d && (e = launch_dropout_dx(mV_k, mA_mn, mDX_sw, dX, mask, d->p, M, K, w.r8, sms, st)) != cudaSuccess)
+    if (d && (e = launch_dropout_dx(mV_k, mA_mn, mDX_sw, dX, mask, d->p, M, K, w.r8, sms, hp)) != cudaSuccess)
         return from_cuda(e);
     // dA = V^T X  (D[k, j] = sum_m X[m, k] V[m, j], stored transposed)
     ProjArgs pa = proj_args(w.pda, K, w, r, 1, 1.0f);
     pa.out_f = dA;
     if ((e = launch_proj(true, true, mX_mn, mV_mn, pa, st)) != cudaSuccess) return from_cuda(e);
-    if ((e = fk.join(1)) != cudaSuccess) return from_cuda(e);
+    if ((e = fk.link(hp, st)) != cudaSuccess || (e = fk.join(1)) != cudaSuccess) return from_cuda(e);
     return QLORA_OK;
 }
 

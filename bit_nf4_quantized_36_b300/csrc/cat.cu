@@ -402,10 +402,12 @@ qlora_status qlora_linear_bwd_cat(const qlora_cat_module *mods, int32_t G, const
     pv.out_h = V;
     pv.ld_h = s.R8;
     if ((e = launch_proj(false, true, mG_k, mB_mn, pv, st)) != cudaSuccess) return from_cuda(e);
-    if ((e = fk.join(0)) != cudaSuccess) return from_cuda(e);
+    // dX on the high-priority stream; the dA_i here, in the SMs its last wave leaves idle
+    cudaStream_t hp = fk.priority();
+    if ((e = fk.link(st, hp)) != cudaSuccess || (e = fk.link(fk.side(0), hp)) != cudaSuccess) return from_cuda(e);
     // dX = dY_cat W^_cat + V_cat A_cat
     const FusedArgs fa = cat_fused_args(s, w.fp, s.Ncat, Acat, s.K, dX, mainp, s.K);
-    if ((e = timed_fused(true, mCodes, mScales, mG_act, mV_act, mDX, fa, w.fp, sms, st)) != cudaSuccess)
+    if ((e = timed_fused(true, mCodes, mScales, mG_act, mV_act, mDX, fa, w.fp, sms, hp)) != cudaSuccess)
         return from_cuda(e);
     // per module: dA_i = V_i^T X (column slices of V_cat)
     for (int i = 0; i < G; ++i) {
@@ -416,7 +418,7 @@ qlora_status qlora_linear_bwd_cat(const qlora_cat_module *mods, int32_t G, const
         pa.out_f = dA[i];
         if ((e = launch_proj(true, true, mX_mn, mV_i, pa, st)) != cudaSuccess) return from_cuda(e);
     }
-    if ((e = fk.join(1)) != cudaSuccess) return from_cuda(e);
+    if ((e = fk.link(hp, st)) != cudaSuccess || (e = fk.join(1)) != cudaSuccess) return from_cuda(e);
     return QLORA_OK;
 }
 

@@ -168,3 +168,42 @@ def test_llama70b_decode(orc, M, mat):
     out = run_layer(inp, fwd_only=True)
     rows = np.arange(M) if M <= 8 else np.array([0, 5, 17, 31])
     check_full(orc, inp, out, rows=rows)
+
+
+def test_graph_capture_replays_the_stream_results():
+    """fwd + bwd captured in a CUDA graph (the library's side-stream fork/join becomes graph edges)
+    and replayed: bit for bit the results of stream launches, for the CTA-pair path with two token
+    tiles per unit and for the GEMV path."""
+    for (M, N, K, r) in [(600, 520, 640, 16), (4, 264, 4160, 8)]:
+        inp = synth.layer_inputs(206 + M, M, N, K, r, 2.0 * r)
+        qw = q.nf4_quantize(torch.from_numpy(inp.W).cuda())
+        X, A, B, G = (dev_bf16(t) for t in (inp.X, inp.A, inp.B, inp.G))
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        U = torch.empty((M, r), dtype=torch.bfloat16, device="cuda")
+        dX = torch.empty((M, K), dtype=torch.bfloat16, device="cuda")
+        dA = torch.empty((r, K), dtype=torch.float32, device="cuda")
+        dB = torch.empty((N, r), dtype=torch.float32, device="cuda")
+        wf = torch.empty(q.fwd_workspace_bytes(M, N, K, r), dtype=torch.uint8, device="cuda")
+        wb = torch.empty(q.bwd_workspace_bytes(M, N, K, r), dtype=torch.uint8, device="cuda")
+
+        def step():
+            q.qlora_linear_fwd(qw, X, A, B, 2.0 * r, Y=Y, U_save=U, workspace=wf)
+            q.qlora_linear_bwd(qw, X, A, B, 2.0 * r, G, U, dX=dX, dA=dA, dB=dB, workspace=wb)
+
+        step()
+        torch.cuda.synchronize()
+        ref = [t.clone() for t in (Y, U, dX, dA, dB)]
+        for t in (Y, U, dX, dA, dB):
+            t.zero_()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(graph, stream=s):
+                step()
+        torch.cuda.current_stream().wait_stream(s)
+        graph.replay()
+        torch.cuda.synchronize()
+        q.check_device_error()
+        for name, a, b in zip(("Y", "U", "dX", "dA", "dB"), (Y, U, dX, dA, dB), ref):
+            assert torch.equal(a, b), (M, name)
