@@ -214,7 +214,8 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // 2-D row-major tensor [outer, inner] of `esize`-byte elements with row stride `ld` elements.
 static bool make_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int esize, uint64_t inner,
-                     uint64_t outer, uint64_t ld, uint32_t box_inner, uint32_t box_outer, bool swz128) {
+                     uint64_t outer, uint64_t ld, uint32_t box_inner, uint32_t box_outer, bool swz128,
+                     CUtensorMapSwizzle swz_other = CU_TENSOR_MAP_SWIZZLE_NONE) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {inner, outer};
@@ -222,17 +223,18 @@ static bool make_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, i
     cuuint32_t box[2] = {box_inner, box_outer};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(m, dt, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    swz128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                    swz128 ? CU_TENSOR_MAP_SWIZZLE_128B : swz_other, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 static bool map_bf16(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, uint32_t bi, uint32_t bo) {
     return make_map(m, base, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, inner, outer, inner, bi, bo, true);
 }
-// the fused kernel's bf16 output [rows, cols], stored through TMA in [32][128] tiles
+// the fused kernel's bf16 output [rows, cols], stored through TMA by each epilogue warp in
+// 64-byte-swizzled [32 tokens][32 features] tiles
 static bool map_out(CUtensorMap *m, const void *out, int64_t rows, int64_t cols) {
-    return make_map(m, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)cols, (uint64_t)rows, (uint64_t)cols, 128u,
-                    32u, false);
+    return make_map(m, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)cols, (uint64_t)rows, (uint64_t)cols, 32u,
+                    32u, false, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 static bool map_codes(CUtensorMap *m, const void *codes, int64_t N, int64_t K, bool dx) {
     return make_map(m, codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)K / 2, (uint64_t)N, (uint64_t)K / 2,

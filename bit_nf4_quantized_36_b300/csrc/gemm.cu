@@ -363,15 +363,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFusedThreads, 1)
             if (!okw) break;
             tc_fence_after();
             const int64_t f = ((int64_t)ui.w_tile * 2 + rank) * 128 + quarter * 32 + lane;
-            const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)a * 256u;
             const int nchunks = kMT * p.BN / 32;
             for (int cc = 0; cc < nchunks; ++cc) {
                 const int i = cc / (p.BN / 32), c = cc % (p.BN / 32);  // token tile, 32-column chunk
                 const int m0 = (ui.m_tile * kMT + i) * p.BN;
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(taddr + (uint32_t)i * 256u + (uint32_t)c * 32u, r);
-                tmem_ld_wait();
+                const uint32_t tcol = tmem_base + (uint32_t)a * 256u + (uint32_t)i * 256u + (uint32_t)c * 32u;
                 if (kMT == 2 && p.splits == 1) {
+                    // this warp's 32 features x 32 tokens as two accumulator fragments (features
+                    // 16h .. 16h + 15 of the warp), written to shared memory transposed by stmatrix
+                    uint32_t v[2][16];
+                    tmem_ld_16x256b_x4(tcol + ((uint32_t)(quarter * 32) << 16), v[0]);
+                    tmem_ld_16x256b_x4(tcol + ((uint32_t)(quarter * 32 + 16) << 16), v[1]);
+                    tmem_ld_wait();
                     if (cc == nchunks - 1) {
                         // the accumulator is read out: the next unit's MMAs may start
                         tc_fence_before();
@@ -381,25 +384,46 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFusedThreads, 1)
                             else mbar_arrive_remote(acc_empty_leader + (uint32_t)a * 8u);
                         }
                     }
-                    // [32 tokens][128 features] through shared memory, one TMA store per chunk
-                    const int et = threadIdx.x - kEpiWarp0 * 32;
-                    uint8_t *buf = sOut + (cc & 1) * (kOutStageBytes / 2);
-                    if (et == 0) bulk_wait_group_read<1>();  // the store two chunks back has read buf
-                    named_barrier_sync(1, 128);
-                    const uint32_t col = (uint32_t)(quarter * 32 + lane) * 2u;
+                    // each warp stages its [32 tokens][32 features] in its own double-buffered,
+                    // 64-byte-swizzled 2 KB tile and stores it with one TMA store: no barrier
+                    // between the epilogue warps
+                    uint8_t *buf = sOut + (quarter * 2 + (cc & 1)) * (kOutStageBytes / 8);
+                    if (lane == 0) bulk_wait_group_read<1>();  // this warp's store two chunks back has read buf
+                    __syncwarp();
+                    {
+                        const int mi = lane >> 3, j = lane & 7;  // this thread addresses row j of matrix mi
+                        const uint32_t buf_addr = smem_u32(buf);
 #pragma unroll
-                    for (int jj = 0; jj < 32; ++jj) {
-                        __nv_bfloat16 h = __float2bfloat16_rn(__uint_as_float(r[jj]));
-                        *reinterpret_cast<__nv_bfloat16 *>(buf + jj * 256 + col) = h;
+                        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                            for (int kk = 0; kk < 2; ++kk) {
+                                // matrices: features (top, bottom 8 of 16 h .. 16 h + 15) x tokens
+                                // 8 k .. 8 k + 7, k = 2 kk, 2 kk + 1
+                                const int k = 2 * kk + (mi >> 1), bot = mi & 1;
+                                const int tok = 8 * k + j;
+                                const int ch = 2 * h + bot;  // 16-byte chunk of the token's 64-byte row
+                                const uint32_t addr = buf_addr + (uint32_t)tok * 64u +
+                                                      ((uint32_t)(ch ^ ((tok >> 1) & 3)) << 4);
+                                const uint32_t *w = v[h] + 8 * kk;
+                                stmatrix_x4_trans(addr, bf16x2(__uint_as_float(w[0]), __uint_as_float(w[1])),
+                                                  bf16x2(__uint_as_float(w[2]), __uint_as_float(w[3])),
+                                                  bf16x2(__uint_as_float(w[4]), __uint_as_float(w[5])),
+                                                  bf16x2(__uint_as_float(w[6]), __uint_as_float(w[7])));
+                            }
+                        }
                     }
                     fence_proxy_async_smem();
-                    named_barrier_sync(1, 128);
-                    if (et == 0) {
-                        tma_store_2d(&map_out, buf, (int)(((int64_t)ui.w_tile * 2 + rank) * 128), m0 + c * 32);
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&map_out, buf, (int)(((int64_t)ui.w_tile * 2 + rank) * 128) + quarter * 32,
+                                     m0 + c * 32);
                         bulk_commit_group();
                     }
                     continue;
                 }
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(tcol + ((uint32_t)(quarter * 32) << 16), r);
+                tmem_ld_wait();
                 if (f < p.wdim) {
                     if (p.splits == 1) {
 #pragma unroll
@@ -428,7 +452,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFusedThreads, 1)
             }
         }
         // the output stores have completed before the CTA exits
-        if (kMT == 2 && threadIdx.x == kEpiWarp0 * 32) bulk_wait_group_all();
+        if (kMT == 2 && lane == 0) bulk_wait_group_all();
     } else {
         // ------------------------------ decode warps -------------------------------------
         // Two groups of four warps take alternate pipeline stages (stage s always goes to
