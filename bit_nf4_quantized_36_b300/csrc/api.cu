@@ -413,7 +413,7 @@ qlora_status qlora_merge(const qlora_nf4_tensor *W, const uint16_t *A, const uin
     if (!make_map(&mCodes, W->codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)K / 2, (uint64_t)N, (uint64_t)K / 2,
                   128u, 128u, false) ||
         !map_bf16(&mB, Bq, r_vec ? r : r8, N, 64, 128) || !map_bf16(&mA, A, K, r, 64, 64) ||
-        !map_bf16(&mOut, W_out, K, N, 64, 128))
+        !map_bf16(&mOut, W_out, K, N, 64, 32))
         return QLORA_ERR_CUDA;
     return from_cuda(launch_merge(mCodes, mB, mA, mOut, W->scale_codes, W->scale_scales, W->scale_offset, N, K, r,
                                   alpha / (float)r, tables(), sms, st));
@@ -594,7 +594,7 @@ static qlora_status layer_bwd(const qlora_nf4_tensor *W, const uint16_t *X, int6
         !map_out(&mDX, dX, M, K))
         return QLORA_ERR_CUDA;
     if (d && (!map_bf16(&mV_k, V, w.r8, M, 64, 128) || !map_bf16(&mA_mn, A, K, r, 64, 64) ||
-              !map_bf16(&mDX_sw, dX, K, M, 64, 128)))
+              !map_bf16(&mDX_sw, dX, K, M, 64, 32)))
         return QLORA_ERR_CUDA;
 
     cudaError_t e;

@@ -34,7 +34,8 @@ static constexpr uint32_t kMrgBBytes = 128u * 128u;        // 128 rows x 64 rank
 static constexpr uint32_t kMrgABytes = 4u * 64u * 128u;    // 4 MN blocks of 64 k x 64 rank, SW128
 static constexpr uint32_t kMrgOpBytes = kMrgBBytes + kMrgABytes;
 static constexpr uint32_t kMrgCodesBytes = 128u * 128u;    // 128 rows x 256 codes
-static constexpr uint32_t kMrgOutBytes = 128u * 128u;      // 128 rows x 64 bf16, SW128
+static constexpr uint32_t kMrgOutBytes = 128u * 128u;      // staging: 128 rows x 64 bf16, SW128
+static constexpr uint32_t kMrgWarpOutBytes = 32u * 128u;   // one epilogue warp's 32 rows of it
 static constexpr uint32_t kMrgSmem = 2 * kMrgOpBytes + 2 * kMrgCodesBytes + 4 * kMrgOutBytes + 256;
 
 struct MergeArgs {
@@ -243,9 +244,11 @@ __global__ void __launch_bounds__(kMrgThreads, 1)
             for (int g = 0; g < 2; ++g, ++store_n) {
                 uint32_t lo[4], hi[4];
                 if (kMode == 0) build_table(sc[g], p.tab, lo, hi);
-                uint8_t *buf = sOut + (half * 2 + (store_n & 1)) * kMrgOutBytes;
-                if (et == 0) bulk_wait_group_read<1>();  // the store two groups back has read buf
-                named_barrier_sync(1 + half, 128);
+                // each warp stages its own 32 rows (double-buffered) and stores them with one TMA
+                // store: no barrier between the epilogue warps
+                uint8_t *buf = sOut + ((warp - kMrgEpiWarp0) * 2 + (store_n & 1)) * kMrgWarpOutBytes;
+                if (lane == 0) bulk_wait_group_read<1>();  // this warp's store two groups back has read buf
+                __syncwarp();
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
                     uint32_t r[32];
@@ -278,14 +281,14 @@ __global__ void __launch_bounds__(kMrgThreads, 1)
                             o[e] = bf16x2(t0, t1);
                         }
                         // 16-byte chunk (4 c + w) of this row's 128 bytes, 128-byte swizzle
-                        st_shared_v4(smem_u32(buf) + (uint32_t)row * 128u + ((((uint32_t)(4 * c + w)) ^ r7) << 4),
+                        st_shared_v4(smem_u32(buf) + (uint32_t)lane * 128u + ((((uint32_t)(4 * c + w)) ^ r7) << 4),
                                      make_uint4(o[0], o[1], o[2], o[3]));
                     }
                 }
                 fence_proxy_async_smem();
-                named_barrier_sync(1 + half, 128);
-                if (et == 0) {
-                    tma_store_2d(&map_out, buf, k0 + half * 128 + g * 64, n0);
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(&map_out, buf, k0 + half * 128 + g * 64, n0 + quarter * 32);
                     bulk_commit_group();
                 }
             }
@@ -297,7 +300,7 @@ __global__ void __launch_bounds__(kMrgThreads, 1)
                 if (kMode == 0) mbar_arrive(&codes_empty[a]);
             }
         }
-        if (et == 0) bulk_wait_group_all();
+        if (lane == 0) bulk_wait_group_all();
     }
 
     tc_fence_before();

@@ -67,8 +67,8 @@ cudaError_t launch_small(bool dx, const CUtensorMap &map_codes, const CUtensorMa
 // map_scales: rebuilt block scales, fp32 {N, KB} (transposed, [KB][N]); box {128, 1} or {64, 2}
 // map_act   : X [M, K] (forward) or G [M, N] (backward), bf16, box {64, BN/2}, 128-byte swizzle
 // map_lora  : U or V [M, ld] bf16, box {64, BN/2}, 128-byte swizzle (columns >= r read as 0)
-// map_out   : the output [M, wdim] bf16, box {128, 32}, no swizzle (two-tile pair units store
-//             through it)
+// map_out   : the output [M, wdim] bf16, box {32, 32}, 64-byte swizzle (two-tile pair units store
+//             through it, one box per epilogue warp and 32-token chunk)
 cudaError_t launch_fused(bool dx, const CUtensorMap &map_codes, const CUtensorMap &map_scales,
                          const CUtensorMap &map_act, const CUtensorMap &map_lora, const CUtensorMap &map_out,
                          const FusedArgs &args, const FusedPlan &plan, cudaStream_t st);
@@ -117,7 +117,7 @@ cudaError_t launch_gemv(const uint8_t *codes, const int8_t *scale_q, const float
 // ---- adapter merge (merge.cu): W_m = bf16(W^ + s B A) -----------------------------------
 // map_codes: codes {K/2, N} u8, box {128, 128}; map_b: B [N, rb] bf16, box {64, 128}, 128-byte
 // swizzle; map_a: A [r, K] bf16, box {64, 64}, 128-byte swizzle; map_out: W_m [N, K] bf16, box
-// {64, 128}, 128-byte swizzle.
+// {64, 32}, 128-byte swizzle (one box per epilogue warp and 64-column group).
 cudaError_t launch_merge(const CUtensorMap &map_codes, const CUtensorMap &map_b, const CUtensorMap &map_a,
                          const CUtensorMap &map_out, const int8_t *scale_q, const float *scale_c2,
                          const float *scale_mu, int64_t N, int64_t K, int r, float s, const NF4Tables &tab,
@@ -130,7 +130,7 @@ cudaError_t launch_dropout_x(const uint16_t *X, int64_t n, uint64_t seed, uint64
                              uint32_t *mask_bits, int num_sms, cudaStream_t st);
 // dX[m, k] = bf16(dX0[m, k] + kept(m, k) / (1 - p) * (V A)[m, k]) in place (dx0 = the dX buffer);
 // map_v: V [M, rv] bf16, box {64, 128}, 128-byte swizzle; map_a: A [r, K] bf16, box {64, 64},
-// 128-byte swizzle; map_dx: dX [M, K] bf16, box {64, 128}, 128-byte swizzle; r = rv.
+// 128-byte swizzle; map_dx: dX [M, K] bf16, box {64, 32}, 128-byte swizzle; r = rv.
 cudaError_t launch_dropout_dx(const CUtensorMap &map_v, const CUtensorMap &map_a, const CUtensorMap &map_dx,
                               const uint16_t *dx0, const uint32_t *mask_bits, float p_drop, int64_t M, int64_t K,
                               int r, int num_sms, cudaStream_t st);
