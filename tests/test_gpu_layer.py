@@ -207,3 +207,51 @@ def test_graph_capture_replays_the_stream_results():
         q.check_device_error()
         for name, a, b in zip(("Y", "U", "dX", "dA", "dB"), (Y, U, dX, dA, dB), ref):
             assert torch.equal(a, b), (M, name)
+
+
+def test_concurrent_host_threads_on_their_own_streams():
+    """Two host threads run fwd + bwd of different layers on their own streams at once: the
+    library's side streams are shared per device (their enqueue is serialised), and every result
+    equals that of the same call made alone."""
+    import threading
+    shapes = [(600, 520, 640, 16), (300, 264, 384, 8)]
+    layers = []
+    for i, (M, N, K, r) in enumerate(shapes):
+        inp = synth.layer_inputs(220 + i, M, N, K, r, 2.0 * r)
+        qw = q.nf4_quantize(torch.from_numpy(inp.W).cuda())
+        X, A, B, G = (dev_bf16(t) for t in (inp.X, inp.A, inp.B, inp.G))
+        layers.append((qw, X, A, B, G, 2.0 * r))
+    torch.cuda.synchronize()
+
+    def run(layer):
+        qw, X, A, B, G, alpha = layer
+        Y, U = q.qlora_linear_fwd(qw, X, A, B, alpha)
+        dX, dA, dB = q.qlora_linear_bwd(qw, X, A, B, alpha, G, U)
+        return [t for t in (Y, U, dX, dA, dB)]
+
+    ref = [run(layer) for layer in layers]
+    torch.cuda.synchronize()
+    out = [None, None]
+    errors = []
+
+    def worker(i):
+        try:
+            s = torch.cuda.Stream()
+            with torch.cuda.stream(s):
+                for _ in range(20):
+                    res = run(layers[i])
+                s.synchronize()
+            out[i] = res
+        except Exception as e:  # surfaced below
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    q.check_device_error()
+    for i in range(2):
+        for a, b in zip(out[i], ref[i]):
+            assert torch.equal(a, b), i
