@@ -657,19 +657,24 @@ def run_ncu_target(args):
     bench workload (--ncu-target fused), three small-M forwards on a 70B MLP matrix
     (--ncu-target decode), three AdamW steps over the Llama-3-8B adapter set with the moments
     in plain device memory (--ncu-target adamw; the same kernel as with paged moments), or three
-    quantizations of a 28672 x 8192 matrix (--ncu-target quantize)."""
+    quantizations or dequantizations of a 28672 x 8192 matrix (--ncu-target quantize, dequantize)."""
     import torch
 
     import bit_nf4_quantized_36_b300 as q
     from bit_nf4_quantized_36_b300 import synth
     dev = torch.device("cuda")
-    if args.ncu_target == "quantize":
+    if args.ncu_target in ("quantize", "dequantize"):
         W = synth.sweep_weight_gpu(0, 4, 28672, 8192)
+        qw = q.nf4_quantize(W)
+        What = q.nf4_dequantize(qw)
         for _ in range(3):
-            qw = q.nf4_quantize(W)
+            if args.ncu_target == "quantize":
+                q.nf4_quantize(W, out=qw)
+            else:
+                q.nf4_dequantize(qw, out=What)
         torch.cuda.synchronize()
         q.check_device_error()
-        print(json.dumps({"ncu_target": "quantize", "rows": 28672, "cols": 8192, "ok": True}))
+        print(json.dumps({"ncu_target": args.ncu_target, "rows": 28672, "cols": 8192, "ok": True}))
         return 0
     if args.ncu_target == "adamw":
         n = synth.adapter_param_count()
@@ -713,7 +718,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch the timed steps on the stream, not as a graph")
-    ap.add_argument("--ncu-target", choices=["fused", "decode", "adamw", "quantize"], default=None,
+    ap.add_argument("--ncu-target", choices=["fused", "decode", "adamw", "quantize", "dequantize"], default=None,
                     help="untimed short run of one kernel family, for profiler captures")
     ap.add_argument("--decode-m", type=int, default=1)
     args = ap.parse_args()

@@ -287,10 +287,14 @@ __global__ void __launch_bounds__(kEncodeThreads) dq_encode_kernel(const float *
 }
 
 // ---------------------------------------------------------------------------------------
-// K3: dequantize.  One thread per 8 weights (one 32-bit word of codes -> one 16-byte store).
+// K3: dequantize.  One thread per 8 weights (one 32-bit word of codes -> one 16-byte store) per
+// step, four steps' loads in flight before any of them is used: warp-coalesced loads and stores,
+// and enough of the code stream in flight per thread.
 //   s'_b = fmaf(q_b, fl32(c2_g / 127), mu);  W^ = bf16_rne(fl32(NF4[c] * s'_b))
 // ---------------------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) nf4_dequantize_kernel(const uint32_t *__restrict__ codes32,
+static constexpr int kDqUnroll = 4;
+
+__global__ void __launch_bounds__(256, 8) nf4_dequantize_kernel(const uint32_t *__restrict__ codes32,
                                                              const int8_t *__restrict__ qcode,
                                                              const float *__restrict__ c2,
                                                              const float *__restrict__ mu_ptr, int64_t n8,
@@ -299,20 +303,35 @@ __global__ void __launch_bounds__(256) nf4_dequantize_kernel(const uint32_t *__r
     if (threadIdx.x < 16) L[threadIdx.x] = tab.level[threadIdx.x];
     __syncthreads();
     const float mu = *mu_ptr;
-    for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < n8; t += (int64_t)gridDim.x * blockDim.x) {
-        const uint32_t x = __ldcs(codes32 + t);
-        const int64_t b = t >> 3;
-        const float s = __fmaf_rn((float)qcode[b], __fdiv_rn(c2[b >> 8], 127.0f), mu);
-        uint32_t w[4];
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t t0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t0 < n8; t0 += kDqUnroll * stride) {
+        uint32_t x[kDqUnroll];
+        int32_t qb[kDqUnroll];
+        float cg[kDqUnroll];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const uint32_t byte = (x >> (8 * j)) & 0xFFu;
-            const float e0 = __fmul_rn(L[byte >> 4], s);   // element 2j   (high nibble)
-            const float e1 = __fmul_rn(L[byte & 15u], s);  // element 2j+1 (low nibble)
-            __nv_bfloat162 p = __floats2bfloat162_rn(e0, e1);
-            w[j] = *reinterpret_cast<uint32_t *>(&p);
+        for (int u = 0; u < kDqUnroll; ++u) {
+            const int64_t t = t0 + u * stride;
+            const bool in = t < n8;
+            x[u] = in ? __ldcs(codes32 + t) : 0u;
+            qb[u] = in ? (int32_t)qcode[t >> 3] : 0;
+            cg[u] = in ? c2[t >> 11] : 0.0f;
         }
-        __stcs(out + t, make_uint4(w[0], w[1], w[2], w[3]));
+#pragma unroll
+        for (int u = 0; u < kDqUnroll; ++u) {
+            const int64_t t = t0 + u * stride;
+            if (t >= n8) break;
+            const float s = __fmaf_rn((float)qb[u], __fdiv_rn(cg[u], 127.0f), mu);
+            uint32_t w[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t byte = (x[u] >> (8 * j)) & 0xFFu;
+                const float e0 = __fmul_rn(L[byte >> 4], s);   // element 2j   (high nibble)
+                const float e1 = __fmul_rn(L[byte & 15u], s);  // element 2j+1 (low nibble)
+                __nv_bfloat162 p = __floats2bfloat162_rn(e0, e1);
+                w[j] = *reinterpret_cast<uint32_t *>(&p);
+            }
+            __stcs(out + t, make_uint4(w[0], w[1], w[2], w[3]));
+        }
     }
 }
 
