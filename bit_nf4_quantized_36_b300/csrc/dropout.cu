@@ -23,39 +23,54 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint2 k) {
 }
 
 // x_d[e] = bf16(x[e] * inv) where kept, 0 where dropped; mask_bits (nullable): bit e % 32 of word
-// e / 32 set where element e is kept.  One thread per block of 4 elements (n % 128 == 0).
+// e / 32 set where element e is kept.  One thread per block of 4 elements and step; the loads of
+// kDropUnroll steps are issued before any is used (the stream is otherwise latency-bound).
+static constexpr int kDropUnroll = 4;
+
 __global__ void __launch_bounds__(256)
     dropout_x_kernel(const uint16_t *__restrict__ X, int64_t n, uint64_t seed, uint64_t offset, uint32_t thr,
                      float inv, uint16_t *__restrict__ Xd, uint32_t *__restrict__ mask_bits) {
     const uint2 key = make_uint2((uint32_t)seed, (uint32_t)(seed >> 32));
     const int64_t nblk = n / 4;
-    for (int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; b - (threadIdx.x & 31) < nblk;
-         b += (int64_t)gridDim.x * blockDim.x) {
-        uint32_t nib = 0;
-        if (b < nblk) {
-            const uint4 w = philox4x32_10(make_uint4((uint32_t)b, (uint32_t)((uint64_t)b >> 32), (uint32_t)offset,
-                                                     (uint32_t)(offset >> 32)),
-                                          key);
-            const uint2 xv = *reinterpret_cast<const uint2 *>(X + 4 * b);
-            const uint32_t words[4] = {w.x, w.y, w.z, w.w};
-            const uint32_t xs[4] = {xv.x & 0xffffu, xv.x >> 16, xv.y & 0xffffu, xv.y >> 16};
-            uint32_t o[4];
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    // warp-uniform loop: the mask gathering below shuffles across lanes
+    for (int64_t b0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; b0 - (threadIdx.x & 31) < nblk;
+         b0 += kDropUnroll * stride) {
+        uint2 xv[kDropUnroll];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const bool keep = words[i] >= thr;
-                nib |= (keep ? 1u : 0u) << i;
-                __nv_bfloat16 h = __float2bfloat16_rn(keep ? __fmul_rn(__uint_as_float(xs[i] << 16), inv) : 0.0f);
-                o[i] = *reinterpret_cast<uint16_t *>(&h);
-            }
-            *reinterpret_cast<uint2 *>(Xd + 4 * b) = make_uint2(o[0] | (o[1] << 16), o[2] | (o[3] << 16));
+        for (int u = 0; u < kDropUnroll; ++u) {
+            const int64_t b = b0 + u * stride;
+            xv[u] = b < nblk ? *reinterpret_cast<const uint2 *>(X + 4 * b) : make_uint2(0u, 0u);
         }
-        if (mask_bits) {
-            // eight lanes cover 32 consecutive elements: gather their nibbles into one word
-            uint32_t word = nib << (4 * (threadIdx.x & 7));
-            word |= __shfl_xor_sync(0xffffffffu, word, 1);
-            word |= __shfl_xor_sync(0xffffffffu, word, 2);
-            word |= __shfl_xor_sync(0xffffffffu, word, 4);
-            if ((threadIdx.x & 7) == 0 && b < nblk) mask_bits[b / 8] = word;
+#pragma unroll
+        for (int u = 0; u < kDropUnroll; ++u) {
+            const int64_t b = b0 + u * stride;
+            if (b - (threadIdx.x & 31) >= nblk) break;  // uniform over the warp
+            uint32_t nib = 0;
+            if (b < nblk) {
+                const uint4 w = philox4x32_10(make_uint4((uint32_t)b, (uint32_t)((uint64_t)b >> 32), (uint32_t)offset,
+                                                         (uint32_t)(offset >> 32)),
+                                              key);
+                const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+                const uint32_t xs[4] = {xv[u].x & 0xffffu, xv[u].x >> 16, xv[u].y & 0xffffu, xv[u].y >> 16};
+                uint32_t o[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const bool keep = words[i] >= thr;
+                    nib |= (keep ? 1u : 0u) << i;
+                    __nv_bfloat16 h = __float2bfloat16_rn(keep ? __fmul_rn(__uint_as_float(xs[i] << 16), inv) : 0.0f);
+                    o[i] = *reinterpret_cast<uint16_t *>(&h);
+                }
+                *reinterpret_cast<uint2 *>(Xd + 4 * b) = make_uint2(o[0] | (o[1] << 16), o[2] | (o[3] << 16));
+            }
+            if (mask_bits) {
+                // eight lanes cover 32 consecutive elements: gather their nibbles into one word
+                uint32_t word = nib << (4 * (threadIdx.x & 7));
+                word |= __shfl_xor_sync(0xffffffffu, word, 1);
+                word |= __shfl_xor_sync(0xffffffffu, word, 2);
+                word |= __shfl_xor_sync(0xffffffffu, word, 4);
+                if ((threadIdx.x & 7) == 0 && b < nblk) mask_bits[b / 8] = word;
+            }
         }
     }
 }
