@@ -330,15 +330,26 @@ def run_ours(args):
     # One process on one GPU: the K timed steps (flushes and events included) are captured once
     # into a CUDA graph and replayed, as a training loop would replay its step; every kernel of
     # every step still runs.  Under torchrun the all-reduces stay outside a graph.
+    graph_note = None
     if use_graph:
-        cap = torch.cuda.Stream()
-        cap.wait_stream(torch.cuda.current_stream())
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(cap):
-            with torch.cuda.graph(graph, stream=cap):
-                timed_steps()
-        torch.cuda.current_stream().wait_stream(cap)
-        barrier()
+        try:
+            cap = torch.cuda.Stream()
+            cap.wait_stream(torch.cuda.current_stream())
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(cap):
+                with torch.cuda.graph(graph, stream=cap):
+                    timed_steps()
+            torch.cuda.current_stream().wait_stream(cap)
+            barrier()
+        except Exception as e:  # keep a measurement: the same steps launched on the stream
+            use_graph = False
+            graph_note = f"graph capture failed ({type(e).__name__}); stream launches"
+            torch.cuda.synchronize()
+            n0 = q.launch_count()
+            L.qlora_set_kernel_timer(None, 0)
+            if L.qlora_set_kernel_timer(ctypes.cast(kev_arr, ctypes.c_void_p), 2 * Ksteps) != 0:
+                raise RuntimeError("qlora_set_kernel_timer rejected the events")
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(Ksteps)]
     with sampler:
         if use_graph:
             graph.replay()
@@ -435,7 +446,7 @@ def run_ours(args):
                            "step": "nf4_quantize + nf4_dequantize + qlora_linear_fwd + qlora_linear_bwd",
                            "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write, outside the step events)",
                            "launch": ("the K timed steps captured in one CUDA graph, replayed once" if use_graph
-                                      else "stream launches"),
+                                      else graph_note or "stream launches"),
                            "parallelism": f"dp{world}"},
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
                 "gpu_launches_per_step": launches / Ksteps, "clocks": clocks,

@@ -161,10 +161,23 @@ class Fork {
     explicit Fork(cudaStream_t caller) : st_(caller), ss_(side_streams()) {
         if (ss_) lock_ = std::unique_lock<std::mutex>(ss_->mu);
     }
+    // A call that returns early (an error after some side work was enqueued) still leaves the
+    // caller's stream ordered after everything it enqueued on the side streams.
+    ~Fork() {
+        if (!ss_) return;
+        for (int i = 0; i < 3; ++i)
+            if (pending_ & (1u << i)) (void)link(i < 2 ? ss_->s[i] : ss_->hp, st_);
+        (void)cudaGetLastError();
+    }
     cudaError_t link(cudaStream_t from, cudaStream_t to) {
         if (!ss_ || from == to) return cudaSuccess;
         cudaError_t e = cudaEventRecord(ss_->ev, from);
         if (e == cudaSuccess) e = cudaStreamWaitEvent(to, ss_->ev, 0);
+        if (e == cudaSuccess) {
+            // work enqueued on a side stream after it waited is pending until it is linked back
+            if (to != st_) pending_ |= bit(to);
+            if (to == st_) pending_ &= ~bit(from);
+        }
         return e;
     }
     cudaError_t fork() {
@@ -178,8 +191,12 @@ class Fork {
     cudaError_t join(int i) { return link(side(i), st_); }
 
   private:
+    uint32_t bit(cudaStream_t x) const {
+        return x == ss_->s[0] ? 1u : x == ss_->s[1] ? 2u : x == ss_->hp ? 4u : 0u;
+    }
     cudaStream_t st_;
     SideStreams *ss_;
+    uint32_t pending_ = 0;  // side streams forked from the caller and not yet joined back
     std::unique_lock<std::mutex> lock_;
 };
 
