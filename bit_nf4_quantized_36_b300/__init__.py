@@ -502,3 +502,11 @@ class PagedAdamW:
 
 def check_device_error(stream=None) -> None:
     _check(_lib.load().qlora_check_device_error(_stream(stream)), "device error word")
+
+
+def test_inject(flags: int) -> None:
+    """Failure-path test hook of the library (qlora_test_inject); 0 switches it off."""
+    _check(_lib.load().qlora_test_inject(int(flags)), "test_inject")
+
+
+test_inject.__test__ = False  # a library hook, not a pytest test

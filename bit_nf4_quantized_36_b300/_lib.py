@@ -21,12 +21,14 @@ EXPORTS = (
     "qlora_cat_fwd_workspace_bytes", "qlora_cat_bwd_workspace_bytes", "qlora_linear_fwd_cat", "qlora_linear_bwd_cat",
     "qlora_fwd_dropout_workspace_bytes", "qlora_bwd_dropout_workspace_bytes", "qlora_linear_fwd_dropout",
     "qlora_linear_bwd_dropout",
-    "qlora_check_device_error", "qlora_status_string", "qlora_launch_count", "qlora_nf4_levels",
+    "qlora_check_device_error", "qlora_test_inject", "qlora_status_string", "qlora_launch_count",
+    "qlora_nf4_levels",
     "qlora_set_kernel_timer", "qlora_kernel_timer_count", "nf4_quantize_noalloc",
     "qlora_paged_alloc", "qlora_paged_free", "qlora_paged_prefetch", "qlora_adamw_step",
 )
 
 QLORA_PAGE_HOST = -1
+QLORA_INJECT_SKIP_CODES = 1
 
 
 class NF4TensorStruct(ctypes.Structure):
@@ -83,6 +85,7 @@ def load():
         "qlora_linear_fwd": (ctypes.c_int, [ST, P, I64, P, P, I32, ctypes.c_float, P, P, P, SZ, P]),
         "qlora_linear_bwd": (ctypes.c_int, [ST, P, I64, P, P, I32, ctypes.c_float, P, P, P, P, P, P, SZ, P]),
         "qlora_check_device_error": (ctypes.c_int, [P]),
+        "qlora_test_inject": (ctypes.c_int, [ctypes.c_uint32]),
         "qlora_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "qlora_launch_count": (ctypes.c_uint64, []),
         "qlora_nf4_levels": (None, [P]),

@@ -724,4 +724,9 @@ qlora_status qlora_check_device_error(void *stream) {
     return (word & kErrLayout) ? QLORA_ERR_CUDA : QLORA_OK;
 }
 
+qlora_status qlora_test_inject(uint32_t flags) {
+    if (flags & ~(uint32_t)QLORA_INJECT_SKIP_CODES) return QLORA_ERR_INVALID_ARG;
+    return cudaMemcpyToSymbol(g_inject, &flags, sizeof(flags)) == cudaSuccess ? QLORA_OK : QLORA_ERR_CUDA;
+}
+
 }  // extern "C"

@@ -237,6 +237,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFusedThreads, 1)
             bool issued[kStages];
             for (int i = 0; i < kStages; ++i) issued[i] = false, issued_parity[i] = 0;
             bool ok = true;
+            // test hook: no codes copy (and no arrival on full_c) for the first k-step of pair 0
+            bool skip_codes = leader && pair_id == 0 && (*(volatile uint32_t *)&g_inject & kInjectSkipCodes);
             for (int u = pair_id; u < total_units && ok; u += num_pairs) {
                 const UnitInfo ui = unit_info(p, u);
                 const int wt = ui.w_tile * 2 + (int)rank;  // this CTA's 128-row weight tile
@@ -245,7 +247,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFusedThreads, 1)
                     if (!mbar_wait_cl(&empty[s | kPairMask], ph ^ 1u, s_abort)) { ok = false; break; }
                     const bool lora = (ui.kt0 + j) >= ui.kt1;
                     if (leader) mbar_arrive_expect_tx(&full_b[s], 2u * bs_bytes);
-                    if (!lora) {
+                    if (skip_codes && !lora) {
+                        skip_codes = false;
+#pragma unroll
+                        for (int i = 0; i < kMT; ++i)
+                            tma_load_2d_pair(sB + s * bs_bytes + i * b_bytes, &map_act, full_b_leader + (uint32_t)s * 8u,
+                                             (ui.kt0 + j) * 64, m_row + i * p.BN);
+                    } else if (!lora) {
                         const int kt = ui.kt0 + j;
                         uint8_t *dc = sC + s * kCStageBytes;
                         mbar_arrive_expect_tx(&full_c[s], kCStageBytes);

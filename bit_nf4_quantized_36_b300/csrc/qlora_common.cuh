@@ -45,6 +45,11 @@ struct NF4Tables {
 enum : uint32_t { kErrTimeout = 1u, kErrLayout = 2u };
 // Defined here: the library is one translation unit (libqlora.cu includes every .cu file).
 __device__ uint32_t g_error_word = 0;
+// Test hook (qlora_test_inject): kInjectSkipCodes makes the leader CTA of the fused GEMM's first
+// pair skip the codes copy of its first k-step, and with it that stage's arrival on the barrier
+// its decode warps wait on, so the bounded wait runs out and the kernel unwinds without a fault.
+enum : uint32_t { kInjectSkipCodes = 1u };
+__device__ uint32_t g_inject = 0;
 
 __device__ __forceinline__ uint64_t globaltimer_ns() {
     uint64_t t;

@@ -264,6 +264,18 @@ qlora_status qlora_adamw_step(const qlora_adamw *hp, int64_t t, int64_t n, float
  * early; its outputs are undefined) or QLORA_ERR_CUDA. */
 qlora_status qlora_check_device_error(void *stream);
 
+/* Test hook for the device-side failure path (not for normal use).  flags ==
+ * QLORA_INJECT_SKIP_CODES makes every following launch of the fused NF4-dequant GEMM (layer
+ * calls with more than 32 tokens, forward and backward dX) on the current device leave out one
+ * copy of packed codes: the leader CTA of its first CTA pair issues no codes copy for its first
+ * k-step, so that stage's barrier never completes.  The decode warps' bounded wait then runs
+ * out (about 2 s), the kernel's roles drain and exit, and the next qlora_check_device_error
+ * returns QLORA_ERR_TIMEOUT; the call's outputs are undefined.  flags == 0 switches it off.
+ * Synchronous with respect to the host; do not change it while calls are in flight.  Returns
+ * QLORA_ERR_INVALID_ARG for an unknown flag, QLORA_ERR_CUDA if the device is unusable. */
+#define QLORA_INJECT_SKIP_CODES 1u
+qlora_status qlora_test_inject(uint32_t flags);
+
 /* Short English description of a status code (static string). */
 const char *qlora_status_string(qlora_status s);
 

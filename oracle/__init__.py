@@ -36,9 +36,11 @@ def build(force: bool = False) -> str:
 
 
 def lib():
+    """The compiled oracle; ORACLE_LIB names another build of nf4_oracle.c to load instead (the
+    sanitizer test runs the pins against an AddressSanitizer / UBSan build that way)."""
     global _lib
     if _lib is None:
-        _lib = ctypes.CDLL(build())
+        _lib = ctypes.CDLL(os.environ.get("ORACLE_LIB") or build())
         _declare(_lib)
     return _lib
 

@@ -150,6 +150,8 @@ def test_argument_errors_before_any_launch(L):
     assert L.qlora_paged_free(None) == 0
     assert L.qlora_paged_prefetch(None, 64, 0, None) == 1
     assert L.qlora_paged_prefetch(P(0x1000), 64, -2, None) == 1
+    # failure-path test hook: unknown flags are refused before the device is touched
+    assert L.qlora_test_inject(2) == 1 and L.qlora_test_inject(0xFFFFFFFF) == 1
     assert L.qlora_launch_count() == 0  # nothing above reached a kernel launch
 
 
