@@ -248,6 +248,36 @@ def traffic_from_profile(gemm_src_sha):
         return None
 
 
+def host_link_ms(torch, s_in, s_out, ins, outs, reps=10):
+    """Time of one step's host copies alone: every (device, pinned host) input pair copied in on
+    s_in while every (pinned host, device) result pair is copied out on s_out."""
+    ins, outs = list(ins), list(outs)
+    cur = torch.cuda.current_stream()
+
+    def once():
+        s_in.wait_stream(cur)
+        s_out.wait_stream(cur)
+        with torch.cuda.stream(s_in):
+            for d, h in ins:
+                d.copy_(h, non_blocking=True)
+        with torch.cuda.stream(s_out):
+            for h, d in outs:
+                h.copy_(d, non_blocking=True)
+        cur.wait_stream(s_in)
+        cur.wait_stream(s_out)
+
+    for _ in range(2):
+        once()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        once()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / reps
+
+
 def run_ours(args):
     import torch
 
@@ -465,6 +495,12 @@ def run_ours(args):
            "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "copies": pipe_note,
            "serial": {"value": world * flops / (serial_ms * 1e-3) / 1e12, "ms_per_step": serial_ms,
                       "copies": "inputs, step and results one after another on one stream"}}
+    try:  # the bound of the end-to-end step: the same copies alone, both directions at once
+        link_ms = host_link_ms(torch, s_in, s_out, zip(ins[1], hosts_in), zip(outs_h, outs[1]))
+        e2e["link"] = {"ms_per_step": link_ms, "frac": link_ms / e2e_ms,
+                       "what": "the step's input and result copies alone, in and out at once (no GPU work)"}
+    except Exception as e:
+        e2e["link"] = {"error": repr(e)}
     q.check_device_error()
 
     extras = {}
