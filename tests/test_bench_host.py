@@ -1,0 +1,40 @@
+"""Host-side pieces of bench.py that need no GPU: the FLOP count behind the headline number,
+the ncu traffic lookup and its source-hash guard, and the roofline denominators."""
+import json
+import os
+import re
+
+import bench
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_layer_flops_is_the_sum_of_the_step_products():
+    """2 m n k for every product of one forward and backward: Y = X W^T, U = X A^T, U B^T;
+    dX = dY W, V = dY B, V A; dA = V^T X, dB = dY^T U."""
+    for M, N, K, r in [(4096, 4096, 4096, 16), (8192, 14336, 4096, 64), (16, 256, 512, 8), (3, 5, 7, 2)]:
+        products = [(M, N, K), (M, r, K), (M, N, r),
+                    (M, K, N), (M, r, N), (M, K, r),
+                    (r, K, M), (N, r, M)]
+        assert bench.layer_flops(M, N, K, r) == sum(2.0 * m * n * k for m, n, k in products)
+
+
+def test_traffic_lookup_follows_the_recorded_kernel_hash():
+    text = open(os.path.join(ROOT, "profiles", "fused_gemm_llama8b_attn.md")).read()
+    sha = re.search(r"kernel_source_sha256: `([0-9a-f]{64})`", text).group(1)
+    dram = float(re.search(r"dram_bytes_per_launch_avg: `(\d+)`", text).group(1))
+    assert bench.traffic_from_profile(sha) == dram
+    assert bench.traffic_from_profile("0" * 64) is None
+    # the hash covers a non-empty stretch of the kernel source
+    assert re.fullmatch(r"[0-9a-f]{64}", bench.fused_kernel_source_sha() or "")
+
+
+def test_peaks_come_from_the_measured_file():
+    p = bench.load_peaks()
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        m = json.load(open(path))
+        assert p["source"] == "measured"
+        assert p["hbm_gbs"] == m["hbm_gbs"] and p["bf16_tflops"] == m["bf16_tflops"]
+    else:
+        assert p["source"] == "fallback"
