@@ -484,6 +484,8 @@ def run_ours(args):
         barrier()
         e2e_ms = p0.elapsed_time(p1) / e2e_steps
     except Exception as e:  # keep the serial measurement as the end-to-end number
+        if dist is not None:
+            raise  # a rank that fell back alone would leave the others waiting at a barrier
         torch.cuda.synchronize()
         e2e_ms = serial_ms
         pipe_note = f"serial (the pipelined form failed: {type(e).__name__})"
