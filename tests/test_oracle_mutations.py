@@ -1,0 +1,124 @@
+"""The pins can tell a wrong oracle from a right one.
+
+Each case below plants one plausible mistake in a copy of oracle/nf4_oracle.c: a dropped
+term, a wrong sign, index or operand, a rounding taken twice, a tie broken the other way, an
+off-by-one in a table. The mutated copy is built like the oracle and the whole pin suite
+(tests/test_oracle_pins.py) runs against it in a child process. Every mutant must fail at least
+one pin. The copies live in a temporary directory; the oracle itself is never modified."""
+import os
+import subprocess
+import sys
+from concurrent.futures import ThreadPoolExecutor
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "nf4_oracle.c")
+
+# (name, text in the oracle, replacement): the first occurrence is replaced
+MUTANTS = [
+    ("Phi^-1 without the sqrt(2) of the normal tail",
+     "0.5 * erfc(x / sqrt(2.0))", "0.5 * erfc(x / 2.0)"),
+    ("NF4 negative half on 9 points instead of 8",
+     "-orc_norm_ppf(lin(top, 0.5, 8, j))", "-orc_norm_ppf(lin(top, 0.5, 9, j))"),
+    ("int4 absmax codes truncated instead of rounded",
+     "float c = nearbyintf(t); /* default rounding mode", "float c = truncf(t); /* default rounding mode"),
+    ("nearest-level ties to the higher index",
+     "if (d < bd) { bd = d; best = k; }", "if (d <= bd) { bd = d; best = k; }"),
+    ("all-zero block coded as level 0 instead of the zero level",
+     "codes[b * bs + i] = (uint8_t)zero_idx;", "codes[b * bs + i] = (uint8_t)0;"),
+    ("nibble order swapped in packing",
+     "packed[j] = (uint8_t)((codes[2 * j] << 4) | (codes[2 * j + 1] & 0xF));",
+     "packed[j] = (uint8_t)((codes[2 * j + 1] << 4) | (codes[2 * j] & 0xF));"),
+    ("mean of the block scales divided by one block too many",
+     "return (float)(total / (double)nb);", "return (float)(total / (double)(nb + 1));"),
+    ("scale codes on 128 steps instead of 127",
+     "float t = (d / m) * 127.0f;", "float t = (d / m) * 128.0f;"),
+    ("rebuilt scale rounded twice (multiply, then add)",
+     "return fmaf((float)q, k, mu);", "return (float)q * k + mu;"),
+    ("bf16 ties rounded up instead of to even",
+     "else pick = ((lo_bits >> 16) & 1u) ? hi_bits : lo_bits;", "else pick = hi_bits;"),
+    ("dequantization reads the nibbles in the other order",
+     "int c = (i % 2 == 0) ? (byte >> 4) : (byte & 0xF);", "int c = (i % 2 == 0) ? (byte & 0xF) : (byte >> 4);"),
+    ("storage size without the fp32 offset",
+     "return n / 2 + nb + 4 * ng + 4;", "return n / 2 + nb + 4 * ng;"),
+    ("forward without the alpha / r scale on the adapter term",
+     "Y_out[ii * N + n] = base + s * lora;", "Y_out[ii * N + n] = base + lora;"),
+    ("dX with the adapter term subtracted",
+     "dX_out[ii * K + k] = row[k] + s * lora;", "dX_out[ii * K + k] = row[k] - s * lora;"),
+    ("dA without the alpha / r scale",
+     "dA_out[j * K + k] = s * acc;", "dA_out[j * K + k] = acc;"),
+    ("dB from V instead of U",
+     "acc += orc_bf16_to_double(G[m * N + n]) * U[m * r + j];",
+     "acc += orc_bf16_to_double(G[m * N + n]) * V[m * r + j];"),
+    ("merge without the alpha / r scale",
+     "orc_bf16_to_double(What[n * K + k]) + s * acc", "orc_bf16_to_double(What[n * K + k]) + acc"),
+    ("Philox with nine rounds",
+     "for (int round = 0; round < 10; ++round)", "for (int round = 0; round < 9; ++round)"),
+    ("dropout without the 1 / (1 - p) rescale of kept elements",
+     "double keep_scale = 1.0 / (1.0 - p);", "double keep_scale = 1.0;"),
+    ("AdamW without the first moment's bias correction",
+     "p[i] -= lr * (m[i] / bc1)", "p[i] -= lr * (m[i])"),
+    ("AdamW weight decay not scaled by the learning rate",
+     "p[i] *= 1.0 - lr * wd;", "p[i] *= 1.0 - wd;"),
+    ("AdamW second moment fed g instead of g^2",
+     "(1.0 - b2) * g[i] * g[i];", "(1.0 - b2) * g[i];"),
+    ("AdamW epsilon inside the square root",
+     "(sqrt(v[i] / bc2) + eps)", "sqrt(v[i] / bc2 + eps)"),
+    ("NF4 table divided by the second-largest level",
+     "double mx = v[15];", "double mx = v[14];"),
+    ("group constant without the mean subtracted",
+     "float d = fabsf(s[b] - mu);", "float d = fabsf(s[b]);"),
+    ("scale codes truncated instead of rounded",
+     "float r = nearbyintf(t);", "float r = truncf(t);"),
+    ("fp64 -> bf16 ties rounded up instead of to even",
+     "else pick = (fmod(lo / step, 2.0) == 0.0) ? lo : hi;", "else pick = hi;"),
+    ("forward reads A transposed",
+     "acc += orc_bf16_to_double(X[m * K + k]) * orc_bf16_to_double(A[j * K + k]);",
+     "acc += orc_bf16_to_double(X[m * K + k]) * orc_bf16_to_double(A[k * r + j]);"),
+    ("dX reads B transposed in V = G B",
+     "for (int64_t n = 0; n < N; ++n) acc += orc_bf16_to_double(G[m * N + n]) * orc_bf16_to_double(B[n * r + j]);",
+     "for (int64_t n = 0; n < N; ++n) acc += orc_bf16_to_double(G[m * N + n]) * orc_bf16_to_double(B[j * N + n]);"),
+    ("dX reads A transposed in V A",
+     "for (int64_t j = 0; j < r; ++j) lora += v[j] * orc_bf16_to_double(A[j * K + k]);",
+     "for (int64_t j = 0; j < r; ++j) lora += v[j] * orc_bf16_to_double(A[k * r + j]);"),
+    ("merge rounded through fp32 (twice)",
+     "out[n * K + k] = orc_bf16_round_d(orc_bf16_to_double(What[n * K + k]) + s * acc);",
+     "out[n * K + k] = orc_bf16_round((float)(orc_bf16_to_double(What[n * K + k]) + s * acc));"),
+    ("Philox with the first Weyl constant for both key words",
+     "k1 += 0xBB67AE85u;", "k1 += 0x9E3779B9u;"),
+    ("dropout takes word 0 of every block",
+     "D[e] = (w[e % 4] >= thr) ? keep_scale : 0.0;", "D[e] = (w[0] >= thr) ? keep_scale : 0.0;"),
+    ("dropout dX without the mask on the adapter term",
+     "dX_out[ii * K + k] = row[k] + D[m * K + k] * s * lora;", "dX_out[ii * K + k] = row[k] + s * lora;"),
+    ("dropout dA without the mask on X",
+     "acc += V[m * r + j] * orc_bf16_to_double(X[m * K + k]) * D[m * K + k];",
+     "acc += V[m * r + j] * orc_bf16_to_double(X[m * K + k]);"),
+]
+
+
+def _run_mutant(tmp, i, old, new, src):
+    assert old in src, f"mutation site not found: {old!r}"
+    path = os.path.join(tmp, f"mutant{i}.c")
+    so = os.path.join(tmp, f"libmutant{i}.so")
+    with open(path, "w") as f:
+        f.write(src.replace(old, new, 1))
+    subprocess.run(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared", "-o", so,
+                    path, "-lm"], check=True, capture_output=True)
+    env = dict(os.environ, ORACLE_LIB=so)
+    r = subprocess.run([sys.executable, "-m", "pytest", os.path.join(ROOT, "tests", "test_oracle_pins.py"), "-x", "-q",
+                        "-p", "no:cacheprovider"], env=env, cwd=ROOT, capture_output=True, text=True, timeout=900)
+    return r.returncode
+
+
+def test_every_planted_mistake_fails_a_pin(tmp_path):
+    if os.environ.get("ORACLE_LIB"):
+        pytest.skip("this process already runs another build of the oracle")
+    src = open(SRC).read()
+    workers = max(1, min(8, os.cpu_count() or 1))
+    with ThreadPoolExecutor(workers) as ex:
+        codes = list(ex.map(lambda a: _run_mutant(str(tmp_path), a[0], a[1][1], a[1][2], src), enumerate(MUTANTS)))
+    survivors = [name for (name, _, _), rc in zip(MUTANTS, codes) if rc == 0]
+    assert not survivors, f"mutants no pin catches: {survivors}"
+    # a failing pin (exit 1), not a crash or a usage error, is what stopped each run
+    assert all(rc == 1 for rc in codes), list(zip([m[0] for m in MUTANTS], codes))

@@ -313,6 +313,29 @@ def test_storage_bits_closed_form(orc):
     assert abs(gb - float(g["gb_65b_approx"][0])) < 1.0
 
 
+def test_storage_bytes_by_enumeration(orc):
+    """Brute force on small matrices, counted item by item as the stored format lists them: a
+    4-bit code per weight, an int8 scale code per 64-weight block, an fp32 constant per started
+    group of 256 blocks, and the fp32 mean of the scales once per matrix. The shapes include a
+    last group that is only partly filled."""
+    for rows, cols in [(1, 64), (64, 64), (3, 4096), (257, 128), (1024, 1024)]:
+        bits = 0
+        blocks = 0
+        for w in range(rows * cols):
+            bits += 4
+            if w % 64 == 63:
+                blocks += 1
+                bits += 8
+                if blocks % 256 == 1:   # the first block of a group opens it
+                    bits += 32
+        bits += 32                      # the mean
+        assert orc.nf4_storage_bytes(rows, cols) * 8 == bits, (rows, cols)
+        # and the quantizer's outputs are exactly those items
+        q = orc.nf4_quantize(np.zeros((rows, cols), F32))
+        stored = q["packed"].nbytes + q["qcode"].nbytes + q["c2"].nbytes + np.float32(q["mu"]).nbytes
+        assert stored * 8 == bits, (rows, cols)
+
+
 # ----------------------------------------------------------------------------------------
 # The layer: explicit effective matrix, finite differences, special cases
 # ----------------------------------------------------------------------------------------
@@ -483,6 +506,22 @@ def test_merge_ties_round_to_even(orc):
     assert np.all(orc.merge(What, A, B1, 1.0) == 0x3F80)
     B3 = np.array([[orc.bf16_round(3 * 2.0 ** -8)]], dtype=np.uint16)     # 1 + 3 2^-8: a tie
     assert np.all(orc.merge(What, A, B3, 1.0) == 0x3F82)
+
+
+def test_merge_rounds_once_from_the_exact_sum(orc):
+    """W^ + s B A just above a bf16 midpoint by less than half an fp32 ulp: rounded once (the
+    reading) it goes up; rounded through fp32 first it would land on the midpoint and go to
+    even.  Both signs, and in another binade."""
+    A = np.full((2, 64), 0x3F80, dtype=np.uint16)                            # 1.0
+    for w_bits, sign in ((0x3F80, 1.0), (0xBF80, -1.0), (0x4100, 1.0)):      # 1, -1, 8
+        w = float(orc.bf16_to_f64(np.array([w_bits], np.uint16))[0])
+        half_ulp = abs(w) * 2.0 ** -8                                         # bf16 midpoint offset
+        B = np.array([[orc.bf16_round(sign * half_ulp), orc.bf16_round(sign * abs(w) * 2.0 ** -30)]] * 1,
+                     dtype=np.uint16)
+        What = np.full((1, 64), w_bits, dtype=np.uint16)
+        got = orc.merge(What, A, B, 2.0)                                      # s = 1
+        away = w_bits + 1                                                     # the next bf16 magnitude
+        assert np.all(got == away), (hex(w_bits), hex(int(got[0, 0])))
 
 
 # ---------------------------------------------------------------------------------------
