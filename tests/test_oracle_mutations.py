@@ -94,6 +94,43 @@ MUTANTS = [
     ("dropout dA without the mask on X",
      "acc += V[m * r + j] * orc_bf16_to_double(X[m * K + k]) * D[m * K + k];",
      "acc += V[m * r + j] * orc_bf16_to_double(X[m * K + k]);"),
+    ("int4 absmax from the signed maximum",
+     "for (int64_t i = 0; i < n; ++i) if (fabsf(w[i]) > am) am = fabsf(w[i]);",
+     "for (int64_t i = 0; i < n; ++i) if (w[i] > am) am = w[i];"),
+    ("NF4 block absmax from the signed maximum",
+     "for (int64_t i = 0; i < bs; ++i) if (fabsf(blk[i]) > am) am = fabsf(blk[i]);",
+     "for (int64_t i = 0; i < bs; ++i) if (blk[i] > am) am = blk[i];"),
+    ("nearest level by signed difference",
+     "        float d = fabsf(x - levels[k]);", "        float d = x - levels[k];"),
+    ("degenerate group coded 1 instead of 0",
+     "if (m == 0.0f) { q[b] = 0; continue; }", "if (m == 0.0f) { q[b] = 1; continue; }"),
+    ("group sums of the mean accumulated in fp32",
+     "        double acc = 0.0;\n        int64_t b1", "        float acc = 0.0f;\n        int64_t b1"),
+    ("dequantization always takes group 0's constant",
+     "int64_t b = i / 64, g = b / 256;", "int64_t b = i / 64, g = 0 * b;"),
+    ("rebuilt scale step c2 / 128",
+     "float k = c2 / 127.0f;", "float k = c2 / 128.0f;"),
+    ("fp32 -> bf16 never rounds up past a non-tie",
+     "else if (dhi < dlo) pick = hi_bits;", "else if (dhi < 0.0) pick = hi_bits;"),
+    ("forward scale alpha / (r + 1)",
+     "double s = alpha / (double)r;", "double s = alpha / (double)(r + 1);"),
+    ("dA from U instead of V",
+     "acc += V[m * r + j] * orc_bf16_to_double(X[m * K + k]);",
+     "acc += U[m * r + j] * orc_bf16_to_double(X[m * K + k]);"),
+    ("Philox mixes the key words the other way round",
+     "uint32_t n0 = hi1 ^ c1 ^ k0, n1 = lo1, n2 = hi0 ^ c3 ^ k1, n3 = lo0;",
+     "uint32_t n0 = hi1 ^ c1 ^ k1, n1 = lo1, n2 = hi0 ^ c3 ^ k0, n3 = lo0;"),
+    ("dropout threshold on 2^31",
+     "uint32_t thr = (uint32_t)floor(p * 4294967296.0);", "uint32_t thr = (uint32_t)floor(p * 2147483648.0);"),
+    ("dropout counter with the element index and the offset swapped",
+     "uint32_t ctr[4] = {(uint32_t)blk, (uint32_t)(blk >> 32), (uint32_t)offset, (uint32_t)(offset >> 32)};",
+     "uint32_t ctr[4] = {(uint32_t)offset, (uint32_t)(offset >> 32), (uint32_t)blk, (uint32_t)(blk >> 32)};"),
+    ("AdamW without the second moment's bias correction",
+     "(sqrt(v[i] / bc2) + eps)", "(sqrt(v[i]) + eps)"),
+    ("AdamW first moment without the (1 - beta1) factor",
+     "m[i] = b1 * m[i] + (1.0 - b1) * g[i];", "m[i] = b1 * m[i] + g[i];"),
+    ("unpacking swaps the nibbles of the second code",
+     "codes[2 * j + 1] = (uint8_t)(packed[j] & 0xF);", "codes[2 * j + 1] = (uint8_t)(packed[j] >> 4);"),
 ]
 
 

@@ -296,6 +296,24 @@ def test_dequantize_definition_small(orc):
     assert np.all(np.abs(Wf - W) <= bound + 1e-7)
 
 
+def test_dequantize_definition_several_groups(orc):
+    """The same definition over 512 blocks in two groups of different magnitude, so that each
+    block must take its own group's constant c2_g."""
+    W = (np.random.default_rng(16).standard_normal((4, 8192)) * 0.02).astype(F32)
+    W[2:] *= 50.0                                    # the second group's scales are 50x larger
+    qz = orc.nf4_quantize(W)
+    # both constants measure from the common mean: they differ, though by less than 50x
+    assert qz["c2"].size == 2 and qz["c2"][1] > 1.5 * qz["c2"][0]
+    Wh = orc.nf4_dequantize(qz["packed"], qz["qcode"], qz["c2"], qz["mu"], 4, 8192).reshape(-1)
+    L = orc.nf4_levels()
+    codes = orc.unpack_nibbles(qz["packed"])
+    s = np.array([orc.dq_scale(int(qz["qcode"][b]), float(qz["c2"][b // 256]), float(qz["mu"]))
+                  for b in range(qz["qcode"].size)], dtype=F32)
+    v = (L[codes].astype(F32) * np.repeat(s, 64)).astype(F32)          # one fp32 rounding
+    want = torch.from_numpy(v).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    np.testing.assert_array_equal(Wh, want)
+
+
 def test_storage_bits_closed_form(orc):
     g = golden("storage_bits.txt")
     n = int(g["params"][0])
@@ -550,6 +568,13 @@ def test_dropout_mask_rate_and_layout(orc):
     for e in (0, 1, 2, 3, 4, 77, n - 1):
         w = orc.philox4x32_10([e // 4, 0, 0, 0], [1234, 0])[e % 4]
         assert keep.flat[e] == (int(w) >= thr)
+    # the full layout at p = 0.5 (every flag a coin toss, so a wrong word, counter or key shows):
+    # counter (e / 4 low, e / 4 high, offset low, offset high), key (seed low, seed high)
+    seed, offset = (7 << 32) | 0x1234, (5 << 32) | 3
+    Dh = orc.dropout_scale(seed, offset, 0.5, 8, 128)
+    for e in range(Dh.size):
+        w = orc.philox4x32_10([e // 4, 0, offset & 0xFFFFFFFF, offset >> 32], [seed & 0xFFFFFFFF, seed >> 32])[e % 4]
+        assert (Dh.flat[e] != 0) == (int(w) >= 2 ** 31), e
     # a different offset gives a different mask; p = 0.5: neighbouring flags look independent
     assert not np.array_equal(keep, orc.dropout_scale(1234, 1, p, 400, 512) != 0)
     k2 = orc.dropout_scale(99, 7, 0.5, 400, 512) != 0
