@@ -129,6 +129,14 @@ MUTANTS = [
      "(sqrt(v[i] / bc2) + eps)", "(sqrt(v[i]) + eps)"),
     ("AdamW first moment without the (1 - beta1) factor",
      "m[i] = b1 * m[i] + (1.0 - b1) * g[i];", "m[i] = b1 * m[i] + g[i];"),
+    ("merge reads A transposed",
+     "acc += orc_bf16_to_double(B[n * r + j]) * orc_bf16_to_double(A[j * K + k]);",
+     "acc += orc_bf16_to_double(B[n * r + j]) * orc_bf16_to_double(A[k * r + j]);"),
+    ("merge reads B transposed",
+     "acc += orc_bf16_to_double(B[n * r + j]) * orc_bf16_to_double(A[j * K + k]);",
+     "acc += orc_bf16_to_double(B[j * N + n]) * orc_bf16_to_double(A[j * K + k]);"),
+    ("sampled dB columns without the alpha / r scale",
+     "dB_cols[jj * N + n] = s * acc;", "dB_cols[jj * N + n] = acc;"),
     ("unpacking swaps the nibbles of the second code",
      "codes[2 * j + 1] = (uint8_t)(packed[j] & 0xF);", "codes[2 * j + 1] = (uint8_t)(packed[j] >> 4);"),
 ]

@@ -517,6 +517,28 @@ def test_merge_closed_form(orc):
                 assert got[n, k] == _bf16_of_fraction(w + delta)
 
 
+def test_merge_general_adapters_exact(orc):
+    """Non-uniform A and B (small multiples of powers of two, so B A is exact in fp64): every
+    element against W^ + s (B A)[n, k] summed in exact rationals over the rank and rounded once."""
+    from fractions import Fraction
+    rng = np.random.default_rng(13)
+    N, K, r, alpha = 5, 64, 3, 6.0                                   # s = 2
+    W = (rng.standard_normal((N, K)) * 0.05).astype(np.float32)
+    q = orc.nf4_quantize(W)
+    What = orc.nf4_dequantize(q["packed"], q["qcode"], q["c2"], q["mu"], N, K)
+    Av = rng.integers(-4, 5, size=(r, K)) * 2.0 ** -5
+    Bv = rng.integers(-4, 5, size=(N, r)) * 2.0 ** -7
+    A = np.array([[orc.bf16_round(x) for x in row] for row in Av], dtype=np.uint16)
+    B = np.array([[orc.bf16_round(x) for x in row] for row in Bv], dtype=np.uint16)
+    got = orc.merge(What, A, B, alpha)
+    s = Fraction(alpha) / r
+    for n in range(N):
+        for k in range(K):
+            w = Fraction(float(orc.bf16_to_f64(What[n, k:k + 1])[0]))
+            ba = sum(Fraction(Bv[n, j]) * Fraction(Av[j, k]) for j in range(r))
+            assert got[n, k] == _bf16_of_fraction(w + s * ba), (n, k)
+
+
 def test_merge_ties_round_to_even(orc):
     What = np.full((1, 64), 0x3F80, dtype=np.uint16)                     # 1.0
     A = np.full((1, 64), 0x3F80, dtype=np.uint16)
