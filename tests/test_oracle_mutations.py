@@ -137,6 +137,25 @@ MUTANTS = [
      "acc += orc_bf16_to_double(B[j * N + n]) * orc_bf16_to_double(A[j * K + k]);"),
     ("sampled dB columns without the alpha / r scale",
      "dB_cols[jj * N + n] = s * acc;", "dB_cols[jj * N + n] = acc;"),
+    ("dropout dB from the unmasked U",
+     "au += orc_bf16_to_double(X[m * K + k]) * D[m * K + k] * orc_bf16_to_double(A[j * K + k]);",
+     "au += orc_bf16_to_double(X[m * K + k]) * orc_bf16_to_double(A[j * K + k]);"),
+    ("int4 reconstruction on 8 steps",
+     "w_hat[i] = (c / 7.0f) * am;", "w_hat[i] = (c / 8.0f) * am;"),
+    ("MSE of the sum instead of the residual",
+     "double e = (double)(r - w[i]);", "double e = (double)(r + w[i]);"),
+    ("fp64 -> bf16 subnormal spacing one binade too fine",
+     "if (q < -133) q = -133;", "if (q < -134) q = -134;"),
+    ("fp64 -> bf16 overflows one binade early",
+     "if (pick >= ldexp(1.0, 128)) return (uint16_t)(sign | 0x7F80);",
+     "if (pick >= ldexp(1.0, 127)) return (uint16_t)(sign | 0x7F80);"),
+    ("fp32 -> bf16 overflow distance taken to the infinity pattern",
+     "double dhi = isinf(hi) ? fabs(ldexp(1.0, 128) - fabs((double)x)) : fabs((double)hi - (double)x);",
+     "double dhi = fabs((double)hi - (double)x);"),
+    ("mean's tree pairs elements i and i + len / 2",
+     "t[i] = t[2 * i] + t[2 * i + 1];", "t[i] = t[i] + t[i + len / 2];"),
+    ("NF4 top probability 0.96",
+     "const double top = 0.9677083;", "const double top = 0.96;"),
     ("unpacking swaps the nibbles of the second code",
      "codes[2 * j + 1] = (uint8_t)(packed[j] & 0xF);", "codes[2 * j + 1] = (uint8_t)(packed[j] >> 4);"),
 ]

@@ -221,6 +221,21 @@ def test_dq_mean_close_to_exact_mean(orc):
         assert abs(int(np.array(mu).view(np.int32)) - int(np.array(ref).view(np.int32))) <= 1
 
 
+def test_dq_mean_tree_order_worked_example(orc):
+    """The mean's rounding order (reading: in-order fp64 group sums, then a pairwise tree over
+    them, elements 2i and 2i + 1 at each level, then one rounding of total / nb to fp32), on four
+    groups built so that the order decides the fp32 result.  By hand, with S = (2^53 + 2^29, 1,
+    0, 1): S0 + S1 is a tie in fp64 (ulp 2) and stays 2^53 + 2^29; S2 + S3 = 1; their sum is the
+    same tie again, so the total is 2^53 + 2^29 and total / 1024 = 2^43 + 2^19, exactly half an
+    fp32 ulp above 2^43: ties to even give 2^43.  (Pairing S0 with S2 instead would keep both 1s,
+    give 2^43 + 2^19 + 2^-9 and round up to 2^43 + 2^20.)"""
+    s = np.zeros(1024, F32)
+    s[0], s[1] = 2.0 ** 53, 2.0 ** 29
+    s[256] = 1.0
+    s[768] = 1.0
+    assert float(orc.dq_mean(s)) == 2.0 ** 43
+
+
 def test_double_quant_invariants(orc):
     g = np.random.default_rng(12)
     s = np.abs(g.standard_normal(256 * 5 + 77) * 0.05).astype(F32) + F32(0.01)
