@@ -60,6 +60,19 @@ def test_all_equal_scales(orc):
     assert np.all(qw.scale_codes.cpu().numpy() == 0)
 
 
+def test_scale_mean_tree_order(orc):
+    """Block scales (2^53, 2^29 in group 0; 1 in groups 1 and 3; zeros elsewhere) for which the
+    pairing order of the mean's tree decides the fp32 mean (2^43 under the oracle's order): the
+    GPU's per-group chain and its subtree pairing must land on the same value."""
+    W = np.zeros((1, 1024 * 64), np.float32)
+    W[0, 0] = 2.0 ** 53
+    W[0, 64] = 2.0 ** 29
+    W[0, 256 * 64] = 1.0
+    W[0, 768 * 64] = 1.0
+    qw, ref = _check_roundtrip(orc, W)
+    assert float(ref["mu"]) == 2.0 ** 43
+
+
 def test_tiny_workload(orc):
     _check_roundtrip(orc, synth.tiny_inputs().W)
 
