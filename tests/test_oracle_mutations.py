@@ -156,6 +156,24 @@ MUTANTS = [
      "t[i] = t[2 * i] + t[2 * i + 1];", "t[i] = t[i] + t[i + len / 2];"),
     ("NF4 top probability 0.96",
      "const double top = 0.9677083;", "const double top = 0.96;"),
+    ("Phi^-1 without the sign for p < 1/2",
+     "double sign = (p < 0.5) ? -1.0 : 1.0;", "double sign = 1.0;"),
+    ("linspace divided by n instead of n - 1",
+     "return a + (b - a) * (double)i / (double)(n - 1); }", "return a + (b - a) * (double)i / (double)n; }"),
+    ("NF4 table sorted descending",
+     "while (j >= 0 && v[j] > x)", "while (j >= 0 && v[j] < x)"),
+    ("unpacking takes the low nibble for the first code",
+     "codes[2 * j] = (uint8_t)(packed[j] >> 4);", "codes[2 * j] = (uint8_t)(packed[j] & 0xF);"),
+    ("AdamW bias correction one step behind",
+     "double bc1 = 1.0 - pow(b1, (double)t)", "double bc1 = 1.0 - pow(b1, (double)(t + 1))"),
+    ("dropout key without the seed's high half",
+     "uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};", "uint32_t key[2] = {(uint32_t)seed, 0u};"),
+    ("dX reads W^ transposed",
+     "for (int64_t k = 0; k < K; ++k) row[k] += g * orc_bf16_to_double(What[n * K + k]);",
+     "for (int64_t k = 0; k < K; ++k) row[k] += g * orc_bf16_to_double(What[k * N + n]);"),
+    ("forward reads W^ transposed",
+     "for (int64_t k = 0; k < K; ++k) base += orc_bf16_to_double(X[m * K + k]) * orc_bf16_to_double(What[n * K + k]);",
+     "for (int64_t k = 0; k < K; ++k) base += orc_bf16_to_double(X[m * K + k]) * orc_bf16_to_double(What[k * N + n]);"),
     ("unpacking swaps the nibbles of the second code",
      "codes[2 * j + 1] = (uint8_t)(packed[j] & 0xF);", "codes[2 * j + 1] = (uint8_t)(packed[j] >> 4);"),
 ]

@@ -291,6 +291,17 @@ def test_bf16_round_matches_torch(orc):
     np.testing.assert_array_equal(got, want)
 
 
+def test_bf16_round_keeps_nan_a_nan(orc):
+    """NaN inputs (outside the layer's contract, which wants finite weights) must not turn into
+    infinities or numbers: whatever the payload, the result has an all-ones exponent and a
+    non-zero significand, and keeps its sign."""
+    for bits in (0x7F800001, 0x7FC00000, 0x7FA00000, 0x7F80FFFF, 0xFF800001, 0xFFFFFFFF):
+        x = np.array([bits], dtype=np.uint32).view(F32)[0]
+        h = int(orc.bf16_round(x))
+        assert (h & 0x7F80) == 0x7F80 and (h & 0x007F) != 0, hex(bits)
+        assert (h >> 15) == (bits >> 31), hex(bits)
+
+
 def test_dequantize_definition_small(orc):
     W = (np.random.default_rng(15).standard_normal((8, 128)) * 0.02).astype(F32)
     W[2, :64] = 0.0
