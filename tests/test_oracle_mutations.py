@@ -15,7 +15,8 @@ import pytest
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SRC = os.path.join(ROOT, "oracle", "nf4_oracle.c")
 
-# (name, text in the oracle, replacement): the first occurrence is replaced
+# (name, text in the oracle, replacement[, which occurrence, counted from 0]): one occurrence
+# is replaced, the first unless stated
 MUTANTS = [
     ("Phi^-1 without the sqrt(2) of the normal tail",
      "0.5 * erfc(x / sqrt(2.0))", "0.5 * erfc(x / 2.0)"),
@@ -174,17 +175,43 @@ MUTANTS = [
     ("forward reads W^ transposed",
      "for (int64_t k = 0; k < K; ++k) base += orc_bf16_to_double(X[m * K + k]) * orc_bf16_to_double(What[n * K + k]);",
      "for (int64_t k = 0; k < K; ++k) base += orc_bf16_to_double(X[m * K + k]) * orc_bf16_to_double(What[k * N + n]);"),
+    ("dropout forward applies the mask to the base term too",
+     "for (int64_t k = 0; k < K; ++k) base += orc_bf16_to_double(X[m * K + k]) * orc_bf16_to_double(What[n * K + k]);",
+     "for (int64_t k = 0; k < K; ++k) base += orc_bf16_to_double(X[m * K + k]) * D[m * K + k] * "
+     "orc_bf16_to_double(What[n * K + k]);", 1),
+    ("dropout forward reads B transposed",
+     "for (int64_t j = 0; j < r; ++j) lora += u[j] * orc_bf16_to_double(B[n * r + j]);",
+     "for (int64_t j = 0; j < r; ++j) lora += u[j] * orc_bf16_to_double(B[j * N + n]);", 1),
+    ("sampled dA rows without the alpha / r scale",
+     "dA_rows[jj * K + k] = s * acc;", "dA_rows[jj * K + k] = acc;"),
+    ("sampled grads read B transposed in V",
+     "for (int64_t n = 0; n < N; ++n) av += orc_bf16_to_double(G[m * N + n]) * orc_bf16_to_double(B[n * r + j]);",
+     "for (int64_t n = 0; n < N; ++n) av += orc_bf16_to_double(G[m * N + n]) * orc_bf16_to_double(B[j * N + n]);", 1),
+    ("dropout grads read B transposed in V",
+     "for (int64_t n = 0; n < N; ++n) av += orc_bf16_to_double(G[m * N + n]) * orc_bf16_to_double(B[n * r + j]);",
+     "for (int64_t n = 0; n < N; ++n) av += orc_bf16_to_double(G[m * N + n]) * orc_bf16_to_double(B[j * N + n]);", 2),
+    ("dropout dB without the alpha / r scale",
+     "dB_out[n * r + j] = s * acc;", "dB_out[n * r + j] = acc;", 1),
+    ("dropout dA without the alpha / r scale",
+     "dA_out[j * K + k] = s * acc;", "dA_out[j * K + k] = acc;", 1),
     ("unpacking swaps the nibbles of the second code",
      "codes[2 * j + 1] = (uint8_t)(packed[j] & 0xF);", "codes[2 * j + 1] = (uint8_t)(packed[j] >> 4);"),
 ]
 
 
-def _run_mutant(tmp, i, old, new, src):
-    assert old in src, f"mutation site not found: {old!r}"
+def _mutate(src, old, new, nth=0):
+    at = -1
+    for _ in range(nth + 1):
+        at = src.find(old, at + 1)
+        assert at >= 0, f"mutation site not found: {old!r} (occurrence {nth})"
+    return src[:at] + new + src[at + len(old):]
+
+
+def _run_mutant(tmp, i, mutant, src):
     path = os.path.join(tmp, f"mutant{i}.c")
     so = os.path.join(tmp, f"libmutant{i}.so")
     with open(path, "w") as f:
-        f.write(src.replace(old, new, 1))
+        f.write(_mutate(src, *mutant[1:]))
     subprocess.run(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared", "-o", so,
                     path, "-lm"], check=True, capture_output=True)
     env = dict(os.environ, ORACLE_LIB=so)
@@ -199,8 +226,8 @@ def test_every_planted_mistake_fails_a_pin(tmp_path):
     src = open(SRC).read()
     workers = max(1, min(8, os.cpu_count() or 1))
     with ThreadPoolExecutor(workers) as ex:
-        codes = list(ex.map(lambda a: _run_mutant(str(tmp_path), a[0], a[1][1], a[1][2], src), enumerate(MUTANTS)))
-    survivors = [name for (name, _, _), rc in zip(MUTANTS, codes) if rc == 0]
+        codes = list(ex.map(lambda a: _run_mutant(str(tmp_path), a[0], a[1], src), enumerate(MUTANTS)))
+    survivors = [m[0] for m, rc in zip(MUTANTS, codes) if rc == 0]
     assert not survivors, f"mutants no pin catches: {survivors}"
     # a failing pin (exit 1), not a crash or a usage error, is what stopped each run
     assert all(rc == 1 for rc in codes), list(zip([m[0] for m in MUTANTS], codes))

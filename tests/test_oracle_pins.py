@@ -657,6 +657,10 @@ def test_dropout_grads_finite_differences(orc):
     dA, dB = orc.layer_adapter_grads_drop(X, A, B, G, alpha, D)
     dX = orc.layer_dx_rows_drop(What, A, B, G, alpha, D)
     Xf, Af, Bf = f(X), f(A), f(B)
+    # the oracle's forward is the expression differentiated here (the mask on the adapter input
+    # only), evaluated with the adapters merged first: X W^T + s (X o D) (B A)^T
+    Yd, _ = orc.layer_fwd_rows_drop(What, X, A, B, alpha, D)
+    np.testing.assert_allclose(Yd, Xf @ f(What).T + s * (Xf * D) @ (Bf @ Af).T, rtol=1e-12, atol=1e-12)
     h = 1e-3
     for (j, k) in [(0, 0), (1, 17), (0, 63)]:
         E = np.zeros_like(Af)
