@@ -38,3 +38,23 @@ def test_peaks_come_from_the_measured_file():
         assert p["hbm_gbs"] == m["hbm_gbs"] and p["bf16_tflops"] == m["bf16_tflops"]
     else:
         assert p["source"] == "fallback"
+
+
+def test_reference_arm_prints_the_contract_line():
+    """`bench.py --impl reference` (the oracle on this host's cores) prints one JSON line with
+    the benchmark contract's keys, on the same metric and workload as the GPU arm."""
+    import subprocess
+    import sys
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                        "--warmup", "3"], cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == "TFLOP/s"
+    assert d["value"] > 0 and d["ms_per_step"] > 0 and d["higher_is_better"] is True
+    assert (d["steps"], d["warmup"], d["n_gpus"]) == (1, 3, 1)
+    assert d["config"]["workload"] == bench.WORKLOAD and d["vs_baseline"] is None and d["data"] == "synthetic"
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] == 1 and cb["value"] == d["value"] and cb["sample"]
+    e = d["e2e"]
+    assert e["value"] == d["value"] and e["unit"] == "TFLOP/s"
+    assert e["h2d_bytes_per_step"] == 0 and e["d2h_bytes_per_step"] == 0
