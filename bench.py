@@ -752,8 +752,8 @@ def hbm_extras(q, _lib, L, dev, peaks, flush):
         L.qlora_set_kernel_timer(None, 0)
         tk = statistics.median(kev[2 * i].elapsed_time(kev[2 * i + 1]) for i in range(10))
         byt = storage + 2 * r * (rows + cols) + 2 * M * (rows + cols)
-        dec[f"M={M}"] = {"call_ms": t, "kernel": ("nf4_gemv_fma_kernel" if M == 1 else "nf4_gemv_kernel") + " + gemv_finish_kernel"
-                         if M <= 8 else "nf4_lora_gemm_small_kernel", "kernel_ms": tk, "GB/s_kernel": byt / tk / 1e6,
+        dec[f"M={M}"] = {"call_ms": t, "kernel": "nf4_gemv_kernel" if M <= 8 else "nf4_lora_gemm_small_kernel",
+                         "kernel_ms": tk, "GB/s_kernel": byt / tk / 1e6,
                          "frac_hbm_kernel": byt / tk / 1e6 / peaks["hbm_gbs"], "GB/s_call": byt / t / 1e6}
     out["decode_forward_28672x8192_r16"] = dec
     out["hbm_peak_GB/s"] = f"{peaks['hbm_gbs']} ({peaks['source']})"
@@ -763,7 +763,8 @@ def hbm_extras(q, _lib, L, dev, peaks, flush):
 def run_ncu_target(args):
     """A short, untimed run for profiler captures: three forward+backward passes of the layer on the
     bench workload (--ncu-target fused), three small-M forwards on a 70B MLP matrix
-    (--ncu-target decode), three AdamW steps over the Llama-3-8B adapter set with the moments
+    (--ncu-target decode: the up projection 28672 x 8192; decode_down: the down projection
+    8192 x 28672), three AdamW steps over the Llama-3-8B adapter set with the moments
     in plain device memory (--ncu-target adamw; the same kernel as with paged moments), or three
     quantizations or dequantizations of a 28672 x 8192 matrix (--ncu-target quantize, dequantize)."""
     import torch
@@ -797,6 +798,8 @@ def run_ncu_target(args):
     if args.ncu_target == "fused":
         c = synth.LLAMA8B_ATTN
         M, N, K, r, alpha = c["M"], c["N"], c["K"], c["r"], c["alpha"]
+    elif args.ncu_target == "decode_down":
+        M, N, K, r, alpha = args.decode_m, 8192, 28672, 16, 32.0
     else:
         M, N, K, r, alpha = args.decode_m, 28672, 8192, 16, 32.0
     g = torch.Generator(device=dev)
@@ -826,7 +829,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch the timed steps on the stream, not as a graph")
-    ap.add_argument("--ncu-target", choices=["fused", "decode", "adamw", "quantize", "dequantize"], default=None,
+    ap.add_argument("--ncu-target", choices=["fused", "decode", "decode_down", "adamw", "quantize", "dequantize"],
+                    default=None,
                     help="untimed short run of one kernel family, for profiler captures")
     ap.add_argument("--decode-m", type=int, default=1)
     args = ap.parse_args()

@@ -257,6 +257,30 @@ static bool map_codes(CUtensorMap *m, const void *codes, int64_t N, int64_t K, b
     return make_map(m, codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)K / 2, (uint64_t)N, (uint64_t)K / 2,
                     dx ? 64u : 32u, dx ? 64u : 128u, false);
 }
+// the codes for the small-M forward: as a 3-D byte tensor {128 bytes of a row's 256-column unit,
+// row, unit} over the whole units only (strides K/2 and 128 bytes; one box is kGemvBoxRows rows x
+// kGemvBoxUnits units, stored unit by unit), and as the 2-D tensor {K/2, N} with boxes of one
+// unit (128 bytes x kGemvBoxRows rows) for slabs that are not eight whole units; 128-byte swizzle
+static bool map_codes_gemv(CUtensorMap *m3, CUtensorMap *m2, const void *codes, int64_t N, int64_t K) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const uint64_t whole = (uint64_t)(K / 256);
+    cuuint64_t dims[3] = {128u, (uint64_t)N, whole > 0 ? whole : 1u};
+    cuuint64_t strides[2] = {(uint64_t)K / 2, 128u};
+    cuuint32_t box[3] = {128u, (uint32_t)kGemvBoxRows, (uint32_t)kGemvBoxUnits};
+    cuuint32_t estr[3] = {1, 1, 1};
+    // (with no whole unit the 3-D map is never used; it is encoded over the first row's bytes)
+    if (whole == 0) {
+        dims[1] = 1;
+        dims[0] = (uint64_t)K / 2 >= 128 ? 128u : 16u;
+    }
+    CUresult r = fn(m3, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(codes), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return false;
+    return make_map(m2, codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)K / 2, (uint64_t)N, (uint64_t)K / 2, 128u,
+                    (uint32_t)kGemvBoxRows, true);
+}
 // rebuilt block scales, transposed [KB][N] fp32
 static bool map_scales(CUtensorMap *m, const float *sT, int64_t N, int64_t KB, bool dx) {
     return make_map(m, sT, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, (uint64_t)N, (uint64_t)KB, (uint64_t)N, dx ? 64u : 128u,
@@ -286,7 +310,7 @@ static QuantWs quant_ws(int64_t rows, int64_t cols) {
 
 struct LayerWs {
     int r8, r64;
-    bool gemv;  // forward with M <= 8: the register-resident GEMV instead of the fused kernel
+    bool gemv;  // forward with M <= 8: the one-launch small-M kernel instead of the fused kernel
     FusedPlan fp;
     ProjPlan pu, pv, pda, pdb;
     size_t off_scales, off_u, off_v, off_bpad, off_main, off_xd, off_mask, total;
@@ -304,7 +328,7 @@ static LayerWs layer_ws(int64_t M, int64_t N, int64_t K, int r, bool bwd, int nu
         w.fp = plan_fused(M, K, (N + 63) / 64, w.r64, num_sms);
     } else {
         w.fp = plan_fused(M, N, K / 64, w.r64, num_sms);
-        w.gemv = M <= 8;
+        w.gemv = gemv_supported(M, N, K);
     }
     size_t off = 0;
     w.off_scales = off;  // rebuilt block scales, for the CTA-pair kernel only
@@ -316,7 +340,7 @@ static LayerWs layer_ws(int64_t M, int64_t N, int64_t K, int r, bool bwd, int nu
     w.off_bpad = off;
     if (bwd && r % 8 != 0) off += align256((size_t)N * w.r8 * 2);
     w.off_main = off;
-    off += align256(w.gemv ? (size_t)gemv_slices(K) * M * N * 4 : w.fp.partial_bytes);
+    off += align256(w.gemv ? gemv_ws(N, K, r).total : w.fp.partial_bytes);
     // LoRA dropout: the masked adapter input, and (backward) its kept-element bits
     w.off_xd = off;
     if (drop) off += align256((size_t)M * K * 2);
@@ -525,6 +549,24 @@ static qlora_status layer_fwd(const qlora_nf4_tensor *W, const uint16_t *X, int6
     // the adapter branch's input: X, or X with the dropout mask applied
     const uint16_t *Xl = d ? reinterpret_cast<const uint16_t *>(base + w.off_xd) : X;
 
+    cudaError_t e;
+    if (w.gemv) {
+        // one launch: U = bf16(s Xl A^T), Y = X W^T + U B^T; its counters are cleared first
+        CUtensorMap mG3, mG2;
+        if (!map_codes_gemv(&mG3, &mG2, W->codes, N, K)) return QLORA_ERR_CUDA;
+        if (d && (e = launch_dropout_x(X, M * K, d->seed, d->offset, d->p, const_cast<uint16_t *>(Xl), nullptr, sms,
+                                       st)) != cudaSuccess)
+            return from_cuda(e);
+        const GemvWs gw = gemv_ws(N, K, r);
+        if ((e = cudaMemsetAsync(reinterpret_cast<uint8_t *>(mainp) + gw.off_counters, 0, gw.counter_bytes, st)) !=
+            cudaSuccess)
+            return from_cuda(e);
+        const int32_t ti = timer_open(st);
+        e = launch_gemv(mG3, mG2, W->scale_codes, W->scale_scales, W->scale_offset, X, Xl, (int)M, N, K, A, B, r, scale, Y,
+                        U_save, mainp, tables(), sms, st);
+        timer_close(ti, st);
+        return from_cuda(e);
+    }
     CUtensorMap mX_k, mA_k, mCodes, mScales, mX_act, mU_act, mY;
     std::memset(&mScales, 0, sizeof(mScales));
     if (!map_bf16(&mX_k, Xl, K, M, 64, 128) || !map_bf16(&mA_k, A, K, r, 64, w.r64) ||
@@ -534,7 +576,6 @@ static qlora_status layer_fwd(const qlora_nf4_tensor *W, const uint16_t *X, int6
         !map_out(&mY, Y, M, N))
         return QLORA_ERR_CUDA;
 
-    cudaError_t e;
     Fork fk(st);
     if ((e = fk.fork()) != cudaSuccess) return from_cuda(e);
     // the fused kernel's block scales, alongside the adapter product
@@ -551,13 +592,6 @@ static qlora_status layer_fwd(const qlora_nf4_tensor *W, const uint16_t *X, int6
     pu.out_h2 = U_save;
     if ((e = launch_proj(false, false, mX_k, mA_k, pu, st)) != cudaSuccess) return from_cuda(e);
     if ((e = fk.join(0)) != cudaSuccess) return from_cuda(e);
-    if (w.gemv) {
-        const int32_t ti = timer_open(st);
-        e = launch_gemv(W->codes, W->scale_codes, W->scale_scales, W->scale_offset, X, (int)M, N, K, mainp, U, w.r8, B,
-                        r, Y, tables(), sms, st);
-        timer_close(ti, st);
-        return from_cuda(e);
-    }
     // Y = X W^T + U B^T
     const FusedArgs fa = fused_args(W, M, w, r, B, r, Y, mainp, N);
     if ((e = timed_fused(false, mCodes, mScales, mX_act, mU_act, mY, fa, w.fp, sms, st)) != cudaSuccess)

@@ -106,13 +106,25 @@ ProjPlan plan_proj(int64_t Mp, int64_t Kc, int r64, int num_sms);
 cudaError_t launch_proj(bool p_mn, bool q_mn, const CUtensorMap &map_p, const CUtensorMap &map_q, const ProjArgs &args,
                         cudaStream_t st);
 
-// ---- forward for M <= 8, register-resident (gemv.cu) --------------------------------------
-// Y[m, n] = bf16(sum_k X[m, k] W^[n, k] + sum_j U[m, j] B[n, j]) for m < M (1..8), with W^ decoded
-// from the NF4 tensor's codes and int8 scale codes; partial: [gemv_slices(K), M, N] fp32.
-int gemv_slices(int64_t K);
-cudaError_t launch_gemv(const uint8_t *codes, const int8_t *scale_q, const float *scale_c2, const float *scale_mu,
-                        const uint16_t *X, int M, int64_t N, int64_t K, float *partial, const uint16_t *U, int ldu,
-                        const uint16_t *B, int r, uint16_t *Y, const NF4Tables &tab, int num_sms, cudaStream_t st);
+// ---- forward for M <= 8 in one launch (gemv.cu) ------------------------------------------
+// Y[m, n] = bf16(sum_b s'_b sum_{k in b} L[c_nk] X[m, k] + sum_j U[m, j] B[n, j]) and
+// U = bf16(s Xa A^T) (also to U_save when given) for m < M (1..8).  map3: the codes as a 3-D byte
+// tensor {128, N, floor(K/256)} (strides K/2, 128: the whole 256-column units only), box {128,
+// kGemvBoxRows, kGemvBoxUnits}; map2: the codes as a 2-D byte tensor {K/2, N}, box {128,
+// kGemvBoxRows}; both 128-byte swizzled.  ws: gemv_ws(N, K, r).total bytes, whose counters
+// (counter_bytes at off_counters) must be zero when the kernel starts.
+static constexpr int kGemvBoxRows = 32;
+static constexpr int kGemvBoxUnits = 8;
+bool gemv_supported(int64_t M, int64_t N, int64_t K);
+struct GemvWs {
+    int64_t RG;
+    size_t off_u, off_partial, off_counters, counter_bytes, total;
+};
+GemvWs gemv_ws(int64_t N, int64_t K, int r);
+cudaError_t launch_gemv(const CUtensorMap &map3, const CUtensorMap &map2, const int8_t *scale_q, const float *scale_c2,
+                        const float *scale_mu, const uint16_t *X, const uint16_t *Xa, int M, int64_t N, int64_t K,
+                        const uint16_t *A, const uint16_t *B, int r, float s, uint16_t *Y, uint16_t *U_save, void *ws,
+                        const NF4Tables &tab, int num_sms, cudaStream_t st);
 
 // ---- adapter merge (merge.cu): W_m = bf16(W^ + s B A) -----------------------------------
 // map_codes: codes {K/2, N} u8, box {128, 128}; map_b: B [N, rb] bf16, box {64, 128}, 128-byte

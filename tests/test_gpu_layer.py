@@ -93,6 +93,8 @@ def test_tiny_workload(orc):
     (1, 136, 2112, 3),     # one token, odd rank, ragged rows
     (7, 264, 4160, 16),    # seven tokens: eight token columns of the GEMV, one unused
     (8, 136, 2112, 3),     # eight tokens, ragged rows, a contraction tail inside a 256-step
+    (3, 72, 9216, 8),      # a row's five 2048-column slabs in two work items (partials added in order)
+    (1, 64, 8256, 8),      # the same with a 64-column tail unit (per-unit boxes for the last slab)
     (12, 264, 4160, 8),    # twelve tokens: the small-M tensor kernel
     (600, 520, 640, 16),   # two 256-token tiles per unit: token ranges that cross weight tiles
     (1100, 776, 384, 8),   # the same with more pairs, ragged tokens and weight rows
