@@ -23,8 +23,8 @@
 // The stream.  The codes are read in stages of 32 weight rows x 1 KB of each row (2048 columns,
 // one 3-D TMA box of eight 128-byte units), so that every row segment is one contiguous read: 128-byte
 // pieces of many rows fetched microseconds apart ran at a quarter of the HBM bandwidth.
-//   - One producer warp per CTA takes work items from a launch-wide counter (so an SM that gets
-//     its data late does less of the work), issues each stage's codes by TMA, and stores the
+//   - One producer warp per CTA takes the work items of W from a launch-wide counter (so an SM
+//     that gets its data late does less of the work), issues each stage's codes by TMA, and stores the
 //     stage's int8 scale codes (loaded into registers one stage ahead) with each row's group
 //     constants; each consumer rebuilds the s'_b it needs from them (the same fmaf as the
 //     dequantization).
@@ -35,9 +35,10 @@
 //   - A work item is one row group and up to four consecutive slabs (the warps add its stages up
 //     in registers, and x of the next stage is loaded during the current one); the CTAs working
 //     at the same time take neighbouring row groups.
-//   - The adapter's down product U = X A^T comes first in the item order (the rows of A, bf16, no
-//     decode), so it is finished by running CTAs before any weight item is taken; the term
-//     U B^T is added by the stage of each row group's last slab (bf16 B rows as the A operand).
+//   - The adapter's down product U = X A^T comes first: its items (the rows of A, bf16, no decode,
+//     one slab each) are the first items of the first CTAs, so U is done early and by many CTAs at
+//     once; the term U B^T is added by the stage of each row group's last slab (bf16 B rows as
+//     the A operand).
 //   - The last slab of a row group to finish (a counter per row group) hands the row group to the
 //     CTA's finisher warp, which adds its partials in slab order (so the result is deterministic)
 //     and writes bf16 Y (or, for the rows of A, publishes bf16(s X A^T)).
@@ -55,30 +56,32 @@ static constexpr int kGvSub = 256;                      // contraction columns p
 static constexpr int kGvSlab = kGvCW;                   // units per stage (slab = 2048 columns)
 static_assert(kGvSlab == kGemvBoxUnits, "one TMA box per stage");
 static constexpr int kGvRun = 4;                        // slabs per work item (of one row group)
-static constexpr int kGvStages = 3;
+static constexpr int kGvStages = 4;
 static constexpr int kGvMaxM = 8;
 static constexpr int kGvAcc = 8;                        // fp32 sums per lane: 2 tiles x (2 rows x 2 tokens)
 static constexpr int kGvRQ = 4;                         // work items' warp sums in flight to the finisher
-// stage layout (bytes from the stage base)
-static constexpr uint32_t kGvBoxBytes = kGvRows * 128;                   // one unit's codes
-static constexpr uint32_t kGvOffQ = kGvSlab * kGvBoxBytes;     // int8 scale codes [32 rows][32 blocks]
-static constexpr uint32_t kGvOffK = kGvOffQ + kGvRows * 32;      // per row {k0, k1, jsplit, jvalid}
-static constexpr uint32_t kGvOffDesc = kGvOffK + kGvRows * 16;   // int4 {kind, rg, slab, item},
-                                                                 // int4 {last of item, next kind, next slab, 0}
-static constexpr uint32_t kGvStageBytes = (kGvOffDesc + 32 + 1023) & ~1023u;
+// Shared memory.  A stage's codes (32 rows x 8 units, 32 KB) sit in a slot of their own; its
+// small parts sit in a side area per slot: the int8 scale codes [32 rows][32 blocks], per row
+// {k0, k1, jsplit, jvalid}, and the descriptor {kind, rg, slab, item}, {last of item, next kind,
+// next slab, flags}.
+static constexpr uint32_t kGvBoxBytes = kGvRows * 128;           // one unit's codes
+static constexpr uint32_t kGvStageBytes = kGvSlab * kGvBoxBytes;  // 32 KB
+static constexpr uint32_t kGvSideQ = 0, kGvSideK = kGvRows * 32, kGvSideDesc = kGvSideK + kGvRows * 16;
+static constexpr uint32_t kGvSideBytes = 2048;
+static_assert(kGvSideDesc + 32 <= kGvSideBytes, "side area");
 // The level-pair table sits at shared-window address 0x10000, so that one byte permute forms a
 // complete address (0x10000 | code byte << 8 | lane << 2).  It uses the first 128 bytes of each
 // 256-byte row; the other halves hold the consumer warps' sums on their way to the finisher
-// (entry (stage slot, warp, element): one half-row, one word per lane, kGvRQ slots).  Stage 0
-// sits below the table, the other stages and the barriers above it.
+// (entry (ring slot, warp, element): one half-row, one word per lane, kGvRQ slots).  Slot 0, the
+// side areas and the barriers sit below the table, slots 1 .. kGvStages - 1 above it.
 static constexpr uint32_t kGvTable = 0x10000u;
 static constexpr uint32_t kGvTableEnd = 0x20000u;
 static constexpr uint32_t kGvMaxBase = 8192u;           // largest dynamic shared memory start allowed
-static_assert(kGvMaxBase + kGvStageBytes <= kGvTable, "stage 0 below the table");
-static_assert(kGvRQ * kGvCW * kGvAcc <= 256, "warp sums fit the table's free half-rows");
-static constexpr uint32_t kGvOffBars = kGvTableEnd + (kGvStages - 1) * kGvStageBytes;
 static constexpr uint32_t kGvTailBytes = 8 * (2 * kGvStages + 2 * kGvRQ) + 16 * kGvRQ + 16;
-static constexpr uint32_t kGvDynBytes = kGvOffBars + kGvTailBytes;  // with the start at 0 (less otherwise)
+static constexpr uint32_t kGvBelow = kGvStageBytes + kGvStages * kGvSideBytes + kGvTailBytes;
+static_assert(kGvMaxBase + kGvBelow <= kGvTable, "slot 0, side areas and barriers below the table");
+static_assert(kGvRQ * kGvCW * kGvAcc <= 256, "warp sums fit the table's free half-rows");
+static constexpr uint32_t kGvDynBytes = kGvTableEnd + (kGvStages - 1) * kGvStageBytes;  // with the start at 0
 static_assert(kGvDynBytes <= 227u * 1024u, "shared memory budget");
 
 enum : int { kGvKindWeight = 0, kGvKindAdapter = 1, kGvKindStop = 2 };
@@ -168,6 +171,23 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
     asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
                  : "memory");
 }
+// Global loads that are issued where they are written (volatile): the prefetches below must not be
+// sunk by the compiler to the first use of their results, a stage later.
+__device__ __forceinline__ uint4 ldg_pin_v4(const void *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ uint32_t ldg_pin_u32(const void *p) {
+    uint32_t v;
+    asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ uint32_t ldg_pin_u16(const void *p) {
+    unsigned short v;
+    asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
+    return v;
+}
 __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 // Non-blocking test of a barrier phase.
 __device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
@@ -234,12 +254,13 @@ __global__ void __launch_bounds__(kGvThreads, 1)
     uint32_t dyn_bytes;
     asm volatile("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn_bytes));
     const uint32_t lo_start = (base + 1023u) & ~1023u;
-    if (base > kGvMaxBase || kGvOffBars + kGvTailBytes > base + dyn_bytes) {
+    if (base > kGvMaxBase || kGvDynBytes > base + dyn_bytes) {
         if (threadIdx.x == 0) atomicOr(&g_error_word, kErrLayout);
         return;
     }
     uint8_t *sm0 = gv_smem - base;  // generic pointer of shared-window address 0
-    uint64_t *full = reinterpret_cast<uint64_t *>(sm0 + kGvOffBars);
+    const uint32_t side_base = lo_start + kGvStageBytes;
+    uint64_t *full = reinterpret_cast<uint64_t *>(sm0 + side_base + kGvStages * kGvSideBytes);
     uint64_t *empty = full + kGvStages;
     uint64_t *rfull = empty + kGvStages;  // an item's eight warp sums are in their ring slot
     uint64_t *rempty = rfull + kGvRQ;     // the finisher has read them
@@ -252,6 +273,7 @@ __global__ void __launch_bounds__(kGvThreads, 1)
     auto stage_addr = [&](int slot) -> uint32_t {
         return slot == 0 ? lo_start : kGvTableEnd + (uint32_t)(slot - 1) * kGvStageBytes;
     };
+    auto side_addr = [&](int slot) -> uint32_t { return side_base + (uint32_t)slot * kGvSideBytes; };
 
     // level-pair table: word (v << 6) + l, for every lane l, holds bf16(L[v >> 4]) | bf16(L[v & 15]) << 16
     for (int idx = threadIdx.x; idx < 256 * 32; idx += kGvThreads) {
@@ -283,18 +305,29 @@ __global__ void __launch_bounds__(kGvThreads, 1)
 
     if (warp == kGvProducer) {
         // ---------------------------------------------------------------- producer warp --------
-        // The stages in the order of the work items (taken two ahead from the counter): wait
+        // The stages in the order of the work items (taken two ahead): wait
         // until the stage's slot is free, describe it (with the stage after it, whose x the
         // consumers load ahead), issue its codes (one 3-D TMA box: 32 rows x 8 units, or a 2-D
         // box per unit), store its raw int8 scale codes and, per row (lane = row), the two group
         // constants fl32(c2 / 127) with the block where the second group starts (the consumers
         // rebuild s'_b from these), and release it.  Then load the next stage's scale codes.
-        int item_nn = 0, item_next = 0;
-        if (lane == 0) {
-            item_next = (int)atomicAdd(a.counters + a.RG + 1, 1u);
-            item_nn = (int)atomicAdd(a.counters + a.RG + 1, 1u);
-        }
+        // This CTA's items: first its share of the adapter items (items blockIdx.x, + gridDim.x,
+        // ..., so that U is computed at once by many CTAs), then items of W from the counter.
+        const int nu = a.RU * a.NS;
+        int u_next = blockIdx.x;
+        auto fetch = [&]() -> int {  // the next item (an item of W: valid in lane 0 only)
+            if (u_next < nu) {
+                const int v = u_next;
+                u_next += gridDim.x;
+                return v;
+            }
+            int v = 0;
+            if (lane == 0) v = nu + (int)atomicAdd(a.counters + a.RG + 1, 1u);
+            return v;
+        };
+        int item_next = fetch();
         item_next = __shfl_sync(0xffffffffu, item_next, 0);
+        int item_nn = item_next < a.n_items ? fetch() : a.n_items;
         int item = -1, rg = 0, slab = 0, slab1 = 0;  // the stage to produce: item, row group, slab; the item's end
         // advance to the next stage; false at the end of the work
         auto next_stage = [&]() -> bool {
@@ -306,7 +339,7 @@ __global__ void __launch_bounds__(kGvThreads, 1)
             slab = it.slab0;
             slab1 = it.slab1;
             item_next = __shfl_sync(0xffffffffu, item_nn, 0);
-            if (lane == 0 && item_next < a.n_items) item_nn = (int)atomicAdd(a.counters + a.RG + 1, 1u);
+            if (item_next < a.n_items) item_nn = fetch();
             return true;
         };
         // scale codes and group constants of this lane's row of a weight stage
@@ -352,8 +385,8 @@ __global__ void __launch_bounds__(kGvThreads, 1)
                 ok = false;
                 break;
             }
-            const uint32_t sb = stage_addr(slot);
-            int4 *desc = reinterpret_cast<int4 *>(sm0 + sb + kGvOffDesc);
+            const uint32_t sb = stage_addr(slot), sd = side_addr(slot);
+            int4 *desc = reinterpret_cast<int4 *>(sm0 + sd + kGvSideDesc);
             if (!more) {  // the end: a stop stage
                 if (lane == 0) {
                     desc[0] = make_int4(kGvKindStop, 0, 0, 0);
@@ -375,7 +408,9 @@ __global__ void __launch_bounds__(kGvThreads, 1)
             }
             if (lane == 0) {
                 desc[0] = make_int4(kind, rg, slab, item);
-                desc[1] = make_int4(last_of_item ? 1 : 0, nxt_kind, nxt_slab, 0);
+                // flags: bit 0 the item's first stage, bit 1 the item holds the row group's last slab
+                const int flags = (slab == gv_item(a, item).slab0 ? 1 : 0) | (slab1 == NS ? 2 : 0);
+                desc[1] = make_int4(last_of_item ? 1 : 0, nxt_kind, nxt_slab, flags);
             }
             if (kind == kGvKindWeight) {
                 // a slab of eight whole units: one 3-D box; otherwise one 2-D box per unit (the
@@ -396,10 +431,10 @@ __global__ void __launch_bounds__(kGvThreads, 1)
                 const int jsplit = 256 - (b0 & 255);
                 const int jvalid = n < a.N ? (a.KB - kb0 < 32 ? a.KB - kb0 : 32) : 0;
                 const float k0 = __fdiv_rn(sc_cur.c0, 127.0f), k1 = __fdiv_rn(sc_cur.c1, 127.0f);
-                const uint32_t qrow = sb + kGvOffQ + (uint32_t)lane * 32;
+                const uint32_t qrow = sd + kGvSideQ + (uint32_t)lane * 32;
                 sts128u(qrow, sc_cur.q0.x, sc_cur.q0.y, sc_cur.q0.z, sc_cur.q0.w);
                 sts128u(qrow + 16, sc_cur.q1.x, sc_cur.q1.y, sc_cur.q1.z, sc_cur.q1.w);
-                sts128u(sb + kGvOffK + (uint32_t)lane * 16, __float_as_uint(k0), __float_as_uint(k1), (uint32_t)jsplit,
+                sts128u(sd + kGvSideK + (uint32_t)lane * 16, __float_as_uint(k0), __float_as_uint(k1), (uint32_t)jsplit,
                         (uint32_t)jvalid);
             }
             __syncwarp();
@@ -572,7 +607,7 @@ __global__ void __launch_bounds__(kGvThreads, 1)
             const int k = unit * kGvSub + 64 * jb + 16 * c;
             if (kind != kGvKindStop && g < a.M && k < a.K) {
                 const uint4 *px = reinterpret_cast<const uint4 *>(Xs + (int64_t)g * a.K + k);
-                const uint4 v0 = __ldg(px), v1 = __ldg(px + 1);
+                const uint4 v0 = ldg_pin_v4(px), v1 = ldg_pin_v4(px + 1);
                 xf[jb][0] = v0.x; xf[jb][1] = v0.y; xf[jb][2] = v0.z; xf[jb][3] = v0.w;
                 xf[jb][4] = v1.x; xf[jb][5] = v1.y; xf[jb][6] = v1.z; xf[jb][7] = v1.w;
             } else {
@@ -585,6 +620,10 @@ __global__ void __launch_bounds__(kGvThreads, 1)
     bool x_valid = false;
     bool u_ready = false;
     int h_items = 0;  // work items handed to the finisher
+    uint32_t bfr[2][2][4] = {};  // B fragments of rank chunks w, w + 8 (two 16-row tiles)
+    uint32_t ufr[2][2] = {};     // U fragments of those chunks (token g)
+    // B's rank pairs are 32-bit words when r is even (then every pair starts at an even element)
+    const bool b_pairs = (a.r & 1) == 0;
     for (int t = 0;; ++t) {
         const int slot = t % kGvStages;
         uint32_t okw = 1;
@@ -592,14 +631,14 @@ __global__ void __launch_bounds__(kGvThreads, 1)
         okw = __shfl_sync(0xffffffffu, okw, 0);
         __syncwarp();
         if (!okw) break;
-        const uint32_t sb = stage_addr(slot);
-        const int4 desc = *reinterpret_cast<const int4 *>(sm0 + sb + kGvOffDesc);
+        const uint32_t sb = stage_addr(slot), sd = side_addr(slot);
+        const int4 desc = *reinterpret_cast<const int4 *>(sm0 + sd + kGvSideDesc);
         if (desc.x == kGvKindStop) {
             // pass the end on to the finisher through the sums ring (bounded wait for the slot;
             // the ring's position is the number of items handed off, kept in `h_items`)
             break;
         }
-        const int4 desc1 = *reinterpret_cast<const int4 *>(sm0 + sb + kGvOffDesc + 16);
+        const int4 desc1 = *reinterpret_cast<const int4 *>(sm0 + sd + kGvSideDesc + 16);
         const int kind = desc.x, rg = desc.y, slab = desc.z, item = desc.w;
         const bool last_of_item = desc1.x != 0;
         if (!x_valid) load_x(kind, slab, xf);
@@ -610,6 +649,31 @@ __global__ void __launch_bounds__(kGvThreads, 1)
         // the next stage's x, in flight while this stage is computed
         load_x(desc1.y, desc1.z, xn);
         x_valid = true;
+        // rows of B for the U B^T term, in flight from the first stage of the item that ends the
+        // row group (lane rows as the weight rows: n0 + 16 tt (+ 8); rank pairs 16 jc + 2c (+ 8))
+        if (kind == kGvKindWeight && (desc1.w & 3) == 3) {
+            const int n0 = (rg - a.RU) * kGvRows + gr;
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const int jc = w + q * kGvCW;
+#pragma unroll
+                for (int tt = 0; tt < 2; ++tt)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int n = n0 + 16 * tt + ((i & 1) ? 8 : 0);
+                        const int j = jc * 16 + 2 * c + (i >= 2 ? 8 : 0);
+                        uint32_t v = 0;
+                        if (n < a.N && j < a.r) {
+                            const uint16_t *row = a.B + (int64_t)n * a.r;
+                            if (b_pairs)
+                                v = ldg_pin_u32(row + j);
+                            else
+                                v = ldg_pin_u16(row + j) | (j + 1 < a.r ? ldg_pin_u16(row + j + 1) << 16 : 0u);
+                        }
+                        bfr[q][tt][i] = v;
+                    }
+            }
+        }
         const int unit = slab * kGvSlab + w;
         if (unit < S) {
             if (kind == kGvKindAdapter) {
@@ -659,8 +723,8 @@ __global__ void __launch_bounds__(kGvThreads, 1)
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const uint32_t row = (uint32_t)(gr + 8 * i);
-                    const uint32_t qw = lds32v(sb + kGvOffQ + row * 32u + 4u * w) ^ 0x80808080u;
-                    const int4 kc = lds128i(sb + kGvOffK + row * 16u);
+                    const uint32_t qw = lds32v(sd + kGvSideQ + row * 32u + 4u * w) ^ 0x80808080u;
+                    const int4 kc = lds128i(sd + kGvSideK + row * 16u);
 #pragma unroll
                     for (int jb = 0; jb < 4; ++jb) {
                         const int jj = 4 * w + jb;
@@ -700,7 +764,8 @@ __global__ void __launch_bounds__(kGvThreads, 1)
         if (lane == 0) mbar_arrive(&empty[slot]);
 
         // U B^T, added by the stage of each weight row group's last slab: warp w takes the
-        // 16-wide rank chunks w, w + 8, ... (A operand: bf16 rows of B; B operand: U)
+        // 16-wide rank chunks w and w + 8 (A operand: bf16 rows of B, loaded at the item's first
+        // stage; B operand: U, loaded once it is published)
         if (kind == kGvKindWeight && slab == NS - 1 && w * 16 < a.r32) {
             if (!u_ready) {
                 uint32_t okr = 1;
@@ -719,30 +784,26 @@ __global__ void __launch_bounds__(kGvThreads, 1)
                 __syncwarp();
                 fence_acq_rel_gpu();
                 u_ready = okr != 0;
-            }
-            if (u_ready) {
-                const int n0 = (rg - a.RU) * kGvRows + gr;
-                for (int jc = w; jc * 16 < a.r32; jc += kGvCW) {
-                    const uint32_t *ub = reinterpret_cast<const uint32_t *>(a.Ubf + g * a.r32 + jc * 16 + 2 * c);
-                    const uint32_t b0 = __ldcg(ub), b1 = __ldcg(ub + 4);
+                if (u_ready) {
 #pragma unroll
-                    for (int tt = 0; tt < 2; ++tt) {
-                        uint32_t av[4];
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const int n = n0 + 16 * tt + ((i & 1) ? 8 : 0);
-                            const int j = jc * 16 + 2 * c + (i >= 2 ? 8 : 0);
-                            uint32_t lo = 0, hi = 0;
-                            if (n < a.N) {
-                                const uint16_t *row = a.B + (int64_t)n * a.r;
-                                if (j < a.r) lo = row[j];
-                                if (j + 1 < a.r) hi = row[j + 1];
-                            }
-                            av[i] = lo | (hi << 16);
+                    for (int q = 0; q < 2; ++q) {
+                        const int jc = w + q * kGvCW;
+                        if (jc * 16 < a.r32) {
+                            const uint32_t *ub = reinterpret_cast<const uint32_t *>(a.Ubf + g * a.r32 + jc * 16 + 2 * c);
+                            ufr[q][0] = __ldcg(ub);
+                            ufr[q][1] = __ldcg(ub + 4);
                         }
-                        mma_bf16_16816(acc + 4 * tt, av[0], av[1], av[2], av[3], b0, b1);
                     }
                 }
+            }
+            if (u_ready) {
+#pragma unroll
+                for (int q = 0; q < 2; ++q)
+                    if ((w + q * kGvCW) * 16 < a.r32)
+#pragma unroll
+                        for (int tt = 0; tt < 2; ++tt)
+                            mma_bf16_16816(acc + 4 * tt, bfr[q][tt][0], bfr[q][tt][1], bfr[q][tt][2], bfr[q][tt][3],
+                                           ufr[q][0], ufr[q][1]);
             }
         }
 
