@@ -61,13 +61,14 @@ static constexpr int kGvMaxM = 8;
 static constexpr int kGvAcc = 8;                        // fp32 sums per lane: 2 tiles x (2 rows x 2 tokens)
 static constexpr int kGvRQ = 4;                         // work items' warp sums in flight to the finisher
 // Shared memory.  A stage's codes (32 rows x 8 units, 32 KB) sit in a slot of their own; its
-// small parts sit in a side area per slot: the int8 scale codes [32 rows][32 blocks], per row
-// {k0, k1, jsplit, jvalid}, and the descriptor {kind, rg, slab, item}, {last of item, next kind,
-// next slab, flags}.
+// small parts sit in a side area per slot: the fp32 block scales s'_b [32 rows][kGvScaleLd]
+// (blocks 0..31 of the slab, padded so that the rows start in different banks), and the
+// descriptor {kind, rg, slab, item}, {last of item, next kind, next slab, flags}.
 static constexpr uint32_t kGvBoxBytes = kGvRows * 128;           // one unit's codes
 static constexpr uint32_t kGvStageBytes = kGvSlab * kGvBoxBytes;  // 32 KB
-static constexpr uint32_t kGvSideQ = 0, kGvSideK = kGvRows * 32, kGvSideDesc = kGvSideK + kGvRows * 16;
-static constexpr uint32_t kGvSideBytes = 2048;
+static constexpr int kGvScaleLd = 36;
+static constexpr uint32_t kGvSideS = 0, kGvSideDesc = kGvRows * kGvScaleLd * 4;
+static constexpr uint32_t kGvSideBytes = (kGvSideDesc + 32 + 127) & ~127u;
 static_assert(kGvSideDesc + 32 <= kGvSideBytes, "side area");
 // The level-pair table sits at shared-window address 0x10000, so that one byte permute forms a
 // complete address (0x10000 | code byte << 8 | lane << 2).  It uses the first 128 bytes of each
@@ -157,14 +158,6 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, u
         " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
         : "memory");
-}
-__device__ __forceinline__ int4 lds128i(uint32_t addr) {
-    int4 v;
-    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
-    return v;
-}
-__device__ __forceinline__ void sts128u(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 // Add `bytes` to the barrier's expected transaction count without arriving.
 __device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
@@ -309,8 +302,8 @@ __global__ void __launch_bounds__(kGvThreads, 1)
         // until the stage's slot is free, describe it (with the stage after it, whose x the
         // consumers load ahead), issue its codes (one 3-D TMA box: 32 rows x 8 units, or a 2-D
         // box per unit), store its raw int8 scale codes and, per row (lane = row), the two group
-        // constants fl32(c2 / 127) with the block where the second group starts (the consumers
-        // rebuild s'_b from these), and release it.  Then load the next stage's scale codes.
+        // the rebuilt block scales s'_b (lane = row), and release it.  Then load the next stage's
+        // scale codes into registers.
         // This CTA's items: first its share of the adapter items (items blockIdx.x, + gridDim.x,
         // ..., so that U is computed at once by many CTAs), then items of W from the counter.
         const int nu = a.RU * a.NS;
@@ -431,11 +424,25 @@ __global__ void __launch_bounds__(kGvThreads, 1)
                 const int jsplit = 256 - (b0 & 255);
                 const int jvalid = n < a.N ? (a.KB - kb0 < 32 ? a.KB - kb0 : 32) : 0;
                 const float k0 = __fdiv_rn(sc_cur.c0, 127.0f), k1 = __fdiv_rn(sc_cur.c1, 127.0f);
-                const uint32_t qrow = sd + kGvSideQ + (uint32_t)lane * 32;
-                sts128u(qrow, sc_cur.q0.x, sc_cur.q0.y, sc_cur.q0.z, sc_cur.q0.w);
-                sts128u(qrow + 16, sc_cur.q1.x, sc_cur.q1.y, sc_cur.q1.z, sc_cur.q1.w);
-                sts128u(sd + kGvSideK + (uint32_t)lane * 16, __float_as_uint(k0), __float_as_uint(k1), (uint32_t)jsplit,
-                        (uint32_t)jvalid);
+                const uint32_t qv[8] = {sc_cur.q0.x, sc_cur.q0.y, sc_cur.q0.z, sc_cur.q0.w,
+                                        sc_cur.q1.x, sc_cur.q1.y, sc_cur.q1.z, sc_cur.q1.w};
+                const uint32_t srow = sd + kGvSideS + (uint32_t)lane * (kGvScaleLd * 4);
+#pragma unroll
+                for (int w4 = 0; w4 < 8; ++w4) {
+                    // s'_b = fmaf(q, k, mu), the int8 code as an exact float (the byte q + 128
+                    // spliced into 2^23's mantissa); blocks jb < jsplit use the row's first group,
+                    // the rest the next one; blocks past KB and rows past N get 0
+                    const uint32_t qw = qv[w4] ^ 0x80808080u;
+                    float v[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int jb = 4 * w4 + e;
+                        const float qf = __fsub_rn(__uint_as_float(prmt(qw, 0x4B000000u, 0x7440u + (uint32_t)e)),
+                                                   8388736.0f);  // 2^23 + 128
+                        v[e] = jb < jvalid ? __fmaf_rn(qf, jb < jsplit ? k0 : k1, mu) : 0.0f;
+                    }
+                    sts128f(srow + 16u * w4, v[0], v[1], v[2], v[3]);
+                }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&full[slot]);
@@ -616,39 +623,31 @@ __global__ void __launch_bounds__(kGvThreads, 1)
             }
         }
     };
-    uint32_t xf[4][8], xn[4][8];  // this stage's x, and the next stage's (loaded one stage ahead)
-    bool x_valid = false;
     bool u_ready = false;
     int h_items = 0;  // work items handed to the finisher
     uint32_t bfr[2][2][4] = {};  // B fragments of rank chunks w, w + 8 (two 16-row tiles)
     uint32_t ufr[2][2] = {};     // U fragments of those chunks (token g)
     // B's rank pairs are 32-bit words when r is even (then every pair starts at an even element)
     const bool b_pairs = (a.r & 1) == 0;
-    for (int t = 0;; ++t) {
+    // one stage: xf holds its x (loaded during the previous stage), the next stage's x goes to xn;
+    // false at the end of the work (or when a wait ran out).  Called with the two buffers
+    // swapped on alternate stages, so that no copy is made.
+    auto stage = [&](int t, uint32_t (&xf)[4][8], uint32_t (&xn)[4][8]) -> bool {
         const int slot = t % kGvStages;
         uint32_t okw = 1;
         if (lane == 0) okw = mbar_wait(&full[slot], (uint32_t)((t / kGvStages) & 1), abort_flag) ? 1u : 0u;
         okw = __shfl_sync(0xffffffffu, okw, 0);
         __syncwarp();
-        if (!okw) break;
+        if (!okw) return false;
         const uint32_t sb = stage_addr(slot), sd = side_addr(slot);
         const int4 desc = *reinterpret_cast<const int4 *>(sm0 + sd + kGvSideDesc);
-        if (desc.x == kGvKindStop) {
-            // pass the end on to the finisher through the sums ring (bounded wait for the slot;
-            // the ring's position is the number of items handed off, kept in `h_items`)
-            break;
-        }
+        if (desc.x == kGvKindStop) return false;
         const int4 desc1 = *reinterpret_cast<const int4 *>(sm0 + sd + kGvSideDesc + 16);
         const int kind = desc.x, rg = desc.y, slab = desc.z, item = desc.w;
         const bool last_of_item = desc1.x != 0;
-        if (!x_valid) load_x(kind, slab, xf);
-#pragma unroll
-        for (int jb = 0; jb < 4; ++jb)
-#pragma unroll
-            for (int i = 0; i < 8; ++i) xf[jb][i] = x_valid ? xn[jb][i] : xf[jb][i];
+        if (t == 0) load_x(kind, slab, xf);
         // the next stage's x, in flight while this stage is computed
         load_x(desc1.y, desc1.z, xn);
-        x_valid = true;
         // rows of B for the U B^T term, in flight from the first stage of the item that ends the
         // row group (lane rows as the weight rows: n0 + 16 tt (+ 8); rank pairs 16 jc + 2c (+ 8))
         if (kind == kGvKindWeight && (desc1.w & 3) == 3) {
@@ -716,22 +715,16 @@ __global__ void __launch_bounds__(kGvThreads, 1)
 #pragma unroll
                     for (int i = 0; i < 4; ++i) cw[jb][i] = lds64(r0 + (uint32_t)(8 * i) * 128u);
                 }
-                // s'_b = fmaf(q_b, k, mu) of rows gr + 8 i, blocks 4 w .. 4 w + 3, from the stage's
-                // raw codes and per-row constants (the int8 code as an exact float: the byte
-                // q + 128 spliced into 2^23's mantissa)
+                // s'_b of rows gr + 8 i, blocks 4 w .. 4 w + 3
                 float sc[4][4];
+                const uint32_t srow = sd + kGvSideS + (uint32_t)gr * (kGvScaleLd * 4) + 16u * w;
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    const uint32_t row = (uint32_t)(gr + 8 * i);
-                    const uint32_t qw = lds32v(sd + kGvSideQ + row * 32u + 4u * w) ^ 0x80808080u;
-                    const int4 kc = lds128i(sd + kGvSideK + row * 16u);
-#pragma unroll
-                    for (int jb = 0; jb < 4; ++jb) {
-                        const int jj = 4 * w + jb;
-                        const float qf = __fsub_rn(__uint_as_float(prmt(qw, 0x4B000000u, 0x7440u + (uint32_t)jb)),
-                                                   8388736.0f);  // 2^23 + 128
-                        sc[i][jb] = jj < kc.w ? __fmaf_rn(qf, __int_as_float(jj < kc.z ? kc.x : kc.y), mu) : 0.0f;
-                    }
+                    const float4 f = lds128f(srow + (uint32_t)(8 * i) * (kGvScaleLd * 4));
+                    sc[i][0] = f.x;
+                    sc[i][1] = f.y;
+                    sc[i][2] = f.z;
+                    sc[i][3] = f.w;
                 }
 #pragma unroll
                 for (int jb = 0; jb < 4; ++jb) {
@@ -817,7 +810,7 @@ __global__ void __launch_bounds__(kGvThreads, 1)
                 okr = mbar_wait(&rempty[rs], (uint32_t)(((hi / kGvRQ) - 1) & 1), abort_flag) ? 1u : 0u;
             okr = __shfl_sync(0xffffffffu, okr, 0);
             __syncwarp();
-            if (!okr) break;
+            if (!okr) return false;
 #pragma unroll
             for (int e = 0; e < kGvAcc; ++e) {
                 sts32(red_addr(rs, w, e), __float_as_uint(acc[e]));
@@ -827,6 +820,12 @@ __global__ void __launch_bounds__(kGvThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&rfull[rs]);
         }
+            return true;
+    };
+    uint32_t xa[4][8], xb[4][8];
+    for (int t = 0;; t += 2) {
+        if (!stage(t, xa, xb)) break;
+        if (!stage(t + 1, xb, xa)) break;
     }
     // pass the end on to the finisher (bounded wait for the ring slot)
     {
