@@ -231,20 +231,18 @@ def fused_kernel_source_sha():
     return hashlib.sha256(src[a:b].encode()).hexdigest()
 
 
-def traffic_from_profile(gemm_src_sha):
-    """DRAM bytes per fused-kernel launch from the committed ncu summary, if that summary was
-    taken on the current kernel source; otherwise None."""
-    path = os.path.join(ROOT, "profiles", "fused_gemm_llama8b_attn.md")
+def traffic_from_profile(gemm_src_sha, name="fused_gemm_llama8b_attn"):
+    """DRAM bytes per fused-kernel launch from the machine-readable sidecar of a committed ncu
+    summary (profiles/<name>.json), if that capture was taken on the current kernel source;
+    otherwise None."""
+    path = os.path.join(ROOT, "profiles", name + ".json")
     try:
-        kv = {}
-        for line in open(path):
-            if ":" in line and line.strip().startswith("- "):
-                k, v = line.strip()[2:].split(":", 1)
-                kv[k.strip()] = v.strip().strip("`")
+        with open(path) as f:
+            kv = json.load(f)
         if kv.get("kernel_source_sha256") != gemm_src_sha:
             return None
         return float(kv["dram_bytes_per_launch_avg"])
-    except Exception:
+    except (OSError, ValueError, KeyError, TypeError):
         return None
 
 

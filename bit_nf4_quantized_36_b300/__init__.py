@@ -142,8 +142,12 @@ def nf4_quantize_noalloc(W: torch.Tensor, out: NF4Weight, stream=None) -> NF4Wei
     """nf4_quantize with the library's fixed scratch area instead of a workspace (for callers that
     may not allocate device memory; rows * cols <= 2**28).  `out` must be preallocated."""
     _need(W, torch.float32, "W", (out.rows, out.cols))
+    if out.codes.device != W.device:
+        raise ValueError(f"nf4_quantize_noalloc: out is on {out.codes.device}, W on {W.device}")
     st = out.struct()
-    _check(_lib.load().nf4_quantize_noalloc(_ptr(W), ctypes.byref(st), _stream(stream)), "nf4_quantize_noalloc")
+    # the library finds its scratch area on the current device: make that W's device
+    with torch.cuda.device(W.device):
+        _check(_lib.load().nf4_quantize_noalloc(_ptr(W), ctypes.byref(st), _stream(stream)), "nf4_quantize_noalloc")
     return out
 
 

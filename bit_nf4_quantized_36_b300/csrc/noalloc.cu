@@ -6,8 +6,6 @@
 // allocation, or an embedding runtime whose own allocator must not be bypassed and that has no
 // way to hand out a temporary buffer sized per matrix.  For them this file keeps one fixed
 // scratch area in the library's own device module, sized for matrices of up to 2^28 weights.
-#include <mutex>
-
 namespace qlora {
 
 // Largest matrix served: 2^28 weights (for example 16384 x 16384 or 28672 x 8192).
@@ -23,23 +21,18 @@ static constexpr size_t kNoAllocScratchBytes =
 // looked up with cudaGetSymbolAddress below.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-static std::mutex g_noalloc_mutex;
-static void *g_noalloc_device_ptr[256];  // per device ordinal, filled by the first call on it
-
-// Device address of the scratch area on the current device (looked up once per device).
+// Device address of the scratch area on the current device.  Looked up on every call (a
+// driver-side table read, negligible next to a quantize) so that no address outlives the module
+// it belongs to, e.g. across cudaDeviceReset, which unloads and reloads the module.  A failed
+// lookup is cleared from the thread's last-error state so that it cannot surface in a later call.
 static cudaError_t noalloc_scratch(void **out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 256) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-    if (!g_noalloc_device_ptr[dev]) {
-        void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess) return e;
-        g_noalloc_device_ptr[dev] = p;
+    void *p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return e;
     }
-    *out = g_noalloc_device_ptr[dev];
+    *out = p;
     return cudaSuccess;
 }
 

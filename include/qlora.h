@@ -103,8 +103,10 @@ qlora_status nf4_quantize(const float *W, const qlora_nf4_tensor *out, void *ws,
  * library's device module (16 MiB + 256 KiB, held on every device that loads the library until
  * the process exits), which limits the matrix to rows * cols <= 2^28 weights; larger matrices
  * return QLORA_ERR_UNSUPPORTED_SHAPE without launching anything.  The call allocates nothing.
- * The first call on a device looks up the scratch area's device address for that device; make
- * that first call before starting any stream capture.  All calls on a device share the one area,
+ * W and out must be on the current device: each call looks up the scratch area's address on the
+ * current device (so no address survives a cudaDeviceReset), and the first call on a device may
+ * load the library's device module there; make that first call before starting any stream
+ * capture.  A failed lookup returns QLORA_ERR_CUDA.  All calls on a device share the one area,
  * so calls whose kernels may overlap on the GPU (different streams, or other host threads) race:
  * order them, e.g. on one stream.  No state carries from one call to the next. */
 qlora_status nf4_quantize_noalloc(const float *W, const qlora_nf4_tensor *out, void *stream);

@@ -20,9 +20,11 @@ def test_layer_flops_is_the_sum_of_the_step_products():
 
 
 def test_traffic_lookup_follows_the_recorded_kernel_hash():
-    text = open(os.path.join(ROOT, "profiles", "fused_gemm_llama8b_attn.md")).read()
-    sha = re.search(r"kernel_source_sha256: `([0-9a-f]{64})`", text).group(1)
-    dram = float(re.search(r"dram_bytes_per_launch_avg: `(\d+)`", text).group(1))
+    with open(os.path.join(ROOT, "profiles", "fused_gemm_llama8b_attn.json")) as f:
+        side = json.load(f)
+    sha, dram = side["kernel_source_sha256"], float(side["dram_bytes_per_launch_avg"])
+    # the sidecar belongs to a summary that exists beside it
+    assert os.path.exists(os.path.join(ROOT, "profiles", side["summary"]))
     assert bench.traffic_from_profile(sha) == dram
     assert bench.traffic_from_profile("0" * 64) is None
     # the hash covers a non-empty stretch of the kernel source

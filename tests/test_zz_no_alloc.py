@@ -48,3 +48,31 @@ def test_noalloc_rejects_matrices_beyond_its_scratch(L):
     n0 = L.qlora_launch_count()
     assert L.nf4_quantize_noalloc(ctypes.c_void_p(0x50000), ctypes.byref(big), None) == 2
     assert L.qlora_launch_count() == n0
+
+
+def test_noalloc_call_allocates_nothing_and_launches_two_kernels(L):
+    rows, cols = 512, 2048
+    W = torch.from_numpy(synth.weight(13, rows, cols, 0.02)).cuda()
+    out = q.empty_nf4(rows, cols)
+    q.nf4_quantize_noalloc(W, out)  # warm-up: the first call may load the device module
+    torch.cuda.synchronize()
+    alloc0, free0 = torch.cuda.memory_allocated(), torch.cuda.mem_get_info()[0]
+    n0 = L.qlora_launch_count()
+    q.nf4_quantize_noalloc(W, out)
+    torch.cuda.synchronize()
+    q.check_device_error()
+    # the absmax/code kernel and the scale double-quantization kernel, nothing else
+    assert L.qlora_launch_count() - n0 == 2
+    assert torch.cuda.memory_allocated() == alloc0
+    assert torch.cuda.mem_get_info()[0] == free0
+    ref = q.nf4_quantize(W)
+    for a, b in zip(_host(out), _host(ref)):
+        np.testing.assert_array_equal(a.view(np.uint8), b.view(np.uint8))
+
+
+def test_noalloc_wrapper_refuses_output_on_another_device(L):
+    W = torch.zeros((64, 64), dtype=torch.float32, device="cuda")
+    # one device: an output in host memory stands in for "another device"
+    bad = q.empty_nf4(64, 64, device="cpu" if torch.cuda.device_count() < 2 else "cuda:1")
+    with pytest.raises(ValueError):
+        q.nf4_quantize_noalloc(W, bad)
