@@ -154,27 +154,105 @@ class ClockSampler:
 # ---------------------------------------------------------------------------------------
 # CPU oracle sample (the reference arm and the cpu_baseline key)
 # ---------------------------------------------------------------------------------------
-def oracle_step_sample(inp, What_ref, rows_q: int, tokens: int):
-    """Time the oracle on a bounded sample and scale it to one whole step.
-    quantize + dequantize of `rows_q` weight rows (scaled by N / rows_q), and the layer forward
-    and backward on `tokens` tokens (Y rows, dX rows, dA and dB over those tokens; scaled by
-    M / tokens).  Returns (seconds per whole step, description)."""
+def host_threads():
+    """Host threads this process may run on (the affinity mask where the OS has one)."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def run_threads(jobs, threads):
+    """Run the callables on `threads` host threads and wait for all.  The oracle's routines are
+    C functions called through ctypes, which releases the interpreter lock for the call, so the
+    threads compute in parallel."""
+    if threads <= 1:
+        return [j() for j in jobs]
+    from concurrent.futures import ThreadPoolExecutor
+    with ThreadPoolExecutor(threads) as ex:
+        return list(ex.map(lambda j: j(), jobs))
+
+
+def oracle_step(inp, What_ref, tokens: int, threads: int):
+    """The oracle's time for one whole step on `threads` host threads.
+    quantize + dequantize of the whole weight matrix, its rows split evenly over the threads
+    (each thread quantizes its rows as a matrix of their own: the same work per weight), then
+    the layer forward and backward on `tokens` distinct tokens per thread, scaled to the step's
+    M tokens.  Returns (seconds per whole step, description, seconds spent)."""
     import oracle
     M, N, K = inp.shape
+    T = max(1, threads)
+    chunk = -(-N // T)
+    parts = [(a, min(N, a + chunk)) for a in range(0, N, chunk)]
+
+    def qd(a, b):
+        qz = oracle.nf4_quantize(inp.W[a:b])
+        oracle.nf4_dequantize(qz["packed"], qz["qcode"], qz["c2"], qz["mu"], b - a, K)
+
+    def layer(i):
+        sel = (np.arange(tokens, dtype=np.int64) + i * tokens) % M
+        oracle.layer_fwd_rows(What_ref, inp.X, inp.A, inp.B, inp.alpha, sel)
+        oracle.layer_dx_rows(What_ref, inp.A, inp.B, inp.G, inp.alpha, sel)
+        oracle.layer_adapter_grads(inp.X[sel], inp.A, inp.B, inp.G[sel], inp.alpha)
+
     t0 = time.perf_counter()
-    qz = oracle.nf4_quantize(inp.W[:rows_q])
-    oracle.nf4_dequantize(qz["packed"], qz["qcode"], qz["c2"], qz["mu"], rows_q, K)
+    run_threads([lambda a=a, b=b: qd(a, b) for a, b in parts], T)
     t_q = time.perf_counter() - t0
-    sel = np.arange(tokens, dtype=np.int64)
     t0 = time.perf_counter()
-    oracle.layer_fwd_rows(What_ref, inp.X, inp.A, inp.B, inp.alpha, sel)
-    oracle.layer_dx_rows(What_ref, inp.A, inp.B, inp.G, inp.alpha, sel)
-    oracle.layer_adapter_grads(inp.X[:tokens], inp.A, inp.B, inp.G[:tokens], inp.alpha)
+    run_threads([lambda i=i: layer(i) for i in range(T)], T)
     t_l = time.perf_counter() - t0
-    step_s = t_q * (N / rows_q) + t_l * (M / tokens)
-    desc = (f"oracle (plain C, 1 thread): quantize+dequantize of {rows_q} of {N} weight rows scaled x{N / rows_q:g}, "
-            f"layer fwd+bwd on {tokens} of {M} tokens scaled x{M / tokens:g}")
+    done = tokens * T
+    step_s = t_q + t_l * (M / done)
+    desc = (f"oracle (plain C) on {T} host thread{'s' if T > 1 else ''}: quantize+dequantize of the whole {N}x{K} "
+            f"matrix (not sampled; rows split over the threads), layer fwd+bwd on {done} of {M} tokens "
+            f"({tokens} per thread) scaled x{M / done:g}")
     return step_s, desc, t_q + t_l
+
+
+def oracle_baseline(inp, What_ref, flops, tokens=2):
+    """The cpu_baseline key: the oracle single-threaded and over every host thread."""
+    T = host_threads()
+    s1, d1, sp1 = oracle_step(inp, What_ref, tokens, 1)
+    sT, dT, spT = (s1, d1, 0.0) if T == 1 else oracle_step(inp, What_ref, tokens, T)
+    return {"value": flops / sT / 1e12, "unit": "TFLOP/s", "cores": T, "kind": "oracle",
+            "sample": dT + f" ({spT:.1f} s wall)", "ms_per_step": sT * 1e3,
+            "single_core": {"value": flops / s1 / 1e12, "cores": 1, "ms_per_step": s1 * 1e3,
+                            "sample": d1 + f" ({sp1:.1f} s)"},
+            "parallel_speedup": s1 / sT}
+
+
+def sweep_oracle_check(samples, threads):
+    """For the sweep's sampled layers: the oracle's nf4_quantize + nf4_dequantize of the whole v
+    matrix (codes, scale codes, c2, mu and the bf16 dequant compared bit for bit with the GPU's)
+    and of 64 rows of up (codes compared), the layers spread over the host threads; returns
+    the check and the oracle's own GB/s on that work."""
+    import oracle
+    if not samples:
+        return None
+
+    def one(smp):
+        N, K = smp["v_shape"]
+        t0 = time.perf_counter()
+        ref = oracle.nf4_quantize(smp["v_W"])
+        deq = oracle.nf4_dequantize(ref["packed"], ref["qcode"], ref["c2"], ref["mu"], N, K)
+        rq = oracle.nf4_quantize(smp["up_W_rows"])
+        dt = time.perf_counter() - t0
+        codes, sc, c2, mu = smp["v_gpu"]
+        ok_v = (np.array_equal(codes.view(np.uint8), ref["packed"]) and np.array_equal(sc.view(np.int8), ref["qcode"])
+                and np.array_equal(c2.view(np.uint32), ref["c2"].view(np.uint32))
+                and int(mu.view(np.uint32)[0]) == int(np.float32(ref["mu"]).view(np.uint32))
+                and np.array_equal(smp["v_deq"].view(np.uint16), deq))
+        ok_up = np.array_equal(smp["up_codes_rows"].reshape(-1), rq["packed"])
+        byt = 4 * N * K + 2 * oracle.nf4_storage_bytes(N, K) + 2 * N * K + smp["up_W_rows"].size * 4.5
+        return smp["layer"], ok_v, ok_up, dt, byt
+
+    t0 = time.perf_counter()
+    res = run_threads([lambda s=s: one(s) for s in samples], min(threads, len(samples)))
+    wall = time.perf_counter() - t0
+    return {"layers": [r[0] for r in res], "v_whole_bit_exact": all(r[1] for r in res),
+            "up_rows_codes_bit_exact": all(r[2] for r in res),
+            "what": "v 1024x8192 whole (codes, scale codes, c2, mu, bf16 dequant) and 64 rows of up (codes)",
+            "oracle_GB/s": sum(r[4] for r in res) / wall / 1e9, "oracle_threads": min(threads, len(samples))}
 
 
 def make_inputs():
@@ -194,15 +272,15 @@ def run_reference(args):
     ref = oracle.nf4_quantize(inp.W)
     What_ref = oracle.nf4_dequantize(ref["packed"], ref["qcode"], ref["c2"], ref["mu"], N, K)
     # size the per-step sample so that warm-up + timed steps take about two minutes
-    t1 = oracle_step_sample(inp, What_ref, 64, 1)[2]
+    T = host_threads()
+    t1 = oracle_step(inp, What_ref, 1, T)[2]
     tokens = int(max(1, min(16, 120.0 / (args.steps + args.warmup) / max(t1, 1e-3))))
-    rows_q = 64 * tokens
     for _ in range(args.warmup):
-        oracle_step_sample(inp, What_ref, rows_q, tokens)
+        oracle_step(inp, What_ref, tokens, T)
     steps = []
     desc = ""
     for _ in range(args.steps):
-        s, desc, _ = oracle_step_sample(inp, What_ref, rows_q, tokens)
+        s, desc, _ = oracle_step(inp, What_ref, tokens, T)
         steps.append(s)
     step_s = statistics.mean(steps)
     value = layer_flops(M, N, K, r) / step_s / 1e12
@@ -210,7 +288,7 @@ def run_reference(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K, "r": r, "alpha": c["alpha"]},
-            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": 1, "kind": "oracle", "sample": desc},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": T, "kind": "oracle", "sample": desc},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -504,6 +582,7 @@ def run_ours(args):
     q.check_device_error()
 
     extras = {}
+    sweep_samples = []
     if rank == 0 and not args.no_extras:
         try:
             extras = hbm_extras(q, _lib, L, dev, peaks, flush)
@@ -523,15 +602,26 @@ def run_ours(args):
             extras["paged_adamw"] = optim_extras(q, dev, peaks, flush)
         except Exception as e:
             extras["paged_adamw"] = {"error": repr(e)}
+        try:
+            extras["llama8b_mlp"] = mlp_extras(q, L, dev, peaks, flush)
+        except Exception as e:
+            extras["llama8b_mlp"] = {"error": repr(e)}
+        try:
+            extras["llama70b_sweep"], sweep_samples = sweep_extras(q, dev, peaks, flush)
+        except Exception as e:
+            extras["llama70b_sweep"] = {"error": repr(e)}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
         ref = oracle.nf4_quantize(inp.W)
         What_ref = oracle.nf4_dequantize(ref["packed"], ref["qcode"], ref["c2"], ref["mu"], N, K)
-        step_s, desc, spent = oracle_step_sample(inp, What_ref, 1024, 128)
-        cpu = {"value": flops / step_s / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
-               "sample": desc + f" ({spent:.1f} s of CPU work)", "ms_per_step": step_s * 1e3}
+        cpu = oracle_baseline(inp, What_ref, flops, tokens=32)
+        if sweep_samples:
+            try:
+                extras["llama70b_sweep"]["oracle_check"] = sweep_oracle_check(sweep_samples, host_threads())
+            except Exception as e:
+                extras["llama70b_sweep"]["oracle_check"] = {"error": repr(e)}
 
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": Ksteps,
@@ -552,6 +642,62 @@ def run_ours(args):
     return 0
 
 
+def replay_timed(torch, fn, flush, reps=10, L=None, kernel_events=None):
+    """Device time of fn() with host enqueue kept out of the timing.  fn runs once untimed
+    (allocations, first-call set-up); then `reps` repetitions, each an L2 flush followed by fn()
+    between two events, are captured into one CUDA graph and replayed once: every kernel of
+    every repetition runs, and the events see only device time.  With `kernel_events` (2 events
+    per timed launch) the library's kernel timer is armed during the capture, so that its event
+    pairs around each timed kernel become graph nodes too.  Returns (median call ms, the timed
+    kernels' durations in launch order or None, how).  If the capture fails the repetitions run
+    as stream launches and `how` says so."""
+    fn()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True, external=True), torch.cuda.Event(enable_timing=True, external=True))
+          for _ in range(reps)]
+
+    def arm():
+        if kernel_events is not None:
+            arr = (ctypes.c_void_p * len(kernel_events))(*[e.cuda_event for e in kernel_events])
+            if L.qlora_set_kernel_timer(ctypes.cast(arr, ctypes.c_void_p), len(kernel_events) // 2) != 0:
+                raise RuntimeError("qlora_set_kernel_timer rejected the events")
+
+    def body():
+        for a, b in ev:
+            flush.zero_()
+            a.record()
+            fn()
+            b.record()
+
+    how = "CUDA graph of the repetitions (L2 flush + call each), replayed once"
+    arm()
+    try:
+        cap = torch.cuda.Stream()
+        cap.wait_stream(torch.cuda.current_stream())
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(graph, stream=cap):
+                body()
+        torch.cuda.current_stream().wait_stream(cap)
+        torch.cuda.synchronize()
+        graph.replay()
+    except Exception as e:
+        torch.cuda.synchronize()
+        if kernel_events is not None:
+            L.qlora_set_kernel_timer(None, 0)
+            arm()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        how = f"stream launches (graph capture failed: {type(e).__name__}); host enqueue inside the events"
+        body()
+    torch.cuda.synchronize()
+    tk = None
+    if kernel_events is not None:
+        nk = min(L.qlora_kernel_timer_count(), len(kernel_events) // 2)
+        L.qlora_set_kernel_timer(None, 0)
+        tk = [kernel_events[2 * i].elapsed_time(kernel_events[2 * i + 1]) for i in range(nk)] or None
+    return statistics.median(a.elapsed_time(b) for a, b in ev), tk, how
+
+
 def dropout_extras(q, dev, flush, inp, reps=10):
     """The bench layer (Llama-3-8B attention projection, M = 4096) fwd + bwd with LoRA dropout
     p = 0.05 on the adapter input, against the same call without dropout."""
@@ -569,21 +715,9 @@ def dropout_extras(q, dev, flush, inp, reps=10):
         _, U = q.qlora_linear_fwd_dropout(qw, X, A, B, inp.alpha, 0.05, 1234)
         q.qlora_linear_bwd_dropout(qw, X, A, B, inp.alpha, 0.05, 1234, G, U)
 
-    def timed(fn):
-        fn()
-        ts = []
-        for _ in range(reps):
-            flush.zero_()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            fn()
-            b.record()
-            torch.cuda.synchronize()
-            ts.append(a.elapsed_time(b))
-        return statistics.median(ts)
-
-    t0, t1 = timed(plain), timed(drop)
-    return {"p": 0.05, "plain_fwd_bwd_ms": t0, "dropout_fwd_bwd_ms": t1, "overhead": t1 / t0 - 1.0}
+    t0, _, how = replay_timed(torch, plain, flush, reps)
+    t1, _, _ = replay_timed(torch, drop, flush, reps)
+    return {"p": 0.05, "plain_fwd_bwd_ms": t0, "dropout_fwd_bwd_ms": t1, "overhead": t1 / t0 - 1.0, "timing": how}
 
 
 def optim_extras(q, dev, peaks, flush, reps=10):
@@ -613,11 +747,7 @@ def optim_extras(q, dev, peaks, flush, reps=10):
         torch.cuda.synchronize()
         return a.elapsed_time(b)
 
-    res = []
-    for _ in range(reps):
-        flush.zero_()
-        res.append(ev(lambda: opt.step(p, g, pb)))
-    t_res = statistics.median(res)
+    t_res, _, how = replay_timed(torch, lambda: opt.step(p, g, pb), flush, reps)
     t_out, t_in, t_fault = [], [], []
     for _ in range(3):
         t_out.append(ev(opt.page_out))
@@ -633,7 +763,8 @@ def optim_extras(q, dev, peaks, flush, reps=10):
             "algorithmic_bytes": byt, "moment_bytes": state,
             "page_out_ms": statistics.median(t_out), "page_in_ms": statistics.median(t_in),
             "page_in_GB/s": state / statistics.median(t_in) / 1e6,
-            "step_ms_faulting": statistics.median(t_fault)}
+            "step_ms_faulting": statistics.median(t_fault), "timing": how,
+            "timing_paging": "one event pair around each page-out, page-in and faulting step (stream launches)"}
 
 
 def concat_extras(q, dev, flush, reps=10):
@@ -664,29 +795,153 @@ def concat_extras(q, dev, flush, reps=10):
         _, U = q.qlora_linear_fwd_cat(mods, X)
         q.qlora_linear_bwd_cat(mods, X, dY, U)
 
-    def timed(fn):
-        fn()
-        ts = []
-        for _ in range(reps):
-            flush.zero_()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            fn()
-            b.record()
-            torch.cuda.synchronize()
-            ts.append(a.elapsed_time(b))
-        return statistics.median(ts)
-
-    t_sep, t_cat = timed(separate), timed(concatenated)
+    t_sep, _, how = replay_timed(torch, separate, flush, reps)
+    t_cat, _, _ = replay_timed(torch, concatenated, flush, reps)
     fl = sum(4.0 * M * N * K + 6.0 * M * r * (N + K) for _, N in specs)
     return {"modules": "q 4096x4096, k 1024x4096, v 1024x4096; M=4096, r=16", "separate_ms": t_sep,
             "concatenated_ms": t_cat, "TFLOP/s_separate": fl / t_sep / 1e9, "TFLOP/s_concatenated": fl / t_cat / 1e9,
-            "speedup": t_sep / t_cat}
+            "speedup": t_sep / t_cat, "timing": how}
 
 
-def hbm_extras(q, _lib, L, dev, peaks, flush):
+def mlp_extras(q, L, dev, peaks, flush, reps=5):
+    """Llama-3-8B MLP with adapters on all three linears (gate and up 4096 -> 14336, down
+    14336 -> 4096; NF4 weights N(0, 0.02) with 0.1% +-U(0.2, 1.0) outliers), M = 8192 tokens,
+    r = 64, alpha = 128: forward and backward (dX, dA, dB) of the three layers per step, graph
+    replayed with an L2 flush before each step.  The fused GEMM's launches (a forward and a dX per
+    layer) are timed by the library's kernel timer for the roofline."""
+    import torch
+    from bit_nf4_quantized_36_b300 import synth
+    c = synth.LLAMA8B_MLP
+    M, r, alpha = c["M"], c["r"], c["alpha"]
+    g = torch.Generator(device=dev)
+    g.manual_seed(synth.SEED_BASE + c["id"] * 0x1000 + 0x900)
+    X = torch.randn((M, 4096), generator=g, device=dev).to(torch.bfloat16)     # MLP input (gate, up)
+    H = torch.randn((M, 14336), generator=g, device=dev).to(torch.bfloat16)    # down's input
+    mods = []
+    for mi, (name, N, K) in enumerate(c["mats"]):
+        W = synth.normal_weight_gpu(c["id"], mi, N, K, 0.02, outliers=True)
+        qw = q.nf4_quantize(W)
+        del W
+        A = (torch.randn((r, K), generator=g, device=dev) / K ** 0.5).to(torch.bfloat16)
+        B = (torch.randn((N, r), generator=g, device=dev) * 0.01).to(torch.bfloat16)
+        G = torch.randn((M, N), generator=g, device=dev).to(torch.bfloat16)
+        Xin = X if K == 4096 else H
+        bufs = dict(Y=torch.empty((M, N), dtype=torch.bfloat16, device=dev),
+                    U=torch.empty((M, r), dtype=torch.bfloat16, device=dev),
+                    dX=torch.empty((M, K), dtype=torch.bfloat16, device=dev),
+                    dA=torch.empty((r, K), dtype=torch.float32, device=dev),
+                    dB=torch.empty((N, r), dtype=torch.float32, device=dev),
+                    wf=torch.empty(q.fwd_workspace_bytes(M, N, K, r), dtype=torch.uint8, device=dev),
+                    wb=torch.empty(q.bwd_workspace_bytes(M, N, K, r), dtype=torch.uint8, device=dev))
+        mods.append((name, N, K, qw, Xin, A, B, G, bufs))
+    torch.cuda.synchronize()
+
+    def step():
+        for name, N, K, qw, Xin, A, B, G, b in mods:
+            q.qlora_linear_fwd(qw, Xin, A, B, alpha, Y=b["Y"], U_save=b["U"], workspace=b["wf"])
+            q.qlora_linear_bwd(qw, Xin, A, B, alpha, G, b["U"], dX=b["dX"], dA=b["dA"], dB=b["dB"], workspace=b["wb"])
+
+    kev = new_events(2 * 6 * reps)
+    t, tks, how = replay_timed(torch, step, flush, reps, L=L, kernel_events=kev)
+    q.check_device_error()
+    flops = sum(layer_flops(M, N, K, r) for _, N, K in c["mats"])
+    fused_fl = [fl for _, N, K in c["mats"] for fl in (2.0 * M * N * K + 2.0 * M * N * r, 2.0 * M * N * K + 2.0 * M * K * r)]
+    res = {"workload": c["name"], "step": "qlora_linear_fwd + qlora_linear_bwd of gate, up and down",
+           "ms_per_step": t, "TFLOP/s": flops / t / 1e9, "flops_per_step": flops, "timing": how}
+    if tks and len(tks) >= 6:
+        nrep = len(tks) // 6
+        per = [statistics.median(tks[6 * i + j] for i in range(nrep)) for j in range(6)]
+        ach = sum(fused_fl) / (sum(per) * 1e-3) / 1e12
+        res["roofline"] = {"kernel": "nf4_lora_gemm_kernel (forward and dX launches of the three layers)",
+                           "bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                           "frac": ach / peaks["bf16_tflops"], "traffic": None,
+                           "peak_source": f"{peaks['source']} bf16 dense (burst)",
+                           "launch_ms": dict(zip([f"{n}_{k}" for n, _, _ in c["mats"] for k in ("fwd", "dx")], per)),
+                           "algorithmic_flops_per_launch": fused_fl,
+                           "share_of_step": sum(per) / t}
+    del mods
+    torch.cuda.empty_cache()
+    return res
+
+
+def sweep_extras(q, dev, peaks, flush, layers=80, check_layers=(0, 40, 79)):
+    """The whole-model sweep: 80 Llama-70B-shaped blocks (q, o 8192 x 8192; k, v 1024 x 8192;
+    gate, up 28672 x 8192; down 8192 x 28672), fp32 weights N(0, 0.02) with 0.1% Student-t(3)
+    entries generated per layer on the GPU (untimed), then nf4_quantize and nf4_dequantize to bf16
+    of each matrix.  Each layer's 7 quantize + dequantize pairs are captured in a graph (an L2
+    flush before each pair, an event pair around it) and replayed once.  For the layers in
+    `check_layers` the v matrix (whole) and 64 rows of up are copied to the host with the
+    GPU's results, for the check against the oracle in the CPU-baseline leg."""
+    import torch
+    from bit_nf4_quantized_36_b300 import synth
+    c = synth.LLAMA70B_SWEEP
+    shapes = sorted({(N, K) for _, N, K in c["mats"]})
+    outs = {s: (q.empty_nf4(s[0], s[1], dev), torch.empty(s, dtype=torch.bfloat16, device=dev)) for s in shapes}
+    ws = torch.empty(max(q.quantize_workspace_bytes(N, K) for N, K in shapes), dtype=torch.uint8, device=dev)
+    per_layer_ms, byt_layer, samples = [], 0, []
+    how = "per layer: a CUDA graph of the 7 (L2 flush, quantize + dequantize) pairs, replayed once"
+    for layer in range(layers):
+        Ws = [synth.sweep_weight_gpu(layer, mi, N, K, device=dev, std=c["w_std"]) for mi, (_, N, K) in enumerate(c["mats"])]
+        ev = [(torch.cuda.Event(enable_timing=True, external=True), torch.cuda.Event(enable_timing=True, external=True))
+              for _ in Ws]
+
+        def body():
+            for (a, b), W, (_, N, K) in zip(ev, Ws, c["mats"]):
+                qw, What = outs[(N, K)]
+                flush.zero_()
+                a.record()
+                q.nf4_quantize(W, out=qw, workspace=ws)
+                q.nf4_dequantize(qw, out=What)
+                b.record()
+
+        torch.cuda.synchronize()
+        try:
+            cap = torch.cuda.Stream()
+            cap.wait_stream(torch.cuda.current_stream())
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(cap):
+                with torch.cuda.graph(graph, stream=cap):
+                    body()
+            torch.cuda.current_stream().wait_stream(cap)
+            graph.replay()
+        except Exception as e:
+            torch.cuda.synchronize()
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in Ws]
+            how = f"stream launches (graph capture failed: {type(e).__name__})"
+            body()
+        torch.cuda.synchronize()
+        per_layer_ms.append(sum(a.elapsed_time(b) for a, b in ev))
+        if layer == 0:
+            byt_layer = sum(4 * N * K + 2 * q.nf4_storage_bytes(N, K) + 2 * N * K for _, N, K in c["mats"])
+        # the v and up matrices' results are still in their shapes' output buffers (each is the
+        # last matrix of its shape in the layer's order)
+        if layer in check_layers:
+            vq, vW = outs[(c["mats"][2][1], c["mats"][2][2])]
+            uq, _ = outs[(c["mats"][5][1], c["mats"][5][2])]
+            uN, uK = c["mats"][5][1], c["mats"][5][2]
+            rows = torch.arange(0, uN, uN // 64, device=dev)[:64]
+            samples.append({"layer": layer, "v_W": Ws[2].cpu().numpy(), "v_shape": (c["mats"][2][1], c["mats"][2][2]),
+                            "v_gpu": [t.cpu().numpy() for t in (vq.codes, vq.scale_codes, vq.scale_scales, vq.scale_offset)],
+                            "v_deq": vW.view(torch.int16).cpu().numpy(),
+                            "up_rows": rows.cpu().numpy(), "up_W_rows": Ws[5][rows].cpu().numpy(),
+                            "up_codes_rows": uq.codes.view(uN, uK // 2)[rows].cpu().numpy()})
+        del Ws
+    total_ms = sum(per_layer_ms)
+    res = {"workload": c["name"], "layers": layers, "matrices_per_layer": len(c["mats"]),
+           "weights_per_layer": sum(N * K for _, N, K in c["mats"]), "ms_total": total_ms,
+           "ms_per_layer_median": statistics.median(per_layer_ms), "algorithmic_bytes_per_layer": byt_layer,
+           "GB/s": layers * byt_layer / total_ms / 1e6, "frac_hbm": layers * byt_layer / total_ms / 1e6 / peaks["hbm_gbs"],
+           "bytes": "quantize reads fp32 and writes the NF4 storage; dequantize reads the storage and writes bf16",
+           "timing": how, "codes_checked": "in the CPU-baseline leg, layers " + ", ".join(map(str, check_layers))}
+    del outs
+    torch.cuda.empty_cache()
+    return res, samples
+
+
+def hbm_extras(q, _lib, L, dev, peaks, flush, reps=10):
     """Secondary numbers for the HBM-bound kernels on a Llama-70B MLP matrix (28672 x 8192):
-    nf4_dequantize, nf4_quantize and adapter-merge GB/s, and the small-M forward (decode) GB/s."""
+    nf4_dequantize, nf4_quantize and adapter-merge GB/s, and the small-M forward (decode) GB/s on
+    both 70B MLP matrices.  Every figure is device time of a graph-replayed call (replay_timed)."""
     import torch
     from bit_nf4_quantized_36_b300 import synth
     rows, cols = 28672, 8192
@@ -698,62 +953,52 @@ def hbm_extras(q, _lib, L, dev, peaks, flush):
     ws = torch.empty(q.quantize_workspace_bytes(rows, cols), dtype=torch.uint8, device=dev)
     torch.cuda.synchronize()
 
-    def timed(fn, reps=10):
-        ts = []
-        for _ in range(reps):
-            flush.zero_()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            fn()
-            b.record()
-            torch.cuda.synchronize()
-            ts.append(a.elapsed_time(b))
-        return statistics.median(ts)
+    def gbs(name, t, byt, how, **kw):
+        return {"matrix": f"{rows}x{cols}", "ms": t, "GB/s": byt / t / 1e6,
+                "frac_hbm": byt / t / 1e6 / peaks["hbm_gbs"], "algorithmic_bytes": byt, "timing": how, **kw}
 
     out = {}
-    t = timed(lambda: q.nf4_dequantize(qw, out=What))
-    byt = storage + 2 * n
-    out["dequantize"] = {"matrix": f"{rows}x{cols}", "ms": t, "GB/s": byt / t / 1e6,
-                         "frac_hbm": byt / t / 1e6 / peaks["hbm_gbs"], "algorithmic_bytes": byt}
-    t = timed(lambda: q.nf4_quantize(W, out=qw, workspace=ws))
-    byt = 4 * n + storage
-    out["quantize"] = {"matrix": f"{rows}x{cols}", "ms": t, "GB/s": byt / t / 1e6,
-                       "frac_hbm": byt / t / 1e6 / peaks["hbm_gbs"], "algorithmic_bytes": byt}
+    t, _, how = replay_timed(torch, lambda: q.nf4_dequantize(qw, out=What), flush, reps)
+    out["dequantize"] = gbs("dequantize", t, storage + 2 * n, how)
+    t, _, how = replay_timed(torch, lambda: q.nf4_quantize(W, out=qw, workspace=ws), flush, reps)
+    out["quantize"] = gbs("quantize", t, 4 * n + storage, how)
     # adapter merge W_m = bf16(W^ + (alpha/r) B A): codes and scales read, bf16 written
     for r_m in (16, 64):
         Am = (torch.randn((r_m, cols), device=dev) / cols ** 0.5).to(torch.bfloat16)
         Bm = (torch.randn((rows, r_m), device=dev) * 0.01).to(torch.bfloat16)
-        t = timed(lambda: q.qlora_merge(qw, Am, Bm, 2.0 * r_m, out=What))
-        byt = storage + 2 * n + 2 * r_m * (rows + cols)
-        out[f"merge_r{r_m}"] = {"matrix": f"{rows}x{cols}", "ms": t, "GB/s": byt / t / 1e6,
-                                "frac_hbm": byt / t / 1e6 / peaks["hbm_gbs"], "algorithmic_bytes": byt}
-    del W, What
-    # decode-like forward: M tokens through the up projection (N = 28672, K = 8192), r = 16
-    r = 16
-    A = (torch.randn((r, cols), device=dev) / cols ** 0.5).to(torch.bfloat16)
-    B = (torch.randn((rows, r), device=dev) * 0.01).to(torch.bfloat16)
-    dec = {}
-    for M in (1, 8, 32):
-        X = torch.randn((M, cols), device=dev).to(torch.bfloat16)
-        Y = torch.empty((M, rows), dtype=torch.bfloat16, device=dev)
-        U = torch.empty((M, r), dtype=torch.bfloat16, device=dev)
-        wsf = torch.empty(q.fwd_workspace_bytes(M, rows, cols, r), dtype=torch.uint8, device=dev)
-        t = timed(lambda: q.qlora_linear_fwd(qw, X, A, B, 32.0, Y=Y, U_save=U, workspace=wsf))
-        kev = new_events(20)
-        arr = (ctypes.c_void_p * 20)(*[e.cuda_event for e in kev])
-        if L.qlora_set_kernel_timer(ctypes.cast(arr, ctypes.c_void_p), 10) != 0:
-            raise RuntimeError("qlora_set_kernel_timer rejected the events")
-        for _ in range(10):
-            flush.zero_()
-            q.qlora_linear_fwd(qw, X, A, B, 32.0, Y=Y, U_save=U, workspace=wsf)
-        torch.cuda.synchronize()
-        L.qlora_set_kernel_timer(None, 0)
-        tk = statistics.median(kev[2 * i].elapsed_time(kev[2 * i + 1]) for i in range(10))
-        byt = storage + 2 * r * (rows + cols) + 2 * M * (rows + cols)
-        dec[f"M={M}"] = {"call_ms": t, "kernel": "nf4_gemv_kernel" if M <= 8 else "nf4_lora_gemm_small_kernel",
-                         "kernel_ms": tk, "GB/s_kernel": byt / tk / 1e6,
-                         "frac_hbm_kernel": byt / tk / 1e6 / peaks["hbm_gbs"], "GB/s_call": byt / t / 1e6}
-    out["decode_forward_28672x8192_r16"] = dec
+        t, _, how = replay_timed(torch, lambda: q.qlora_merge(qw, Am, Bm, 2.0 * r_m, out=What), flush, reps)
+        out[f"merge_r{r_m}"] = gbs("merge", t, storage + 2 * n + 2 * r_m * (rows + cols), how)
+    del W, What, qw, ws
+    torch.cuda.empty_cache()
+    # decode-like forward: M tokens through each 70B MLP matrix, r = 16, W ~ N(0, 0.015)
+    c = synth.LLAMA70B_DECODE
+    r, alpha = c["r"], c["alpha"]
+    for mi, (name, N, K) in enumerate(c["mats"]):
+        Wd = synth.normal_weight_gpu(c["id"], mi, N, K, c["w_std"])
+        qd = q.nf4_quantize(Wd)
+        del Wd
+        A = (torch.randn((r, K), device=dev) / K ** 0.5).to(torch.bfloat16)
+        B = (torch.randn((N, r), device=dev) * 0.01).to(torch.bfloat16)
+        st = q.nf4_storage_bytes(N, K)
+        dec = {}
+        for M in c["Ms"]:
+            X = torch.randn((M, K), device=dev).to(torch.bfloat16)
+            Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            U = torch.empty((M, r), dtype=torch.bfloat16, device=dev)
+            wsf = torch.empty(q.fwd_workspace_bytes(M, N, K, r), dtype=torch.uint8, device=dev)
+            kev = new_events(2 * reps)
+            t, tks, how = replay_timed(torch, lambda: q.qlora_linear_fwd(qd, X, A, B, alpha, Y=Y, U_save=U,
+                                                                         workspace=wsf),
+                                       flush, reps, L=L, kernel_events=kev)
+            tk = statistics.median(tks) if tks else None
+            byt = st + 2 * r * (N + K) + 2 * M * (N + K)
+            dec[f"M={M}"] = {"call_ms": t, "kernel": "nf4_gemv_kernel" if M <= 8 else "nf4_lora_gemm_small_kernel",
+                             "kernel_ms": tk, "GB/s_kernel": byt / tk / 1e6 if tk else None,
+                             "frac_hbm_kernel": byt / tk / 1e6 / peaks["hbm_gbs"] if tk else None,
+                             "GB/s_call": byt / t / 1e6, "frac_hbm_call": byt / t / 1e6 / peaks["hbm_gbs"],
+                             "algorithmic_bytes": byt, "timing": how}
+        out[f"decode_forward_{name}_{N}x{K}_r{r}"] = dec
+        del qd
     out["hbm_peak_GB/s"] = f"{peaks['hbm_gbs']} ({peaks['source']})"
     return out
 

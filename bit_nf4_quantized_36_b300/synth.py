@@ -134,6 +134,23 @@ def sweep_weight_gpu(layer: int, mat_index: int, rows: int, cols: int, device="c
     return w
 
 
+def normal_weight_gpu(workload_id: int, mat_index: int, rows: int, cols: int, std: float, device="cuda",
+                      outliers: bool = False):
+    """fp32 [rows, cols] ~ N(0, std) on the GPU (torch's seeded device generator, one stream per
+    (workload, matrix)); with `outliers`, 0.1% of the entries replaced by +-U(0.2, 1.0) with a
+    random sign (the MLP workload's outlier recipe)."""
+    import torch
+    gen = torch.Generator(device=device)
+    gen.manual_seed(SEED_BASE + workload_id * 0x1000 + 0x800 + mat_index)
+    w = torch.randn((rows, cols), generator=gen, device=device, dtype=torch.float32).mul_(std)
+    if outliers:
+        mask = torch.rand((rows, cols), generator=gen, device=device) < 0.001
+        mag = torch.rand((rows, cols), generator=gen, device=device).mul_(0.8).add_(0.2)
+        sign = torch.where(torch.rand((rows, cols), generator=gen, device=device) < 0.5, -1.0, 1.0)
+        w = torch.where(mask, mag * sign, w)
+    return w
+
+
 # ---------------------------------------------------------------------------------------
 # Optimizer-step inputs (flat fp32 arrays of adapter weights, gradients and AdamW moments).
 # ---------------------------------------------------------------------------------------

@@ -56,7 +56,28 @@ def test_reference_arm_prints_the_contract_line():
     assert (d["steps"], d["warmup"], d["n_gpus"]) == (1, 3, 1)
     assert d["config"]["workload"] == bench.WORKLOAD and d["vs_baseline"] is None and d["data"] == "synthetic"
     cb = d["cpu_baseline"]
-    assert cb["kind"] == "oracle" and cb["cores"] == 1 and cb["value"] == d["value"] and cb["sample"]
+    assert cb["kind"] == "oracle" and cb["cores"] == bench.host_threads() and cb["value"] == d["value"] and cb["sample"]
     e = d["e2e"]
     assert e["value"] == d["value"] and e["unit"] == "TFLOP/s"
     assert e["h2d_bytes_per_step"] == 0 and e["d2h_bytes_per_step"] == 0
+
+
+def test_cpu_baseline_reports_one_thread_and_every_thread():
+    """The oracle timed on one host thread and on all of them, the core count stated, on the
+    small layer (whole-matrix quantize + dequantize, a few tokens of the layer)."""
+    import oracle
+    from bit_nf4_quantized_36_b300 import synth
+    inp = synth.tiny_inputs()
+    M, N, K = inp.shape
+    ref = oracle.nf4_quantize(inp.W)
+    What = oracle.nf4_dequantize(ref["packed"], ref["qcode"], ref["c2"], ref["mu"], N, K)
+    cb = bench.oracle_baseline(inp, What, bench.layer_flops(M, N, K, inp.A.shape[0]), tokens=2)
+    assert cb["kind"] == "oracle" and cb["cores"] == bench.host_threads() >= 1
+    assert cb["value"] > 0 and cb["single_core"]["value"] > 0 and cb["single_core"]["cores"] == 1
+    assert "whole" in cb["sample"] and "not sampled" in cb["sample"]
+
+
+def test_run_threads_runs_every_job_once():
+    seen = []
+    out = bench.run_threads([lambda i=i: seen.append(i) or i * i for i in range(7)], 3)
+    assert out == [i * i for i in range(7)] and sorted(seen) == list(range(7))
