@@ -100,6 +100,10 @@ static const NF4Tables &tables() {
         }
         t.thr[15] = INFINITY;
         for (int j = 0; j < kNF4Buckets; ++j) {
+            if (j > 33) {
+                t.bucket[j] = 0x7FC00000u;
+                continue;
+            }
             const double start = -1.0 + (j - 1) / 16.0 - std::ldexp(1.0, -12);
             int c = 0;
             while (c < 15 && (double)t.thr[c] <= start) ++c;

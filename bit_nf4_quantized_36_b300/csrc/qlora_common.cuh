@@ -25,7 +25,9 @@ static constexpr int kGroup = 256;    // blocks per double-quantization group
 
 // Kernel-argument copy of the tables: levels, and the 15 exact decision thresholds of the
 // nearest-level rule (code = number of thresholds <= x; computed on the host).
-static constexpr int kNF4Buckets = 34;  // entries j = 0..33 for the 1/16-wide buckets j - 1 of [-1, 1]
+// entries j = 0..33 for the 1/16-wide buckets j - 1 of [-1, 1]; entries 34..63 (reached only by
+// a NaN) hold a NaN.  A power of two: the index is masked into the table.
+static constexpr int kNF4Buckets = 64;
 
 struct NF4Tables {
     float level[16];

@@ -36,15 +36,17 @@ __device__ __forceinline__ uint32_t nf4_code(float w, float s, const float *thr)
 }
 
 // Without a division: x0 = fl(w * fl(1/s)) is within 2^-22 of x when s is normal (|w / s| <= 1:
-// two roundings of 2^-24 relative each, plus 2^-24 for x's own rounding).  j = floor(fl(16 x0 +
-// 17)) puts x0 in [b - 2^-23, b + 1/16 + 2^-23) for b = -1 + (j - 1) / 16, so every threshold at or
-// below b - 2^-12 is below x and the one after t = thr[c] is above x: the code is c + [t <= x].
-// With the table's t' (t moved by under 2^-20), the comparison on x0 gives [t <= x] whenever x0
-// is more than 2^-19 from t'; otherwise `unsure` asks for the exact rule.  NaN weights land on
-// j = 0 and are unsure.
+// two roundings of 2^-24 relative each, plus 2^-24 for x's own rounding).  The bucket index
+// j = floor(16 x0 + 17) comes from one fma rounded toward -inf into [2^23, 2^24), where the ulp
+// is 1, so the low bits of its bit pattern are j exactly; x0 lies in [b, b + 1/16) for
+// b = -1 + (j - 1) / 16, every threshold at or below b - 2^-12 is below x, and the one after
+// t = thr[c] is above x: the code is c + [t <= x].  With the table's t' (t moved by under 2^-20),
+// the comparison on x0 gives [t <= x] whenever x0 is more than 2^-19 from t'; otherwise `unsure`
+// asks for the exact rule.  A NaN weight makes d a NaN (unsure); the mask keeps its index in the
+// table.
 __device__ __forceinline__ uint32_t nf4_code_fast(float w, float rcp, const uint32_t *tab, bool &unsure) {
     const float x0 = __fmul_rn(w, rcp);
-    const uint32_t e = tab[__float2int_rd(__fmaf_rn(x0, 16.0f, 17.0f))];  // in [0, 33] for |x0| <= 1 + 2^-22
+    const uint32_t e = tab[__float_as_uint(__fmaf_rd(x0, 16.0f, 8388625.0f)) & (kNF4Buckets - 1)];
     const float d = __fsub_rn(x0, __uint_as_float(e));
     unsure |= !(fabsf(d) > 0x1p-19f);
     return (e & 15u) + (d >= 0.0f ? 1u : 0u);
@@ -124,81 +126,93 @@ __global__ void __launch_bounds__(kQuantThreads, 8) nf4_quantize_groups_kernel(
     // this CTA's groups [g0, g0 + run) hold blocks [B0, B1): a contiguous range of W
     const int64_t g0 = (int64_t)blockIdx.x * run;
     const int64_t B0 = min64(nb, g0 * kGroup), B1 = min64(nb, (g0 + run) * kGroup);
-    const int64_t ngrp = (B1 - B0 + kGroup - 1) / kGroup;  // groups of W in the run
-    const int64_t npass = ngrp * kQPasses;
+    const int nblk = (int)(B1 - B0);                       // < 2^31: run * 256 blocks at most
+    const int ngrp = (nblk + kGroup - 1) / kGroup;         // groups of W in the run
     const uint32_t lane = threadIdx.x & 31u, l8 = threadIdx.x & 7u;
     const uint32_t gmask = 0xFFu << (lane & 24u);
     const int sub = (int)(threadIdx.x >> 3);  // block within a pass
-    auto stage = [&](int64_t p) {             // this thread's two float4 of pass p, or zeros past W
-        const int64_t b = B0 + p * kQPassBlocks + sub;
-        float4 *d = &s_in[p % kQAhead][0][threadIdx.x];
-        if (b < B1) {
-            cp_async_16(smem_u32(d), W + b * 16 + l8);
-            cp_async_16(smem_u32(d + kQuantThreads), W + b * 16 + 8 + l8);
+    // this thread's two float4 of pass p are src[p * kQPassStride] and src[p * kQPassStride + 8]
+    const float4 *src = W + (B0 + sub) * 16 + l8;
+    uint16_t *dst = codes16 + (B0 + sub) * 16 + l8;
+    constexpr int kQPassStride = kQPassBlocks * 16;  // float4 (and code words) per pass
+    // staging slots, rotated by running shared-memory addresses (no index arithmetic per pass)
+    const uint32_t slot0 = smem_u32(&s_in[0][0][threadIdx.x]);
+    constexpr uint32_t kSlotBytes = 2u * kQuantThreads * 16u, kHalf = kQuantThreads * 16u;
+    uint32_t wslot = slot0, rslot = slot0;
+    auto next = [&](uint32_t a) { return a + kSlotBytes == slot0 + kQAhead * kSlotBytes ? slot0 : a + kSlotBytes; };
+    auto stage = [&](int p) {  // this thread's two float4 of pass p, or zeros past the run's blocks
+        if (p * kQPassBlocks + sub < nblk) {
+            cp_async_16(wslot, src + (int64_t)p * kQPassStride);
+            cp_async_16(wslot + kHalf, src + (int64_t)p * kQPassStride + 8);
         } else {
-            d[0] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-            d[kQuantThreads] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            asm volatile("st.shared.v4.f32 [%0], {%1, %1, %1, %1};" ::"r"(wslot), "f"(0.0f) : "memory");
+            asm volatile("st.shared.v4.f32 [%0], {%1, %1, %1, %1};" ::"r"(wslot + kHalf), "f"(0.0f) : "memory");
         }
         cp_async_commit();  // one group per pass, empty or not, keeps the wait count fixed
+        wslot = next(wslot);
     };
 #pragma unroll
     for (int p = 0; p < kQAhead - 1; ++p) stage(p);
 
     double stack[48];  // thread 0: pairwise-tree stack over the run's groups
-    for (int64_t p = 0; p < npass; ++p) {
-        stage(p + kQAhead - 1);
-        cp_async_wait<kQAhead - 1>();  // pass p has landed (only this thread reads its slots)
-        const float4 v = s_in[p % kQAhead][0][threadIdx.x];
-        const float4 u = s_in[p % kQAhead][1][threadIdx.x];
-        const int blk = (int)(p % kQPasses) * kQPassBlocks + sub;  // block within the group
-        // |w| >= 0 orders like its bit pattern; fmaxf drops NaN (finite input is required)
-        float m = fmaxf(fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))),
-                        fmaxf(fmaxf(fabsf(u.x), fabsf(u.y)), fmaxf(fabsf(u.z), fabsf(u.w))));
-        m = __uint_as_float(__reduce_max_sync(gmask, __float_as_uint(fmaxf(m, 0.0f))));
-        uint32_t c[8] = {kZeroCode, kZeroCode, kZeroCode, kZeroCode, kZeroCode, kZeroCode, kZeroCode, kZeroCode};
-        bool unsure = !(m >= 0x1p-100f && m < INFINITY);  // else 1/m is normal and finite
-        if (!unsure) {
-            const float rcp = __frcp_rn(m);
-            c[0] = nf4_code_fast(v.x, rcp, s_tab, unsure);
-            c[1] = nf4_code_fast(v.y, rcp, s_tab, unsure);
-            c[2] = nf4_code_fast(v.z, rcp, s_tab, unsure);
-            c[3] = nf4_code_fast(v.w, rcp, s_tab, unsure);
-            c[4] = nf4_code_fast(u.x, rcp, s_tab, unsure);
-            c[5] = nf4_code_fast(u.y, rcp, s_tab, unsure);
-            c[6] = nf4_code_fast(u.z, rcp, s_tab, unsure);
-            c[7] = nf4_code_fast(u.w, rcp, s_tab, unsure);
-        }
-        if (unsure) {
-            c[0] = nf4_code(v.x, m, s_thr);
-            c[1] = nf4_code(v.y, m, s_thr);
-            c[2] = nf4_code(v.z, m, s_thr);
-            c[3] = nf4_code(v.w, m, s_thr);
-            c[4] = nf4_code(u.x, m, s_thr);
-            c[5] = nf4_code(u.y, m, s_thr);
-            c[6] = nf4_code(u.z, m, s_thr);
-            c[7] = nf4_code(u.w, m, s_thr);
-        }
-        const int64_t b = B0 + p * kQPassBlocks + sub;
-        if (b < B1) {
-            codes16[b * 16 + l8] = (uint16_t)pack4(c[0], c[1], c[2], c[3]);
-            codes16[b * 16 + 8 + l8] = (uint16_t)pack4(c[4], c[5], c[6], c[7]);
-        }
-        const int64_t gi = p / kQPasses;  // group within the run
+    for (int gi = 0; gi < ngrp; ++gi) {
         float *sa = s_abs[gi & 1];
-        if (l8 == 0) sa[blk] = m;  // 0 past the last block
-        if (p % kQPasses == kQPasses - 1) {  // the pass closes a group (uniform over the CTA)
-            // one barrier: the buffer is written again two groups later, after the next group's
-            // barrier, which every reader of this one has passed
-            __syncthreads();
-            const int64_t gb0 = b - blk;
-            if (gb0 + (int64_t)threadIdx.x < B1) absmax[gb0 + threadIdx.x] = sa[threadIdx.x];
-            if (threadIdx.x < 32) {
-                double sum = group_sum(sa, lane);
-                if (lane == 0) {  // leaf gi of the run, paired as the tree's levels pair them
-                    int lvl = 0;
-                    for (int64_t j = gi; j & 1; j >>= 1) sum = __dadd_rn(stack[lvl++], sum);
-                    stack[lvl] = sum;
-                }
+#pragma unroll
+        for (int ps = 0; ps < kQPasses; ++ps) {
+            const int p = gi * kQPasses + ps;
+            stage(p + kQAhead - 1);
+            cp_async_wait<kQAhead - 1>();  // pass p has landed (only this thread reads its slots)
+            float4 v, u;
+            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                         : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(rslot) : "memory");
+            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                         : "=f"(u.x), "=f"(u.y), "=f"(u.z), "=f"(u.w) : "r"(rslot + kHalf) : "memory");
+            rslot = next(rslot);
+            // |w| >= 0 orders like its bit pattern; fmaxf drops NaN (finite input is required)
+            float m = fmaxf(fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))),
+                            fmaxf(fmaxf(fabsf(u.x), fabsf(u.y)), fmaxf(fabsf(u.z), fabsf(u.w))));
+            m = __uint_as_float(__reduce_max_sync(gmask, __float_as_uint(fmaxf(m, 0.0f))));
+            uint32_t c[8] = {kZeroCode, kZeroCode, kZeroCode, kZeroCode, kZeroCode, kZeroCode, kZeroCode, kZeroCode};
+            // the shortcut's error bound needs fl(1/m) normal: 2^-100 <= m < 2^126
+            bool unsure = !(m >= 0x1p-100f && m < 0x1p126f);
+            if (!unsure) {
+                const float rcp = __frcp_rn(m);
+                c[0] = nf4_code_fast(v.x, rcp, s_tab, unsure);
+                c[1] = nf4_code_fast(v.y, rcp, s_tab, unsure);
+                c[2] = nf4_code_fast(v.z, rcp, s_tab, unsure);
+                c[3] = nf4_code_fast(v.w, rcp, s_tab, unsure);
+                c[4] = nf4_code_fast(u.x, rcp, s_tab, unsure);
+                c[5] = nf4_code_fast(u.y, rcp, s_tab, unsure);
+                c[6] = nf4_code_fast(u.z, rcp, s_tab, unsure);
+                c[7] = nf4_code_fast(u.w, rcp, s_tab, unsure);
+            }
+            if (unsure) {
+                c[0] = nf4_code(v.x, m, s_thr);
+                c[1] = nf4_code(v.y, m, s_thr);
+                c[2] = nf4_code(v.z, m, s_thr);
+                c[3] = nf4_code(v.w, m, s_thr);
+                c[4] = nf4_code(u.x, m, s_thr);
+                c[5] = nf4_code(u.y, m, s_thr);
+                c[6] = nf4_code(u.z, m, s_thr);
+                c[7] = nf4_code(u.w, m, s_thr);
+            }
+            if (p * kQPassBlocks + sub < nblk) {
+                dst[(int64_t)p * kQPassStride] = (uint16_t)pack4(c[0], c[1], c[2], c[3]);
+                dst[(int64_t)p * kQPassStride + 8] = (uint16_t)pack4(c[4], c[5], c[6], c[7]);
+            }
+            if (l8 == 0) sa[ps * kQPassBlocks + sub] = m;  // 0 past the last block
+        }
+        // the group is closed.  One barrier: the buffer is written again two groups later, after
+        // the next group's barrier, which every reader of this one has passed
+        __syncthreads();
+        const int64_t gb0 = B0 + (int64_t)gi * kGroup;
+        if (gb0 + (int64_t)threadIdx.x < B1) absmax[gb0 + threadIdx.x] = sa[threadIdx.x];
+        if (threadIdx.x < 32) {
+            double sum = group_sum(sa, lane);
+            if (lane == 0) {  // leaf gi of the run, paired as the tree's levels pair them
+                int lvl = 0;
+                for (int j = gi; j & 1; j >>= 1) sum = __dadd_rn(stack[lvl++], sum);
+                stack[lvl] = sum;
             }
         }
     }
