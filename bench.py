@@ -1009,19 +1009,24 @@ def run_ncu_target(args):
     (--ncu-target decode: the up projection 28672 x 8192; decode_down: the down projection
     8192 x 28672), three AdamW steps over the Llama-3-8B adapter set with the moments
     in plain device memory (--ncu-target adamw; the same kernel as with paged moments), or three
-    quantizations or dequantizations of a 28672 x 8192 matrix (--ncu-target quantize, dequantize)."""
+    quantizations, dequantizations or rank-16 adapter merges of a 28672 x 8192 matrix
+    (--ncu-target quantize, dequantize, merge)."""
     import torch
 
     import bit_nf4_quantized_36_b300 as q
     from bit_nf4_quantized_36_b300 import synth
     dev = torch.device("cuda")
-    if args.ncu_target in ("quantize", "dequantize"):
+    if args.ncu_target in ("quantize", "dequantize", "merge"):
         W = synth.sweep_weight_gpu(0, 4, 28672, 8192)
         qw = q.nf4_quantize(W)
         What = q.nf4_dequantize(qw)
+        Am = (torch.randn((16, 8192), device=dev) / 8192 ** 0.5).to(torch.bfloat16)
+        Bm = (torch.randn((28672, 16), device=dev) * 0.01).to(torch.bfloat16)
         for _ in range(3):
             if args.ncu_target == "quantize":
                 q.nf4_quantize(W, out=qw)
+            elif args.ncu_target == "merge":
+                q.qlora_merge(qw, Am, Bm, 32.0, out=What)
             else:
                 q.nf4_dequantize(qw, out=What)
         torch.cuda.synchronize()
@@ -1072,7 +1077,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch the timed steps on the stream, not as a graph")
-    ap.add_argument("--ncu-target", choices=["fused", "decode", "decode_down", "adamw", "quantize", "dequantize"],
+    ap.add_argument("--ncu-target", choices=["fused", "decode", "decode_down", "adamw", "quantize", "dequantize",
+                                             "merge"],
                     default=None,
                     help="untimed short run of one kernel family, for profiler captures")
     ap.add_argument("--decode-m", type=int, default=1)

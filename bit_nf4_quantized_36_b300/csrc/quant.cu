@@ -108,8 +108,35 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-__device__ __forceinline__ uint32_t pack4(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3) {
-    return ((c0 << 4) | c1) | (((c2 << 4) | c3) << 8);
+__device__ __forceinline__ uint64_t f2pack(uint32_t a, uint32_t b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(a), "r"(b));
+    return r;
+}
+__device__ __forceinline__ void f2unpack(uint64_t r, uint32_t &a, uint32_t &b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=r"(a), "=r"(b) : "l"(r));
+}
+
+// nf4_code_fast for two weights at once, with the packed two-lane fp32 instructions (the same
+// IEEE operations, lane by lane).  Returns the byte (code_a << 4) | code_b.
+__device__ __forceinline__ uint32_t nf4_code_pair(float wa, float wb, uint64_t rcp2, const uint32_t *tab,
+                                                  bool &unsure) {
+    const uint64_t w2 = f2pack(__float_as_uint(wa), __float_as_uint(wb));
+    const uint64_t k16 = 0x4180000041800000ull;   // (16, 16)
+    const uint64_t kmag = 0x4B0000114B000011ull;  // (2^23 + 17, 2^23 + 17)
+    uint64_t x2, y2, d2;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(x2) : "l"(w2), "l"(rcp2));
+    asm("fma.rm.f32x2 %0, %1, %2, %3;" : "=l"(y2) : "l"(x2), "l"(k16), "l"(kmag));
+    uint32_t ya, yb;
+    f2unpack(y2, ya, yb);
+    const uint32_t ea = tab[ya & (kNF4Buckets - 1)], eb = tab[yb & (kNF4Buckets - 1)];
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d2) : "l"(x2), "l"(f2pack(ea, eb)));
+    uint32_t da, db;
+    f2unpack(d2, da, db);
+    unsure |= !(fabsf(__uint_as_float(da)) > 0x1p-19f) || !(fabsf(__uint_as_float(db)) > 0x1p-19f);
+    // the code is c + [d >= 0] (d is never -0 here: x0 - t' rounds an exact zero to +0)
+    const uint32_t ca = (ea & 15u) + ((da >> 31) ^ 1u), cb = (eb & 15u) + ((db >> 31) ^ 1u);
+    return (ca << 4) | cb;
 }
 
 __global__ void __launch_bounds__(kQuantThreads, 8) nf4_quantize_groups_kernel(
@@ -119,6 +146,7 @@ __global__ void __launch_bounds__(kQuantThreads, 8) nf4_quantize_groups_kernel(
     __shared__ float s_thr[16];
     __shared__ float s_abs[2][kGroup];  // double-buffered over groups: one barrier per group
     __shared__ uint32_t s_tab[kNF4Buckets];
+    __shared__ double s_stack[48];      // pairwise-tree stack over the run's groups
     if (threadIdx.x < 16) s_thr[threadIdx.x] = tab.thr[threadIdx.x];
     if (threadIdx.x < kNF4Buckets) s_tab[threadIdx.x] = tab.bucket[threadIdx.x];
     __syncthreads();
@@ -131,101 +159,105 @@ __global__ void __launch_bounds__(kQuantThreads, 8) nf4_quantize_groups_kernel(
     const uint32_t lane = threadIdx.x & 31u, l8 = threadIdx.x & 7u;
     const uint32_t gmask = 0xFFu << (lane & 24u);
     const int sub = (int)(threadIdx.x >> 3);  // block within a pass
-    // this thread's two float4 of pass p are src[p * kQPassStride] and src[p * kQPassStride + 8]
-    const float4 *src = W + (B0 + sub) * 16 + l8;
-    uint16_t *dst = codes16 + (B0 + sub) * 16 + l8;
     constexpr int kQPassStride = kQPassBlocks * 16;  // float4 (and code words) per pass
-    // staging slots, rotated by running shared-memory addresses (no index arithmetic per pass)
+    // this thread's two float4 of a pass are W[i] and W[i + 8], and its two code words of that
+    // pass codes16[i] and codes16[i + 8] (the same index): i advances by a pass each time.  `si`
+    // is the index of the pass staged next, which runs kQAhead - 1 passes ahead of the one coded.
+    int64_t si = (B0 + sub) * 16 + l8;
+    int sblk = sub;  // block (within the run) staged next by this thread
+    // staging slots: the slot read in a pass is rslot; the one staged is the slot before it
     const uint32_t slot0 = smem_u32(&s_in[0][0][threadIdx.x]);
     constexpr uint32_t kSlotBytes = 2u * kQuantThreads * 16u, kHalf = kQuantThreads * 16u;
-    uint32_t wslot = slot0, rslot = slot0;
-    auto next = [&](uint32_t a) { return a + kSlotBytes == slot0 + kQAhead * kSlotBytes ? slot0 : a + kSlotBytes; };
-    auto stage = [&](int p) {  // this thread's two float4 of pass p, or zeros past the run's blocks
-        if (p * kQPassBlocks + sub < nblk) {
-            cp_async_16(wslot, src + (int64_t)p * kQPassStride);
-            cp_async_16(wslot + kHalf, src + (int64_t)p * kQPassStride + 8);
+    static_assert(kQAhead == 3, "slot rotation below");
+    auto stage = [&](uint32_t wslot) {  // the next pass's two float4, or zeros past the run's blocks
+        if (sblk < nblk) {
+            cp_async_16(wslot, W + si);
+            cp_async_16(wslot + kHalf, W + si + 8);
         } else {
             asm volatile("st.shared.v4.f32 [%0], {%1, %1, %1, %1};" ::"r"(wslot), "f"(0.0f) : "memory");
             asm volatile("st.shared.v4.f32 [%0], {%1, %1, %1, %1};" ::"r"(wslot + kHalf), "f"(0.0f) : "memory");
         }
         cp_async_commit();  // one group per pass, empty or not, keeps the wait count fixed
-        wslot = next(wslot);
+        si += kQPassStride;
+        sblk += kQPassBlocks;
     };
-#pragma unroll
-    for (int p = 0; p < kQAhead - 1; ++p) stage(p);
+    stage(slot0);
+    stage(slot0 + kSlotBytes);
+    uint32_t rslot = slot0;
 
-    double stack[48];  // thread 0: pairwise-tree stack over the run's groups
-    for (int gi = 0; gi < ngrp; ++gi) {
-        float *sa = s_abs[gi & 1];
-#pragma unroll
-        for (int ps = 0; ps < kQPasses; ++ps) {
-            const int p = gi * kQPasses + ps;
-            stage(p + kQAhead - 1);
-            cp_async_wait<kQAhead - 1>();  // pass p has landed (only this thread reads its slots)
-            float4 v, u;
-            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                         : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(rslot) : "memory");
-            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                         : "=f"(u.x), "=f"(u.y), "=f"(u.z), "=f"(u.w) : "r"(rslot + kHalf) : "memory");
-            rslot = next(rslot);
-            // |w| >= 0 orders like its bit pattern; fmaxf drops NaN (finite input is required)
-            float m = fmaxf(fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))),
-                            fmaxf(fmaxf(fabsf(u.x), fabsf(u.y)), fmaxf(fabsf(u.z), fabsf(u.w))));
-            m = __uint_as_float(__reduce_max_sync(gmask, __float_as_uint(fmaxf(m, 0.0f))));
-            uint32_t c[8] = {kZeroCode, kZeroCode, kZeroCode, kZeroCode, kZeroCode, kZeroCode, kZeroCode, kZeroCode};
-            // the shortcut's error bound needs fl(1/m) normal: 2^-100 <= m < 2^126
-            bool unsure = !(m >= 0x1p-100f && m < 0x1p126f);
-            if (!unsure) {
-                const float rcp = __frcp_rn(m);
-                c[0] = nf4_code_fast(v.x, rcp, s_tab, unsure);
-                c[1] = nf4_code_fast(v.y, rcp, s_tab, unsure);
-                c[2] = nf4_code_fast(v.z, rcp, s_tab, unsure);
-                c[3] = nf4_code_fast(v.w, rcp, s_tab, unsure);
-                c[4] = nf4_code_fast(u.x, rcp, s_tab, unsure);
-                c[5] = nf4_code_fast(u.y, rcp, s_tab, unsure);
-                c[6] = nf4_code_fast(u.z, rcp, s_tab, unsure);
-                c[7] = nf4_code_fast(u.w, rcp, s_tab, unsure);
-            }
-            if (unsure) {
-                c[0] = nf4_code(v.x, m, s_thr);
-                c[1] = nf4_code(v.y, m, s_thr);
-                c[2] = nf4_code(v.z, m, s_thr);
-                c[3] = nf4_code(v.w, m, s_thr);
-                c[4] = nf4_code(u.x, m, s_thr);
-                c[5] = nf4_code(u.y, m, s_thr);
-                c[6] = nf4_code(u.z, m, s_thr);
-                c[7] = nf4_code(u.w, m, s_thr);
-            }
-            if (p * kQPassBlocks + sub < nblk) {
-                dst[(int64_t)p * kQPassStride] = (uint16_t)pack4(c[0], c[1], c[2], c[3]);
-                dst[(int64_t)p * kQPassStride + 8] = (uint16_t)pack4(c[4], c[5], c[6], c[7]);
-            }
-            if (l8 == 0) sa[ps * kQPassBlocks + sub] = m;  // 0 past the last block
+    const int npass = ngrp * kQPasses;
+    float *sa = s_abs[0] + sub;
+#pragma unroll 1
+    for (int p = 0; p < npass; ++p) {
+        stage(rslot == slot0 ? slot0 + 2 * kSlotBytes : rslot - kSlotBytes);
+        cp_async_wait<kQAhead - 1>();  // pass p has landed (only this thread reads its slots)
+        float4 v, u;
+        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(rslot) : "memory");
+        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(u.x), "=f"(u.y), "=f"(u.z), "=f"(u.w) : "r"(rslot + kHalf) : "memory");
+        rslot = rslot == slot0 + 2 * kSlotBytes ? slot0 : rslot + kSlotBytes;
+        // |w| >= 0 orders like its bit pattern; fmaxf drops NaN (finite input is required)
+        float m = fmaxf(fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))),
+                        fmaxf(fmaxf(fabsf(u.x), fabsf(u.y)), fmaxf(fabsf(u.z), fabsf(u.w))));
+        m = __uint_as_float(__reduce_max_sync(gmask, __float_as_uint(fmaxf(m, 0.0f))));
+        // codes of the thread's 8 weights, weight i in byte i / 2 (even i in the high nibble)
+        uint32_t packed = 0x77777777u;  // an all-zero block
+        // the shortcut's error bound needs fl(1/m) normal: 2^-100 <= m < 2^126
+        bool unsure = !(m >= 0x1p-100f && m < 0x1p126f);
+        if (!unsure) {
+            const uint32_t rb = __float_as_uint(__frcp_rn(m));
+            const uint64_t rcp2 = f2pack(rb, rb);
+            packed = nf4_code_pair(v.x, v.y, rcp2, s_tab, unsure) | (nf4_code_pair(v.z, v.w, rcp2, s_tab, unsure) << 8) |
+                     (nf4_code_pair(u.x, u.y, rcp2, s_tab, unsure) << 16) |
+                     (nf4_code_pair(u.z, u.w, rcp2, s_tab, unsure) << 24);
         }
-        // the group is closed.  One barrier: the buffer is written again two groups later, after
-        // the next group's barrier, which every reader of this one has passed
-        __syncthreads();
-        const int64_t gb0 = B0 + (int64_t)gi * kGroup;
-        if (gb0 + (int64_t)threadIdx.x < B1) absmax[gb0 + threadIdx.x] = sa[threadIdx.x];
-        if (threadIdx.x < 32) {
-            double sum = group_sum(sa, lane);
-            if (lane == 0) {  // leaf gi of the run, paired as the tree's levels pair them
-                int lvl = 0;
-                for (int j = gi; j & 1; j >>= 1) sum = __dadd_rn(stack[lvl++], sum);
-                stack[lvl] = sum;
+        if (unsure) {  // rare: the exact rule, one weight at a time
+            packed = (nf4_code(v.x, m, s_thr) << 4) | nf4_code(v.y, m, s_thr) |
+                     (((nf4_code(v.z, m, s_thr) << 4) | nf4_code(v.w, m, s_thr)) << 8) |
+                     (((nf4_code(u.x, m, s_thr) << 4) | nf4_code(u.y, m, s_thr)) << 16) |
+                     (((nf4_code(u.z, m, s_thr) << 4) | nf4_code(u.w, m, s_thr)) << 24);
+        }
+        if (sblk - kQAhead * kQPassBlocks < nblk) {  // this pass's block is one of W's
+            uint16_t *dst = codes16 + (si - kQAhead * kQPassStride);
+            dst[0] = (uint16_t)packed;
+            dst[8] = (uint16_t)(packed >> 16);
+        }
+        if (l8 == 0) *sa = m;  // 0 past the last block
+        sa += kQPassBlocks;
+        if ((p & (kQPasses - 1)) == kQPasses - 1) {
+            // the group is closed.  One barrier: the buffer is written again two groups later,
+            // after the next group's barrier, which every reader of this one has passed
+            const int gi = p / kQPasses;
+            const float *sg = s_abs[gi & 1];
+            sa = s_abs[(gi + 1) & 1] + sub;
+            __syncthreads();
+            if (gi * kGroup + (int)threadIdx.x < nblk)
+                absmax[min64(nb, (int64_t)blockIdx.x * run * kGroup) + gi * kGroup + threadIdx.x] = sg[threadIdx.x];
+            // the group's sum, by warp gi % 8 (the duty rotates so that no warp falls behind);
+            // the push onto the shared stack follows the previous group's push, which its warp
+            // made before reaching this group's barrier
+            if ((int)(threadIdx.x >> 5) == (gi & 7)) {
+                double sum = group_sum(sg, lane);
+                if (lane == 0) {  // leaf gi of the run, paired as the tree's levels pair them
+                    int lvl = 0;
+                    for (int j = gi; j & 1; j >>= 1) sum = __dadd_rn(s_stack[lvl++], sum);
+                    s_stack[lvl] = sum;
+                }
             }
         }
     }
     cp_async_wait<0>();  // the look-ahead copies past the range are empty groups; nothing lands late
+    __syncthreads();     // the last group's push
     if (threadIdx.x == 0) {
         // groups of the run past the last one of W are leaves of +0.0
         for (int64_t j = ngrp; j < run; ++j) {
             double sum = 0.0;
             int lvl = 0;
-            for (int64_t k = j; k & 1; k >>= 1) sum = __dadd_rn(stack[lvl++], sum);
-            stack[lvl] = sum;
+            for (int64_t k = j; k & 1; k >>= 1) sum = __dadd_rn(s_stack[lvl++], sum);
+            s_stack[lvl] = sum;
         }
-        leaves[blockIdx.x] = stack[__ffsll((long long)run) - 1];
+        leaves[blockIdx.x] = s_stack[__ffsll((long long)run) - 1];
     }
 }
 
