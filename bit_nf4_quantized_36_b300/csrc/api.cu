@@ -456,7 +456,7 @@ qlora_status qlora_merge(const qlora_nf4_tensor *W, const uint16_t *A, const uin
     }
     CUtensorMap mCodes, mB, mA, mOut;
     if (!make_map(&mCodes, W->codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)K / 2, (uint64_t)N, (uint64_t)K / 2,
-                  128u, 128u, false) ||
+                  128u, 128u, true) ||
         !map_bf16(&mB, Bq, r_vec ? r : r8, N, 64, 128) || !map_bf16(&mA, A, K, r, 64, 64) ||
         !map_bf16(&mOut, W_out, K, N, 64, 32))
         return QLORA_ERR_CUDA;

@@ -200,19 +200,39 @@ __global__ void __launch_bounds__(kMrgThreads, 1)
         const float mu = __ldg(p.scale_mu);
         const uint32_t r7 = (uint32_t)row & 7u;
         int lt = 0, store_n = 0;
+        // scale code and second-level constant of this thread's two 64-blocks of unit u (zeros
+        // past the matrix, or when there is no unit u)
+        int32_t sq_next[2] = {0, 0};
+        float c2_next[2] = {0.0f, 0.0f};
+        auto load_scale_codes = [&](int u) {
+#pragma unroll
+            for (int g = 0; g < 2; ++g) {
+                sq_next[g] = 0;
+                c2_next[g] = 0.0f;
+                if (u < total) {
+                    const int64_t n = (int64_t)(u / p.k_tiles) * 128 + row;
+                    const int64_t kb = ((u % p.k_tiles) * 256 + half * 128 + g * 64) / 64;
+                    if (n < p.N && kb < p.KB) {
+                        const int64_t b = n * p.KB + kb;
+                        sq_next[g] = __ldg(p.scale_q + b);
+                        c2_next[g] = __ldg(p.scale_c2 + (b >> 8));
+                    }
+                }
+            }
+        };
+        if (kMode == 0) load_scale_codes(blockIdx.x);
         for (int u = blockIdx.x; u < total; u += gridDim.x, ++lt) {
             const int n0 = (u / p.k_tiles) * 128, k0 = (u % p.k_tiles) * 256;
             const int a = lt & 1;
             const int64_t n = (int64_t)n0 + row;
-            // block scales of this thread's two 64-blocks, requested before the waits
+            // block scales of this thread's two 64-blocks: their codes were requested one unit
+            // earlier (a scale-code miss costs a DRAM latency, which a whole unit's epilogue hides);
+            // this unit's values are taken and the next unit's requested
             float sc[2] = {0.0f, 0.0f};
+            if (kMode == 0) {
 #pragma unroll
-            for (int g = 0; g < 2; ++g) {
-                const int64_t kb = (k0 + half * 128 + g * 64) / 64;
-                if (kMode == 0 && n < p.N && kb < p.KB) {
-                    const int64_t b = n * p.KB + kb;
-                    sc[g] = __fmaf_rn((float)__ldg(p.scale_q + b), __fdiv_rn(__ldg(p.scale_c2 + (b >> 8)), 127.0f), mu);
-                }
+                for (int g = 0; g < 2; ++g) sc[g] = __fmaf_rn((float)sq_next[g], __fdiv_rn(c2_next[g], 127.0f), mu);
+                load_scale_codes(u + (int)gridDim.x);
             }
             // one outcome per half: its four warps meet at named barriers below
             // mode 1: this thread's base values and mask words, requested before the waits
@@ -240,7 +260,8 @@ __global__ void __launch_bounds__(kMrgThreads, 1)
             named_barrier_sync(3 + half, 128);
             if (!okw) break;
             tc_fence_after();
-            const uint8_t *crow = sCodes + a * kMrgCodesBytes + row * 128 + half * 64;
+            // the codes tile is stored with the 128-byte swizzle: 16-byte chunk j of a row at j ^ (row & 7)
+            const uint8_t *crow = sCodes + a * kMrgCodesBytes + row * 128;
             for (int g = 0; g < 2; ++g, ++store_n) {
                 uint32_t lo[4], hi[4];
                 if (kMode == 0) build_table(sc[g], p.tab, lo, hi);
@@ -249,16 +270,21 @@ __global__ void __launch_bounds__(kMrgThreads, 1)
                 uint8_t *buf = sOut + ((warp - kMrgEpiWarp0) * 2 + (store_n & 1)) * kMrgWarpOutBytes;
                 if (lane == 0) bulk_wait_group_read<1>();  // this warp's store two groups back has read buf
                 __syncwarp();
+                // both 32-column halves of the group's accumulator in flight before the first use
+                uint32_t racc[2][32];
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    uint32_t r[32];
+                for (int c = 0; c < 2; ++c)
                     tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)a * 256u +
                                            (uint32_t)(half * 128 + g * 64 + c * 32),
-                                       r);
-                    tmem_ld_wait();
+                                       racc[c]);
+                tmem_ld_wait();
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    const uint32_t *r = racc[c];
                     uint32_t words[4];
-                    if (kMode == 0) {
-                        const uint4 cw = *reinterpret_cast<const uint4 *>(crow + g * 32 + c * 16);  // 32 codes
+                    if (kMode == 0) {  // 32 codes: chunk 4 half + 2 g + c of the row
+                        const uint4 cw = *reinterpret_cast<const uint4 *>(
+                            crow + ((((uint32_t)(4 * half + 2 * g + c)) ^ r7) << 4));
                         words[0] = cw.x; words[1] = cw.y; words[2] = cw.z; words[3] = cw.w;
                     }
 #pragma unroll
