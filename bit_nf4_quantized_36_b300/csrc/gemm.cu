@@ -137,7 +137,9 @@ __device__ __forceinline__ UnitInfo unit_info(const FusedArgs &p, int u) {
 
 // One unit = a 256-row weight tile (128 rows per CTA of the pair) x BN tokens x one split of
 // the contraction.  The pair (a cluster of two CTAs on neighbouring SMs) shares every MMA:
-//   - each CTA stages and decodes its own 128 weight rows and TMA-loads BN/2 of the tokens;
+//   - each CTA stages and decodes its own 128 weight rows and TMA-loads BN/2 of the tokens, every
+//     copy completing on a barrier of the CTA that issued it (so each CTA can account for its
+//     own copies when it unwinds after a timeout);
 //   - the even CTA ("leader") issues tcgen05.mma.cta_group::2 with M = 256, N = BN, reading A
 //     and B from both CTAs' shared memory and accumulating into both CTAs' TMEM;
 //   - MMA completion is multicast to both CTAs' barriers; the odd CTA's decode and epilogue
@@ -177,7 +179,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFusedThreads, 1)
     uint8_t *sOut = sC + kStages * kCStageBytes;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sOut + (kMT == 2 ? kOutStageBytes : 0));
     uint64_t *full_c = bars;                 // codes + scales landed (or LoRA k-step announced); local
-    uint64_t *full_b = bars + kStages;       // leader: both CTAs' token tiles landed
+    uint64_t *full_b = bars + kStages;       // this CTA's token tiles landed (each CTA tracks its own copies)
     uint64_t *full_a = bars + 2 * kStages;   // leader: both CTAs' decoded weight tiles written
     // both: the pair MMAs reading stages s & ~1 and s | 1 finished.  Completion is committed once
     // per two stages (on empty[s | 1]) to halve the MMA thread's commit work; empty[s & ~1] is unused.
@@ -230,7 +232,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFusedThreads, 1)
             tma_prefetch_desc(&map_scales);
             tma_prefetch_desc(&map_act);
             tma_prefetch_desc(&map_lora);
-            const uint32_t full_b_leader = mapa_shared(full_b, 0);
             int s = 0;
             uint32_t ph = 0;
             uint32_t issued_parity[kStages];
@@ -246,13 +247,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFusedThreads, 1)
                 for (int j = 0; j < ui.nk; ++j) {
                     if (!mbar_wait_cl(&empty[s | kPairMask], ph ^ 1u, s_abort)) { ok = false; break; }
                     const bool lora = (ui.kt0 + j) >= ui.kt1;
-                    if (leader) mbar_arrive_expect_tx(&full_b[s], 2u * bs_bytes);
+                    mbar_arrive_expect_tx(&full_b[s], bs_bytes);
                     if (skip_codes && !lora) {
                         skip_codes = false;
 #pragma unroll
                         for (int i = 0; i < kMT; ++i)
-                            tma_load_2d_pair(sB + s * bs_bytes + i * b_bytes, &map_act, full_b_leader + (uint32_t)s * 8u,
-                                             (ui.kt0 + j) * 64, m_row + i * p.BN);
+                            tma_load_2d(sB + s * bs_bytes + i * b_bytes, &map_act, &full_b[s], (ui.kt0 + j) * 64,
+                                        m_row + i * p.BN);
                     } else if (!lora) {
                         const int kt = ui.kt0 + j;
                         uint8_t *dc = sC + s * kCStageBytes;
@@ -266,15 +267,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFusedThreads, 1)
                         }
 #pragma unroll
                         for (int i = 0; i < kMT; ++i)
-                            tma_load_2d_pair(sB + s * bs_bytes + i * b_bytes, &map_act, full_b_leader + (uint32_t)s * 8u,
-                                             kt * 64, m_row + i * p.BN);
+                            tma_load_2d(sB + s * bs_bytes + i * b_bytes, &map_act, &full_b[s], kt * 64, m_row + i * p.BN);
                     } else {
                         const int lt = j - (ui.kt1 - ui.kt0);
                         mbar_arrive(&full_c[s]);
 #pragma unroll
                         for (int i = 0; i < kMT; ++i)
-                            tma_load_2d_pair(sB + s * bs_bytes + i * b_bytes, &map_lora, full_b_leader + (uint32_t)s * 8u,
-                                             lt * 64, m_row + i * p.BN);
+                            tma_load_2d(sB + s * bs_bytes + i * b_bytes, &map_lora, &full_b[s], lt * 64, m_row + i * p.BN);
                     }
                     issued[s] = true;
                     issued_parity[s] = ph;
@@ -290,11 +289,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFusedThreads, 1)
                     if (issued[i] && !mbar_wait_cl(&empty[i | kPairMask], issued_parity[i], s_abort)) break;
                 }
             } else {
-                // let copies already in flight land before the CTA can exit
+                // let copies already in flight land before the CTA can exit.  Every copy this CTA
+                // issued completes on one of its own barriers (its token tiles on full_b, its codes
+                // and scales on full_c), so it can wait for all of them; the pair then meets at the
+                // cluster barrier at the end, so neither CTA leaves while the other's copies land.
                 for (int i = 0; i < kStages; ++i) {
                     if (!issued[i]) continue;
                     const uint64_t t0 = globaltimer_ns();
-                    if (leader) while (!mbar_try_wait_cl(&full_b[i], issued_parity[i]) && globaltimer_ns() - t0 < 10000000ull) {}
+                    while (!mbar_try_wait(&full_b[i], issued_parity[i]) && globaltimer_ns() - t0 < 10000000ull) {}
                     while (!mbar_try_wait(&full_c[i], issued_parity[i]) && globaltimer_ns() - t0 < 20000000ull) {}
                 }
             }
@@ -317,7 +319,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFusedThreads, 1)
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)a * 256u;  // tile i at + i * 256
                 for (int j = 0; j < ui.nk; ++j) {
-                    // full_a completes only after the leader's decode group has also seen full_b
+                    // full_a completes only after both CTAs' decode groups have also seen their full_b
                     if (!mbar_wait_cl(&full_a[s], ph, s_abort)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t a_addr = a_base + (uint32_t)s * kATileBytes;
@@ -550,10 +552,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFusedThreads, 1)
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        // the leader's group also waits for the pair's token tiles, so that the
-                        // MMA thread has a single barrier to wait on
-                        if (leader) {
-                            if (!mbar_wait_cl(&full_b[s], ph, s_abort)) ok = false;
+                        // each CTA's group also waits for that CTA's token tiles, so that the
+                        // leader's MMA thread has a single barrier to wait on: full_a completes
+                        // when both CTAs' weight tiles are decoded and both CTAs' token tiles
+                        // have landed
+                        if (!mbar_wait_cl(&full_b[s], ph, s_abort)) {
+                            ok = false;
+                        } else if (leader) {
                             mbar_arrive(&full_a[s]);
                         } else {
                             mbar_arrive_remote(full_a_leader + (uint32_t)s * 8u);

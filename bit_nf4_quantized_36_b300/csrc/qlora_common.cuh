@@ -290,16 +290,6 @@ __device__ __forceinline__ bool mbar_wait_cl(uint64_t *bar, uint32_t parity, vol
         }
     }
 }
-// TMA load into this CTA's shared memory whose completion is counted on the barrier of either
-// CTA of the pair (`bar_cluster` from mapa_shared).
-__device__ __forceinline__ void tma_load_2d_pair(void *dst, const CUtensorMap *map, uint32_t bar_cluster, int32_t x,
-                                                 int32_t y) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
-        " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y)
-        : "memory");
-}
 // TMEM allocation shared by the pair: both CTAs' allocating warps execute these together.
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t *dst_smem, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
