@@ -321,19 +321,23 @@ __global__ void __launch_bounds__(kGvThreads, 1)
         int item_next = fetch();
         item_next = __shfl_sync(0xffffffffu, item_next, 0);
         int item_nn = item_next < a.n_items ? fetch() : a.n_items;
-        int item = -1, rg = 0, slab = 0, slab1 = 0;  // the stage to produce: item, row group, slab; the item's end
-        // advance to the next stage; false at the end of the work
-        auto next_stage = [&]() -> bool {
-            if (item >= 0 && ++slab < slab1) return true;
-            item = item_next;
-            if (item >= a.n_items) return false;
-            const GvItem it = gv_item(a, item);
-            rg = it.rg;
-            slab = it.slab0;
-            slab1 = it.slab1;
+        // A cursor over the stages in item order: the item (n_items at the end), its row group,
+        // the stage's slab, and the item's first and end slabs.  The producer keeps two: the
+        // stage it produces and the one after it, whose scale codes are loaded a whole stage
+        // before they are needed (their latency is not in any stage's path).
+        struct Cur {
+            int item, rg, slab, slab0, slab1;
+        };
+        auto advance = [&](Cur &cu) {
+            if (cu.item >= 0 && cu.item < a.n_items && ++cu.slab < cu.slab1) return;
+            cu.item = item_next < a.n_items ? item_next : a.n_items;
+            if (cu.item >= a.n_items) return;
+            const GvItem it = gv_item(a, cu.item);
+            cu.rg = it.rg;
+            cu.slab = cu.slab0 = it.slab0;
+            cu.slab1 = it.slab1;
             item_next = __shfl_sync(0xffffffffu, item_nn, 0);
             if (item_next < a.n_items) item_nn = fetch();
-            return true;
         };
         // scale codes and group constants of this lane's row of a weight stage
         struct Sc {
@@ -350,8 +354,8 @@ __global__ void __launch_bounds__(kGvThreads, 1)
             const int64_t b0 = (int64_t)n * a.KB + kb0;
             const int nb = a.KB - kb0 < 32 ? a.KB - kb0 : 32;
             if (nb == 32 && (b0 & 15) == 0) {
-                sc.q0 = __ldg(reinterpret_cast<const uint4 *>(a.scale_q + b0));
-                sc.q1 = __ldg(reinterpret_cast<const uint4 *>(a.scale_q + b0 + 16));
+                sc.q0 = ldg_pin_v4(a.scale_q + b0);
+                sc.q1 = ldg_pin_v4(a.scale_q + b0 + 16);
             } else {
                 uint32_t wv[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
                 for (int jb = 0; jb < nb; ++jb)
@@ -359,12 +363,16 @@ __global__ void __launch_bounds__(kGvThreads, 1)
                 sc.q0 = make_uint4(wv[0], wv[1], wv[2], wv[3]);
                 sc.q1 = make_uint4(wv[4], wv[5], wv[6], wv[7]);
             }
-            sc.c0 = __ldg(a.scale_c2 + (b0 >> 8));
-            sc.c1 = __ldg(a.scale_c2 + ((b0 + nb - 1) >> 8));
+            sc.c0 = __uint_as_float(ldg_pin_u32(a.scale_c2 + (b0 >> 8)));
+            sc.c1 = __uint_as_float(ldg_pin_u32(a.scale_c2 + ((b0 + nb - 1) >> 8)));
         };
-        bool more = next_stage();
-        Sc sc_cur;
-        if (more) load_scales(rg, slab, sc_cur);
+        Cur ca{-1, 0, 0, 0, 0};
+        advance(ca);
+        Cur cb = ca;
+        advance(cb);
+        Sc sc_a, sc_b;
+        if (ca.item < a.n_items) load_scales(ca.rg, ca.slab, sc_a);
+        if (cb.item < a.n_items) load_scales(cb.rg, cb.slab, sc_b);
         int t = 0;
         bool ok = true;
         for (;; ++t) {
@@ -380,31 +388,29 @@ __global__ void __launch_bounds__(kGvThreads, 1)
             }
             const uint32_t sb = stage_addr(slot), sd = side_addr(slot);
             int4 *desc = reinterpret_cast<int4 *>(sm0 + sd + kGvSideDesc);
-            if (!more) {  // the end: a stop stage
+            if (ca.item >= a.n_items) {  // the end: a stop stage
                 if (lane == 0) {
                     desc[0] = make_int4(kGvKindStop, 0, 0, 0);
                     mbar_arrive(&full[slot]);
                 }
                 break;
             }
+            const int rg = ca.rg, slab = ca.slab;
             const int kind = rg < a.RU ? kGvKindAdapter : kGvKindWeight;
-            const bool last_of_item = slab + 1 == slab1;
+            const bool last_of_item = slab + 1 == ca.slab1;
             // the stage after this one (its x is loaded ahead by the consumers)
             int nxt_kind = kGvKindStop, nxt_slab = 0;
-            if (!last_of_item) {
-                nxt_kind = kind;
-                nxt_slab = slab + 1;
-            } else if (item_next < a.n_items) {
-                const GvItem nt = gv_item(a, item_next);
-                nxt_kind = nt.rg < a.RU ? kGvKindAdapter : kGvKindWeight;
-                nxt_slab = nt.slab0;
+            if (cb.item < a.n_items) {
+                nxt_kind = cb.rg < a.RU ? kGvKindAdapter : kGvKindWeight;
+                nxt_slab = cb.slab;
             }
             if (lane == 0) {
-                desc[0] = make_int4(kind, rg, slab, item);
+                desc[0] = make_int4(kind, rg, slab, ca.item);
                 // flags: bit 0 the item's first stage, bit 1 the item holds the row group's last slab
-                const int flags = (slab == gv_item(a, item).slab0 ? 1 : 0) | (slab1 == NS ? 2 : 0);
+                const int flags = (slab == ca.slab0 ? 1 : 0) | (ca.slab1 == NS ? 2 : 0);
                 desc[1] = make_int4(last_of_item ? 1 : 0, nxt_kind, nxt_slab, flags);
             }
+            const Sc &sc_cur = sc_a;
             if (kind == kGvKindWeight) {
                 // a slab of eight whole units: one 3-D box; otherwise one 2-D box per unit (the
                 // 2-D map checks the columns against K / 2, the 3-D map covers whole units only)
@@ -423,32 +429,61 @@ __global__ void __launch_bounds__(kGvThreads, 1)
                 const int b0 = n * a.KB + kb0;
                 const int jsplit = 256 - (b0 & 255);
                 const int jvalid = n < a.N ? (a.KB - kb0 < 32 ? a.KB - kb0 : 32) : 0;
-                const float k0 = __fdiv_rn(sc_cur.c0, 127.0f), k1 = __fdiv_rn(sc_cur.c1, 127.0f);
+                const float k0 = __fdiv_rn(sc_cur.c0, 127.0f);
                 const uint32_t qv[8] = {sc_cur.q0.x, sc_cur.q0.y, sc_cur.q0.z, sc_cur.q0.w,
                                         sc_cur.q1.x, sc_cur.q1.y, sc_cur.q1.z, sc_cur.q1.w};
                 const uint32_t srow = sd + kGvSideS + (uint32_t)lane * (kGvScaleLd * 4);
+                // s'_b = fmaf(q, k, mu), the int8 code as an exact float (the byte q + 128 spliced
+                // into 2^23's mantissa, minus 2^23 + 128)
+                if (jvalid == 32 && jsplit >= 32) {
+                    // the row's 32 blocks are all in W and in one group: two at a time, with the
+                    // packed two-lane fp32 instructions (the same IEEE operations)
+                    const uint64_t kk = f2pack(__float_as_uint(k0), __float_as_uint(k0));
+                    const uint64_t mm = f2pack(__float_as_uint(mu), __float_as_uint(mu));
+                    const uint64_t off = 0x4B0000804B000080ull;  // (2^23 + 128, 2^23 + 128)
 #pragma unroll
-                for (int w4 = 0; w4 < 8; ++w4) {
-                    // s'_b = fmaf(q, k, mu), the int8 code as an exact float (the byte q + 128
-                    // spliced into 2^23's mantissa); blocks jb < jsplit use the row's first group,
-                    // the rest the next one; blocks past KB and rows past N get 0
-                    const uint32_t qw = qv[w4] ^ 0x80808080u;
-                    float v[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int jb = 4 * w4 + e;
-                        const float qf = __fsub_rn(__uint_as_float(prmt(qw, 0x4B000000u, 0x7440u + (uint32_t)e)),
-                                                   8388736.0f);  // 2^23 + 128
-                        v[e] = jb < jvalid ? __fmaf_rn(qf, jb < jsplit ? k0 : k1, mu) : 0.0f;
+                    for (int w4 = 0; w4 < 8; ++w4) {
+                        const uint32_t qw = qv[w4] ^ 0x80808080u;
+                        uint64_t p0 = f2pack(prmt(qw, 0x4B000000u, 0x7440u), prmt(qw, 0x4B000000u, 0x7441u));
+                        uint64_t p1 = f2pack(prmt(qw, 0x4B000000u, 0x7442u), prmt(qw, 0x4B000000u, 0x7443u));
+                        asm("sub.rn.f32x2 %0, %0, %1;" : "+l"(p0) : "l"(off));
+                        asm("sub.rn.f32x2 %0, %0, %1;" : "+l"(p1) : "l"(off));
+                        asm("fma.rn.f32x2 %0, %0, %1, %2;" : "+l"(p0) : "l"(kk), "l"(mm));
+                        asm("fma.rn.f32x2 %0, %0, %1, %2;" : "+l"(p1) : "l"(kk), "l"(mm));
+                        uint32_t v0, v1, v2, v3;
+                        f2unpack(p0, v0, v1);
+                        f2unpack(p1, v2, v3);
+                        sts128f(srow + 16u * w4, __uint_as_float(v0), __uint_as_float(v1), __uint_as_float(v2),
+                                __uint_as_float(v3));
                     }
-                    sts128f(srow + 16u * w4, v[0], v[1], v[2], v[3]);
+                } else {
+                    // blocks jb < jsplit use the row's first group, the rest the next one; blocks
+                    // past KB and rows past N get 0
+                    const float k1 = __fdiv_rn(sc_cur.c1, 127.0f);
+#pragma unroll
+                    for (int w4 = 0; w4 < 8; ++w4) {
+                        const uint32_t qw = qv[w4] ^ 0x80808080u;
+                        float v[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int jb = 4 * w4 + e;
+                            const float qf = __fsub_rn(__uint_as_float(prmt(qw, 0x4B000000u, 0x7440u + (uint32_t)e)),
+                                                       8388736.0f);  // 2^23 + 128
+                            v[e] = jb < jvalid ? __fmaf_rn(qf, jb < jsplit ? k0 : k1, mu) : 0.0f;
+                        }
+                        sts128f(srow + 16u * w4, v[0], v[1], v[2], v[3]);
+                    }
                 }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&full[slot]);
-            // the next stage, and its scale codes into registers
-            more = next_stage();
-            if (more) load_scales(rg, slab, sc_cur);
+            // on to the next stage; the scale codes of the one after it into registers
+            ca = cb;
+            sc_a = sc_b;
+            if (cb.item < a.n_items) {
+                advance(cb);
+                if (cb.item < a.n_items) load_scales(cb.rg, cb.slab, sc_b);
+            }
         }
         if (!ok && lane == 0) {
             // on a timeout, let the copies already issued land (bounded) before the CTA can exit
