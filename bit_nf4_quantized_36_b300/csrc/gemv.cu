@@ -665,8 +665,7 @@ __global__ void __launch_bounds__(kGvThreads, 1)
     // B's rank pairs are 32-bit words when r is even (then every pair starts at an even element)
     const bool b_pairs = (a.r & 1) == 0;
     // one stage: xf holds its x (loaded during the previous stage), the next stage's x goes to xn;
-    // false at the end of the work (or when a wait ran out).  Called with the two buffers
-    // swapped on alternate stages, so that no copy is made.
+    // false at the end of the work (or when a wait ran out).
     auto stage = [&](int t, uint32_t (&xf)[4][8], uint32_t (&xn)[4][8]) -> bool {
         const int slot = t % kGvStages;
         uint32_t okw = 1;
@@ -858,9 +857,14 @@ __global__ void __launch_bounds__(kGvThreads, 1)
             return true;
     };
     uint32_t xa[4][8], xb[4][8];
-    for (int t = 0;; t += 2) {
+    for (int t = 0;; ++t) {
         if (!stage(t, xa, xb)) break;
-        if (!stage(t + 1, xb, xa)) break;
+        // the next stage's x becomes the current one (a register copy: one copy of the stage body
+        // keeps the code small enough for the instruction cache, which two alternating ones did not)
+#pragma unroll
+        for (int jb = 0; jb < 4; ++jb)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) xa[jb][i] = xb[jb][i];
     }
     // pass the end on to the finisher (bounded wait for the ring slot)
     {
