@@ -7,10 +7,15 @@ import os
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libqlora.so")
+# the same library built with device-side bounds checks (build.build(checks=True)); a process
+# selects it with QLORA_LIB=checked before the first call
+CHECKED_LIB_PATH = os.path.join(HERE, "libqlora_checked.so")
+if os.environ.get("QLORA_LIB") == "checked":
+    LIB_PATH = CHECKED_LIB_PATH
 
 QLORA_STATUS = {
     0: "QLORA_OK", 1: "QLORA_ERR_INVALID_ARG", 2: "QLORA_ERR_UNSUPPORTED_SHAPE", 3: "QLORA_ERR_MISALIGNED",
-    4: "QLORA_ERR_WORKSPACE", 5: "QLORA_ERR_CUDA", 6: "QLORA_ERR_TIMEOUT",
+    4: "QLORA_ERR_WORKSPACE", 5: "QLORA_ERR_CUDA", 6: "QLORA_ERR_TIMEOUT", 7: "QLORA_ERR_DEVICE_CHECK",
 }
 
 # every function declared in include/qlora.h
@@ -29,6 +34,7 @@ EXPORTS = (
 
 QLORA_PAGE_HOST = -1
 QLORA_INJECT_SKIP_CODES = 1
+QLORA_INJECT_BOUNDS = 2
 
 
 class NF4TensorStruct(ctypes.Structure):

@@ -8,6 +8,8 @@ import subprocess
 HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 LIB_PATH = os.path.join(HERE, "libqlora.so")
+# the same sources with device-side bounds checks (QLORA_DEVICE_CHECKS): for tests and debugging
+CHECKED_LIB_PATH = os.path.join(HERE, "libqlora_checked.so")
 SRC_MAIN = os.path.join(HERE, "csrc", "libqlora.cu")
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 
@@ -26,23 +28,25 @@ def _sources():
             + glob.glob(os.path.join(ROOT, "include", "*.h")))
 
 
-def needs_build() -> bool:
-    if not os.path.exists(LIB_PATH):
+def needs_build(path: str = LIB_PATH) -> bool:
+    if not os.path.exists(path):
         return True
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(path)
     return any(os.path.getmtime(s) > t for s in _sources())
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and not needs_build():
-        return LIB_PATH
-    tmp = LIB_PATH + ".tmp%d" % os.getpid()
-    cmd = [NVCC, *NVCC_FLAGS, "-o", tmp, SRC_MAIN]
+def build(force: bool = False, verbose: bool = False, checks: bool = False) -> str:
+    """Compile libqlora.so, or with `checks` libqlora_checked.so (device-side bounds checks)."""
+    path = CHECKED_LIB_PATH if checks else LIB_PATH
+    if not force and not needs_build(path):
+        return path
+    tmp = path + ".tmp%d" % os.getpid()
+    cmd = [NVCC, *NVCC_FLAGS, *(["-DQLORA_DEVICE_CHECKS"] if checks else []), "-o", tmp, SRC_MAIN]
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
     subprocess.check_call(cmd)
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, path)
+    return path
 
 
 if __name__ == "__main__":

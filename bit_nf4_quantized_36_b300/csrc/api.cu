@@ -395,6 +395,7 @@ const char *qlora_status_string(qlora_status s) {
         case QLORA_ERR_WORKSPACE: return "workspace missing or too small";
         case QLORA_ERR_CUDA: return "CUDA error";
         case QLORA_ERR_TIMEOUT: return "device-side wait timed out";
+        case QLORA_ERR_DEVICE_CHECK: return "device-side bounds check failed";
     }
     return "unknown status";
 }
@@ -759,11 +760,17 @@ qlora_status qlora_check_device_error(void *stream) {
     if (cudaMemcpyFromSymbol(&word, g_error_word, sizeof(word)) != cudaSuccess) return QLORA_ERR_CUDA;
     if (word && cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero)) != cudaSuccess) return QLORA_ERR_CUDA;
     if (word & kErrTimeout) return QLORA_ERR_TIMEOUT;
-    return (word & kErrLayout) ? QLORA_ERR_CUDA : QLORA_OK;
+    if (word & kErrLayout) return QLORA_ERR_CUDA;
+    return (word & kErrBounds) ? QLORA_ERR_DEVICE_CHECK : QLORA_OK;
 }
 
 qlora_status qlora_test_inject(uint32_t flags) {
-    if (flags & ~(uint32_t)QLORA_INJECT_SKIP_CODES) return QLORA_ERR_INVALID_ARG;
+#ifdef QLORA_DEVICE_CHECKS
+    const uint32_t known = QLORA_INJECT_SKIP_CODES | QLORA_INJECT_BOUNDS;
+#else
+    const uint32_t known = QLORA_INJECT_SKIP_CODES;
+#endif
+    if (flags & ~known) return QLORA_ERR_INVALID_ARG;
     return cudaMemcpyToSymbol(g_inject, &flags, sizeof(flags)) == cudaSuccess ? QLORA_OK : QLORA_ERR_CUDA;
 }
 

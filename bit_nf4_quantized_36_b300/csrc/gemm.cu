@@ -441,14 +441,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFusedThreads, 1)
                             const int m = m0 + c * 32 + jj;
                             if (m < p.M) {
                                 __nv_bfloat16 h = __float2bfloat16_rn(__uint_as_float(r[jj]));
-                                p.out[(int64_t)m * p.wdim + f] = *reinterpret_cast<uint16_t *>(&h);
+                                if (QLORA_IN_BOUNDS((int64_t)m * p.wdim + f < (int64_t)p.M * p.wdim))
+                                    p.out[(int64_t)m * p.wdim + f] = *reinterpret_cast<uint16_t *>(&h);
                             }
                         }
                     } else {
 #pragma unroll
                         for (int jj = 0; jj < 32; ++jj) {
                             const int m = m0 + c * 32 + jj;
-                            if (m < p.M) p.partial[((int64_t)ui.split * p.M + m) * p.wdim + f] = __uint_as_float(r[jj]);
+                            if (m < p.M && QLORA_IN_BOUNDS(ui.split < p.splits))
+                                p.partial[((int64_t)ui.split * p.M + m) * p.wdim + f] = __uint_as_float(r[jj]);
                         }
                     }
                 }
@@ -593,7 +595,7 @@ __device__ __forceinline__ void proj_store(const ProjArgs &a, int64_t i, int j, 
         if (j < a.ld_h) {
             __nv_bfloat16 h = __float2bfloat16_rn(__fmul_rn(v, a.col_scale ? a.col_scale[j] : a.scale));
             const uint16_t hb = *reinterpret_cast<uint16_t *>(&h);
-            a.out_h[i * a.ld_h + j] = hb;
+            if (QLORA_IN_BOUNDS(i < a.Mp)) a.out_h[i * a.ld_h + j] = hb;
             if (a.out_h2 && j < a.r) a.out_h2[i * a.r + j] = hb;
         }
     } else if (a.mode == 1) {

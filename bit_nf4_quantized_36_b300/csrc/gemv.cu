@@ -516,13 +516,14 @@ __global__ void __launch_bounds__(kGvThreads, 1)
                     const int jj = rg * kGvRows + row;
                     const __nv_bfloat16 hh = __float2bfloat16_rn(__fmul_rn(a.s, v[e]));
                     const uint16_t hb = *reinterpret_cast<const uint16_t *>(&hh);
-                    a.Ubf[m * a.r32 + jj] = hb;
+                    if (QLORA_IN_BOUNDS(m < kGvMaxM && jj < a.r32)) a.Ubf[m * a.r32 + jj] = hb;
                     if (a.U_save && m < a.M && jj < a.r) a.U_save[(int64_t)m * a.r + jj] = hb;
                 } else {
                     const int nn = (rg - a.RU) * kGvRows + row;
                     if (m < a.M && nn < a.N) {
                         const __nv_bfloat16 hh = __float2bfloat16_rn(v[e]);
-                        a.Y[(int64_t)m * a.N + nn] = *reinterpret_cast<const uint16_t *>(&hh);
+                        if (QLORA_IN_BOUNDS((int64_t)m * a.N + nn < (int64_t)a.M * a.N))
+                            a.Y[(int64_t)m * a.N + nn] = *reinterpret_cast<const uint16_t *>(&hh);
                     }
                 }
             }
@@ -608,8 +609,9 @@ __global__ void __launch_bounds__(kGvThreads, 1)
                     finish_vals(d.y, v);
                 } else {
                     float *pp = a.partial + (int64_t)d.z * (kGvAcc * 32) + lane;
+                    if (QLORA_IN_BOUNDS(d.z >= 0 && d.z < a.n_items))
 #pragma unroll
-                    for (int e = 0; e < kGvAcc; ++e) __stcg(pp + 32 * e, v[e]);
+                        for (int e = 0; e < kGvAcc; ++e) __stcg(pp + 32 * e, v[e]);
                     if (lane == i) my_rg = d.y;
                 }
             }

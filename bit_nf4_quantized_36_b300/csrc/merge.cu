@@ -214,7 +214,7 @@ __global__ void __launch_bounds__(kMrgThreads, 1)
                     const int64_t kb = ((u % p.k_tiles) * 256 + half * 128 + g * 64) / 64;
                     if (n < p.N && kb < p.KB) {
                         const int64_t b = n * p.KB + kb;
-                        sq_next[g] = __ldg(p.scale_q + b);
+                        if (QLORA_IN_BOUNDS(b < p.N * p.KB)) sq_next[g] = __ldg(p.scale_q + b);
                         c2_next[g] = __ldg(p.scale_c2 + (b >> 8));
                     }
                 }

@@ -43,15 +43,32 @@ struct NF4Tables {
 // Device error word (latched; read and cleared by qlora_check_device_error).
 // ---------------------------------------------------------------------------------------
 // kErrTimeout: a bounded wait gave up; kErrLayout: a kernel found its shared memory laid out
-// other than it was built for (it then does no work)
-enum : uint32_t { kErrTimeout = 1u, kErrLayout = 2u };
+// other than it was built for (it then does no work); kErrBounds: (device-check builds only) an
+// index failed its bounds check, and the access was skipped
+enum : uint32_t { kErrTimeout = 1u, kErrLayout = 2u, kErrBounds = 4u };
 // Defined here: the library is one translation unit (libqlora.cu includes every .cu file).
 __device__ uint32_t g_error_word = 0;
-// Test hook (qlora_test_inject): kInjectSkipCodes makes the leader CTA of the fused GEMM's first
+// Test hooks (qlora_test_inject): kInjectSkipCodes makes the leader CTA of the fused GEMM's first
 // pair skip the codes copy of its first k-step, and with it that stage's arrival on the barrier
 // its decode warps wait on, so the bounded wait runs out and the kernel unwinds without a fault.
-enum : uint32_t { kInjectSkipCodes = 1u };
+// kInjectBounds (device-check builds only) moves one store index of nf4_dequantize past the end
+// of its output, so that its bounds check fires (and skips the store).
+enum : uint32_t { kInjectSkipCodes = 1u, kInjectBounds = 2u };
 __device__ uint32_t g_inject = 0;
+
+// Device-side bounds checks.  Built with QLORA_DEVICE_CHECKS (libqlora_checked.so), QLORA_IN_BOUNDS
+// tests an index condition before a global-memory access: when it fails, the kernel latches
+// kErrBounds in the error word and skips the access (no trap: the context stays usable and
+// qlora_check_device_error reports it).  In the released library the condition is not evaluated.
+#ifdef QLORA_DEVICE_CHECKS
+__device__ __forceinline__ bool device_check(bool ok) {
+    if (!ok) atomicOr(&g_error_word, kErrBounds);
+    return ok;
+}
+#define QLORA_IN_BOUNDS(cond) (::qlora::device_check((cond)))
+#else
+#define QLORA_IN_BOUNDS(cond) (true)
+#endif
 
 __device__ __forceinline__ uint64_t globaltimer_ns() {
     uint64_t t;

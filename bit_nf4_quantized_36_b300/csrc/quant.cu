@@ -219,9 +219,11 @@ __global__ void __launch_bounds__(kQuantThreads, 8) nf4_quantize_groups_kernel(
                      (((nf4_code(u.z, m, s_thr) << 4) | nf4_code(u.w, m, s_thr)) << 24);
         }
         if (sblk - kQAhead * kQPassBlocks < nblk) {  // this pass's block is one of W's
-            uint16_t *dst = codes16 + (si - kQAhead * kQPassStride);
-            dst[0] = (uint16_t)packed;
-            dst[8] = (uint16_t)(packed >> 16);
+            const int64_t ci = si - kQAhead * kQPassStride;  // this pass's first code word
+            if (QLORA_IN_BOUNDS(ci >= 0 && ci + 8 < nb * 16)) {
+                codes16[ci] = (uint16_t)packed;
+                codes16[ci + 8] = (uint16_t)(packed >> 16);
+            }
         }
         if (l8 == 0) *sa = m;  // 0 past the last block
         sa += kQPassBlocks;
@@ -232,8 +234,10 @@ __global__ void __launch_bounds__(kQuantThreads, 8) nf4_quantize_groups_kernel(
             const float *sg = s_abs[gi & 1];
             sa = s_abs[(gi + 1) & 1] + sub;
             __syncthreads();
-            if (gi * kGroup + (int)threadIdx.x < nblk)
-                absmax[min64(nb, (int64_t)blockIdx.x * run * kGroup) + gi * kGroup + threadIdx.x] = sg[threadIdx.x];
+            if (gi * kGroup + (int)threadIdx.x < nblk) {
+                const int64_t bi = min64(nb, (int64_t)blockIdx.x * run * kGroup) + gi * kGroup + threadIdx.x;
+                if (QLORA_IN_BOUNDS(bi < nb)) absmax[bi] = sg[threadIdx.x];
+            }
             // the group's sum, by warp gi % 8 (the duty rotates so that no warp falls behind);
             // the push onto the shared stack follows the previous group's push, which its warp
             // made before reaching this group's barrier
@@ -376,7 +380,12 @@ __global__ void __launch_bounds__(256, 8) nf4_dequantize_kernel(const uint32_t *
                 __nv_bfloat162 p = __floats2bfloat162_rn(e0, e1);
                 w[j] = *reinterpret_cast<uint32_t *>(&p);
             }
-            __stcs(out + t, make_uint4(w[0], w[1], w[2], w[3]));
+            int64_t ts = t;
+#ifdef QLORA_DEVICE_CHECKS
+            // test hook: the first thread's first store index moved past the end of the output
+            if (t == 0 && (*(volatile uint32_t *)&g_inject & kInjectBounds)) ts = n8;
+#endif
+            if (QLORA_IN_BOUNDS(ts < n8)) __stcs(out + ts, make_uint4(w[0], w[1], w[2], w[3]));
         }
     }
 }

@@ -45,7 +45,8 @@ typedef enum {
     QLORA_ERR_MISALIGNED = 3,       /* a pointer is not 16-byte aligned                        */
     QLORA_ERR_WORKSPACE = 4,        /* workspace NULL or smaller than the size query returns  */
     QLORA_ERR_CUDA = 5,             /* a CUDA runtime/driver call or a kernel launch failed    */
-    QLORA_ERR_TIMEOUT = 6           /* a device-side bounded wait ran out (from the check call)*/
+    QLORA_ERR_TIMEOUT = 6,          /* a device-side bounded wait ran out (from the check call)*/
+    QLORA_ERR_DEVICE_CHECK = 7      /* device-check build: an index failed its bounds check    */
 } qlora_status;
 
 /* One NF4 matrix with double-quantized scales.
@@ -263,7 +264,9 @@ qlora_status qlora_adamw_step(const qlora_adamw *hp, int64_t t, int64_t n, float
 
 /* Synchronizes `stream`, then reads and clears the library's device error word on the current
  * device.  QLORA_OK, QLORA_ERR_TIMEOUT (a pipelined kernel gave up a bounded wait and exited
- * early; its outputs are undefined) or QLORA_ERR_CUDA. */
+ * early; its outputs are undefined), QLORA_ERR_DEVICE_CHECK (only from libqlora_checked.so, the
+ * same library built with device-side bounds checks: an index failed its check and the access
+ * was skipped; the outputs are undefined) or QLORA_ERR_CUDA. */
 qlora_status qlora_check_device_error(void *stream);
 
 /* Test hook for the device-side failure path (not for normal use).  flags ==
@@ -276,6 +279,11 @@ qlora_status qlora_check_device_error(void *stream);
  * Synchronous with respect to the host; do not change it while calls are in flight.  Returns
  * QLORA_ERR_INVALID_ARG for an unknown flag, QLORA_ERR_CUDA if the device is unusable. */
 #define QLORA_INJECT_SKIP_CODES 1u
+/* flags == QLORA_INJECT_BOUNDS (libqlora_checked.so only; QLORA_ERR_INVALID_ARG from the released
+ * library) moves one store index of each following nf4_dequantize past the end of its output:
+ * the kernel's bounds check skips that store and the next qlora_check_device_error returns
+ * QLORA_ERR_DEVICE_CHECK.  Nothing is written out of bounds. */
+#define QLORA_INJECT_BOUNDS 2u
 qlora_status qlora_test_inject(uint32_t flags);
 
 /* Short English description of a status code (static string). */
