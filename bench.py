@@ -364,7 +364,9 @@ def run_ours(args):
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     dist = None
-    if world > 1:
+    # under torchrun (LOCAL_RANK set) the process group is formed even for one rank, so that the
+    # multi-GPU path (NCCL group, barriers, all-reduces, max over ranks) runs as it would at N > 1
+    if world > 1 or "LOCAL_RANK" in os.environ:
         import torch.distributed as dist
         torch.cuda.set_device(local)
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
