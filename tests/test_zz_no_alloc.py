@@ -64,7 +64,9 @@ def test_noalloc_call_allocates_nothing_and_launches_two_kernels(L):
     # the absmax/code kernel and the scale double-quantization kernel, nothing else
     assert L.qlora_launch_count() - n0 == 2
     assert torch.cuda.memory_allocated() == alloc0
-    assert torch.cuda.mem_get_info()[0] == free0
+    # device-wide free memory cannot have dropped (it may rise while the driver reclaims what an
+    # earlier process on the device released)
+    assert torch.cuda.mem_get_info()[0] >= free0
     ref = q.nf4_quantize(W)
     for a, b in zip(_host(out), _host(ref)):
         np.testing.assert_array_equal(a.view(np.uint8), b.view(np.uint8))
