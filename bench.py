@@ -645,15 +645,17 @@ def run_ours(args):
 
 
 def replay_timed(torch, fn, flush, reps=10, L=None, kernel_events=None):
-    """Device time of fn() with host enqueue kept out of the timing.  fn runs once untimed
-    (allocations, first-call set-up); then `reps` repetitions, each an L2 flush followed by fn()
-    between two events, are captured into one CUDA graph and replayed once: every kernel of
-    every repetition runs, and the events see only device time.  With `kernel_events` (2 events
+    """Device time of fn() with host enqueue kept out of the timing.  fn runs three times untimed
+    (allocations, first-call set-up, clocks); then `reps` repetitions, each an L2 flush followed by
+    fn() between two events, are captured into one CUDA graph and replayed twice, the events
+    keeping the second replay's times: every kernel of every repetition runs, and the events see
+    only device time.  With `kernel_events` (2 events
     per timed launch) the library's kernel timer is armed during the capture, so that its event
     pairs around each timed kernel become graph nodes too.  Returns (median call ms, the timed
     kernels' durations in launch order or None, how).  If the capture fails the repetitions run
     as stream launches and `how` says so."""
-    fn()
+    for _ in range(3):
+        fn()
     torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True, external=True), torch.cuda.Event(enable_timing=True, external=True))
           for _ in range(reps)]
@@ -681,6 +683,10 @@ def replay_timed(torch, fn, flush, reps=10, L=None, kernel_events=None):
             with torch.cuda.graph(graph, stream=cap):
                 body()
         torch.cuda.current_stream().wait_stream(cap)
+        torch.cuda.synchronize()
+        # a first replay (graph upload, clocks up); the events, graph nodes like the kernel
+        # timer's, keep the second replay's times
+        graph.replay()
         torch.cuda.synchronize()
         graph.replay()
     except Exception as e:
