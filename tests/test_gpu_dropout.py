@@ -40,6 +40,7 @@ def test_dropout_mask_is_the_generators(orc):
 
 
 @pytest.mark.parametrize("M,N,K,r,p", [
+    (5, 264, 4160, 8, 0.1),      # the one-launch GEMV (masked X for the adapter term only)
     (17, 256, 512, 8, 0.05),     # small-M kernel
     (300, 264, 320, 24, 0.5),    # CTA pairs, one token tile, ragged
     (600, 256, 512, 16, 0.1),    # CTA pairs, two token tiles

@@ -94,6 +94,8 @@ def test_tiny_workload(orc):
     (7, 264, 4160, 16),    # seven tokens: eight token columns of the GEMV, one unused
     (8, 136, 2112, 3),     # eight tokens, ragged rows, a contraction tail inside a 256-step
     (3, 72, 9216, 8),      # a row's five 2048-column slabs in two work items (partials added in order)
+    (5, 256, 2048, 256),   # the GEMV at the maximum rank: eight adapter row groups, sixteen rank chunks
+    (4, 136, 1024, 72),    # the GEMV with a rank that is not a multiple of 32
     (1, 64, 8256, 8),      # the same with a 64-column tail unit (per-unit boxes for the last slab)
     (12, 264, 4160, 8),    # twelve tokens: the small-M tensor kernel
     (600, 520, 640, 16),   # two 256-token tiles per unit: token ranges that cross weight tiles
@@ -118,6 +120,17 @@ def test_deterministic():
     b = run_layer(inp)
     for k in ("Y", "U", "dX", "dA", "dB"):
         assert torch.equal(a[k], b[k]), k
+
+
+def test_gemv_deterministic():
+    """The one-launch GEMV takes its work items from a launch-wide counter (which CTA does which
+    item changes from call to call) and still adds every row group's partials in item order."""
+    inp = synth.layer_inputs(203, 6, 1000 - 1000 % 8, 6208, 24, 48.0)
+    a = run_layer(inp, fwd_only=True)
+    for _ in range(3):
+        b = run_layer(inp, fwd_only=True)
+        for k in ("Y", "U"):
+            assert torch.equal(a[k], b[k]), k
 
 
 def test_adapter_b_zero(orc):
