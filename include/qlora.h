@@ -191,7 +191,9 @@ qlora_status qlora_merge(const qlora_nf4_tensor *W, const uint16_t *A, const uin
 /* Forward of the layer ("Parte 4 - LoRA encima", h = W^ x + (alpha/r) B A x):
  *   Y [M, N] (bf16) = X W^T + U B^T,   U = bf16((alpha/r) X A^T)  [M, r]
  * X [M, K] bf16, A [r, K] bf16, B [N, r] bf16; fp32 accumulation; W^ is dequantized inside the
- * GEMM main loop and never written to memory.
+ * GEMM main loop and never written to memory.  For M <= 8 the block scale is instead factored out
+ * of each 64-weight block's dot product (the bf16 levels times x, summed in fp32, times the exact
+ * block scale s'_b), so Y is the product with W^ up to the layer tolerance, not bit for bit.
  * U_save (nullable) receives U [M, r] (bf16, already multiplied by alpha/r) for the backward. */
 qlora_status qlora_linear_fwd(const qlora_nf4_tensor *W, const uint16_t *X, int64_t M,
                               const uint16_t *A, const uint16_t *B, int32_t r, float alpha,
@@ -300,9 +302,9 @@ void qlora_nf4_levels(float out[16]);
  * cudaEvent_t handles created by the caller; from now on the library records events[2i] just
  * before and events[2i+1] just after the i-th weight-streaming step of a layer call: the
  * launch of the fused NF4-dequant GEMM kernel (forward or backward dX, with the reduction of its
- * partials when the contraction is split), or, for a forward of
- * up to eight tokens, the register-resident GEMV and its finishing kernel; on the launch stream, until
- * `capacity` steps are recorded.
+ * partials when the contraction is split), or, for a forward of up to eight tokens, the
+ * one-launch GEMV (which also computes the adapter terms and the finish); on the launch stream,
+ * until `capacity` steps are recorded.
  * Under stream capture the records become event-record nodes of the graph, timing each replay.
  * events == NULL switches the recording off.  Process-wide; do not change it while calls are
  * in flight on other host threads.  Returns QLORA_ERR_INVALID_ARG for capacity < 0 or a NULL
