@@ -21,27 +21,27 @@
 //     2^-9 relative per weight, well inside the layer tolerance.
 //
 // The stream.  The codes are read in stages of 32 weight rows x 1 KB of each row (2048 columns,
-// one 3-D TMA box of eight 128-byte units), so that every row segment is one contiguous read: 128-byte
-// pieces of many rows fetched microseconds apart ran at a quarter of the HBM bandwidth.
-//   - One producer warp per CTA takes the work items of W from a launch-wide counter (so an SM
-//     that gets its data late does less of the work), issues each stage's codes by TMA, and stores the
-//     stage's int8 scale codes (loaded into registers one stage ahead) with each row's group
-//     constants; each consumer rebuilds the s'_b it needs from them (the same fmaf as the
-//     dequantization).
-//   - Eight consumer warps each take one 256-column unit (two 16-row MMA tiles) of every stage;
-//     a warp keeps x of its unit in registers for all row groups of a work item (its columns do
-//     not change).  Their sums are added across the eight warps in shared memory (fixed order)
-//     and stored as the stage's fp32 partial.
-//   - A work item is one row group and up to four consecutive slabs (the warps add its stages up
-//     in registers, and x of the next stage is loaded during the current one); the CTAs working
-//     at the same time take neighbouring row groups.
+// one 3-D TMA box of eight 128-byte units), so that every row segment is one contiguous read:
+// 128-byte pieces of many rows fetched microseconds apart ran at a quarter of the HBM bandwidth.
+//   - One producer warp per CTA takes the work items from a launch-wide counter, two items ahead
+//     (so an SM that gets its data late does less of the work), issues each stage's codes by TMA
+//     into one of four stage slots, and rebuilds the stage's block scales
+//     s'_b = fmaf(q_b, fl32(c2_g / 127), mu) (the dequantization's arithmetic) from int8 scale codes
+//     it loaded a whole stage earlier, into the slot's side area (lane = weight row).
+//   - Eight consumer warps each take one 256-column unit (two 16-row MMA tiles) of every stage.
+//     A warp loads x of the next stage's unit while it computes the current one, and adds the
+//     stages of a work item up in registers.
+//   - A work item is one row group and up to four consecutive slabs; at its end each consumer
+//     warp hands its sums to the CTA's finisher warp through a ring in the table's free
+//     half-rows, and the finisher adds the eight warps' sums (fixed order) into the item's fp32
+//     partial.
 //   - The adapter's down product U = X A^T comes first: its items (the rows of A, bf16, no decode,
 //     one slab each) are the first items of the first CTAs, so U is done early and by many CTAs at
 //     once; the term U B^T is added by the stage of each row group's last slab (bf16 B rows as
-//     the A operand).
-//   - The last slab of a row group to finish (a counter per row group) hands the row group to the
-//     CTA's finisher warp, which adds its partials in slab order (so the result is deterministic)
-//     and writes bf16 Y (or, for the rows of A, publishes bf16(s X A^T)).
+//     the A operand, loaded at the item's first stage).
+//   - The last item of a row group to be counted in (a counter per row group) finishes it: its
+//     finisher adds the row group's partials in item order (so the result is deterministic) and
+//     writes bf16 Y, or, for the rows of A, publishes bf16(s X A^T).
 // Every wait is bounded; the counters must be zero at launch (the host clears them first).
 
 namespace qlora {
@@ -298,12 +298,11 @@ __global__ void __launch_bounds__(kGvThreads, 1)
 
     if (warp == kGvProducer) {
         // ---------------------------------------------------------------- producer warp --------
-        // The stages in the order of the work items (taken two ahead): wait
-        // until the stage's slot is free, describe it (with the stage after it, whose x the
-        // consumers load ahead), issue its codes (one 3-D TMA box: 32 rows x 8 units, or a 2-D
-        // box per unit), store its raw int8 scale codes and, per row (lane = row), the two group
-        // the rebuilt block scales s'_b (lane = row), and release it.  Then load the next stage's
-        // scale codes into registers.
+        // The stages in the order of the work items (taken two ahead): wait until the stage's
+        // slot is free, describe it (with the stage after it, whose x the consumers load ahead),
+        // issue its codes (one 3-D TMA box: 32 rows x 8 units, or a 2-D box per unit), store its
+        // rebuilt block scales s'_b in the slot's side area (lane = weight row) and release it.
+        // Then load the scale codes of the stage after the next one into registers.
         // This CTA's items: first its share of the adapter items (items blockIdx.x, + gridDim.x,
         // ..., so that U is computed at once by many CTAs), then items of W from the counter.
         const int nu = a.RU * a.NS;
