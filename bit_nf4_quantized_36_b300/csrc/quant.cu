@@ -15,8 +15,9 @@ namespace qlora {
 // ---------------------------------------------------------------------------------------
 // K1: per 64-block absmax, NF4 code of every weight, two codes per byte, and the fp64 sums of
 // the 256-block groups' scales folded into aligned subtrees of the mean's pairwise tree.
-// One CTA (256 threads) per run of `run` consecutive groups; 16 threads per 64-block (float4
-// each), four blocks' loads in flight per thread; the absmax is a 16-lane max reduction.
+// One CTA (256 threads, eight per SM) per run of `run` consecutive groups; 8 threads per 64-block
+// (two float4 each, staged by cp.async three passes deep); the absmax is an 8-lane max reduction;
+// the codes are formed two weights at a time with the packed two-lane fp32 instructions.
 //
 // Code rule: thr[0..14] are the exact fp32 decision thresholds of the nearest-level rule
 // (thr[k] = smallest x in (L_k, L_k+1] with fl(L_k+1 - x) < fl(x - L_k)), so the code is the
